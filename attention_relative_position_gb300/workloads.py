@@ -1,0 +1,128 @@
+"""Seeded synthetic workloads shared by the tests, the smoke check and the benchmark.
+
+This module only draws random inputs with the shapes and distributions of the FAT5 report's
+attention benchmark (T5 encoder/decoder self-attention, head_dim 64/128, sequence 128 to 16384)
+and of padding-free packing (concatenated documents with cu_seqlens boundaries). It holds none
+of the attention arithmetic: the CUDA path and the oracle each do their own.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    seqlens: Tuple[int, ...]
+    num_heads: int
+    head_dim: int
+    qkv_std: float = 1.0
+    t5: Optional[Tuple[int, int, bool]] = None  # (num_buckets, max_distance, bidirectional)
+    alibi: bool = False
+    causal: bool = False
+    scale: float = 1.0
+    seed: int = 0
+    table_std: float = 0.5
+    description: str = ""
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.seqlens))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.seqlens)) if self.seqlens else 0
+
+    def fwd_flops(self) -> float:
+        """4 * L^2 * d per head per document, halved when causal."""
+        f = sum(4.0 * L * L * self.head_dim for L in self.seqlens) * self.num_heads
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops()
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+def lognormal_lengths(total: int, mu: float, sigma: float, lo: int, hi: int, seed: int):
+    """Document lengths round(lognormal(mu, sigma)) clipped to [lo, hi], drawn until their sum
+    reaches `total`; the last one is truncated so the sum is exactly `total`."""
+    rng = np.random.default_rng(seed)
+    out = []
+    s = 0
+    while s < total:
+        L = int(np.clip(round(float(rng.lognormal(mu, sigma))), lo, hi))
+        L = min(L, total - s)
+        out.append(L)
+        s += L
+    return tuple(out)
+
+
+def alibi_slopes(num_heads: int) -> np.ndarray:
+    """The ALiBi paper's geometric slopes 2^(-8(h+1)/H), h = 0..H-1 (caller-provided input)."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / num_heads) for h in range(num_heads)], np.float32)
+
+
+# The five benchmark workloads. Index 0 is the small case the oracle finishes in seconds;
+# index 1 (T5 encoder, batch 8 x seq 1024) is the headline benchmark line; indices 3 and 4 are
+# the long-sequence cases (seq >= 4096).
+WORKLOADS = (
+    Workload("t5enc_b1_h2_s128_d64", (128,), 2, 64, 1.0, (32, 128, True), False, False, 1.0,
+             seed=1001, description="T5 encoder, batch 1, 2 heads, seq 128, head_dim 64"),
+    Workload("t5enc_b8_h8_s1024_d64", (1024,) * 8, 8, 64, 1.0 / math.sqrt(8.0), (32, 128, True),
+             False, False, 1.0, seed=1002,
+             description="T5 encoder, batch 8, 8 heads, seq 1024, head_dim 64"),
+    Workload("t5dec_causal_varlen_16k_h12_d64",
+             lognormal_lengths(16384, 5.8, 0.8, 16, 2048, seed=1003), 12, 64, 1.0,
+             (32, 128, False), False, True, 1.0, seed=1003,
+             description="T5 decoder causal, varlen packed 16384 tokens, lognormal(5.8,0.8) "
+                         "lengths in [16,2048], 12 heads, head_dim 64"),
+    Workload("alibi_causal_b2_h16_s8192_d128", (8192,) * 2, 16, 128, 1.0, None, True, True,
+             1.0 / math.sqrt(128.0), seed=1004,
+             description="causal ALiBi, batch 2, 16 heads, seq 8192, head_dim 128"),
+    Workload("t5enc_long_b1_h12_s16384_d64", (16384,), 12, 64, 1.0, (64, 1024, True), False,
+             False, 1.0, seed=1005,
+             description="long-context T5 encoder, batch 1, 12 heads, seq 16384, head_dim 64"),
+)
+
+
+def by_name(name: str) -> Workload:
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def make_inputs(w: Workload, device: str = "cpu", with_dout: bool = True) -> dict:
+    """Draw the inputs of workload `w` on the CPU (torch generator seeded with w.seed) and move
+    them to `device`. bf16 tensors are fp32 normals rounded to nearest-even bf16."""
+    g = torch.Generator().manual_seed(w.seed)
+    T, H, d = w.total_tokens, w.num_heads, w.head_dim
+
+    def normal(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g, dtype=torch.float32) * std)
+
+    q = normal(T, H, d, std=w.qkv_std).to(torch.bfloat16)
+    k = normal(T, H, d, std=w.qkv_std).to(torch.bfloat16)
+    v = normal(T, H, d, std=w.qkv_std).to(torch.bfloat16)
+    table = None
+    if w.t5 is not None:
+        table = normal(w.t5[0], H, std=w.table_std)
+    dout = normal(T, H, d).to(torch.bfloat16) if with_dout else None
+    slopes = torch.from_numpy(alibi_slopes(H)) if w.alibi else None
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(w.seqlens)]).astype(np.int32))
+    out = dict(q=q, k=k, v=v, table=table, slopes=slopes, dout=dout, cu_seqlens=cu)
+    if device != "cpu":
+        out = {key: (t.to(device) if t is not None else None) for key, t in out.items()}
+    return out
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw bit patterns of a bf16 tensor as numpy uint16 (exact, no conversion)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,209 @@
+"""fp64 CPU oracle for attention with an in-kernel relative-position bias.
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` are the only callers. The product library never imports this package, and this
+package never imports the product library.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP); this module compiles it with gcc and
+marshals numpy arrays through ctypes. Inputs may be the exact bf16 bit patterns the GPU path
+receives (numpy ``uint16``), fp32 or fp64 arrays; all are widened exactly to fp64 here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                   os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("total_tokens", ctypes.c_int),
+        ("num_seqs", ctypes.c_int),
+        ("num_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("bias_table", ctypes.c_void_p),
+        ("num_buckets", ctypes.c_int),
+        ("max_distance", ctypes.c_int),
+        ("bidirectional", ctypes.c_int),
+        ("alibi_slopes", ctypes.c_void_p),
+        ("causal", ctypes.c_int),
+        ("softmax_scale", ctypes.c_double),
+    ]
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.POINTER(_Problem)
+        vp = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.oracle_t5_bucket.argtypes = [ctypes.c_longlong, i, i, i]
+        lib.oracle_t5_bucket.restype = i
+        lib.oracle_alibi_bias.argtypes = [ctypes.c_longlong, ctypes.c_double]
+        lib.oracle_alibi_bias.restype = ctypes.c_double
+        lib.oracle_attn_fwd.argtypes = [P, vp, vp]
+        lib.oracle_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp]
+        lib.oracle_attn_fwd_rows.argtypes = [P, i, i, vp, i, vp, vp]
+        lib.oracle_attn_bwd_rows.argtypes = [P, vp, i, i, vp, i, vp, i, vp, vp, vp, vp]
+        for f in ("oracle_attn_fwd", "oracle_attn_bwd", "oracle_attn_fwd_rows",
+                  "oracle_attn_bwd_rows", "oracle_num_threads"):
+            getattr(lib, f).restype = i
+        _lib = lib
+    return _lib
+
+
+def widen(a) -> np.ndarray:
+    """Exact fp64 copy of a uint16 array of bf16 bit patterns, or of an fp32/fp64 array."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+@dataclass
+class Problem:
+    """One packed varlen attention problem, host side.
+
+    q, k, v: [T, H, d] as bf16 bit patterns (uint16) or floats; cu_seqlens: int32 [n+1];
+    table: [nb, H] floats or None; slopes: [H] floats or None. Stored widened to fp64.
+    """
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    cu_seqlens: np.ndarray
+    table: Optional[np.ndarray] = None
+    num_buckets: int = 0
+    max_distance: int = 0
+    bidirectional: bool = True
+    slopes: Optional[np.ndarray] = None
+    causal: bool = False
+    scale: float = 1.0
+
+    def __post_init__(self):
+        self.q, self.k, self.v = widen(self.q), widen(self.k), widen(self.v)
+        self.cu_seqlens = np.ascontiguousarray(self.cu_seqlens, dtype=np.int32)
+        if self.table is not None:
+            self.table = widen(self.table)
+        if self.slopes is not None:
+            self.slopes = widen(self.slopes)
+
+    @property
+    def shape(self):
+        return self.q.shape
+
+    def _c(self) -> _Problem:
+        T, H, d = self.q.shape
+        p = _Problem()
+        p.total_tokens, p.num_seqs, p.num_heads, p.head_dim = T, len(self.cu_seqlens) - 1, H, d
+        p.cu_seqlens = self.cu_seqlens.ctypes.data
+        p.q, p.k, p.v = self.q.ctypes.data, self.k.ctypes.data, self.v.ctypes.data
+        p.bias_table = self.table.ctypes.data if self.table is not None else None
+        p.num_buckets, p.max_distance = int(self.num_buckets), int(self.max_distance)
+        p.bidirectional = int(bool(self.bidirectional))
+        p.alibi_slopes = self.slopes.ctypes.data if self.slopes is not None else None
+        p.causal = int(bool(self.causal))
+        p.softmax_scale = float(self.scale)
+        return p
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def t5_bucket(delta: int, num_buckets: int, max_distance: int, bidirectional: bool) -> int:
+    return int(_load().oracle_t5_bucket(int(delta), int(num_buckets), int(max_distance),
+                                        int(bool(bidirectional))))
+
+
+def alibi_bias(delta: int, slope: float) -> float:
+    return float(_load().oracle_alibi_bias(int(delta), float(slope)))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def attn_fwd(pb: Problem):
+    """Full forward. Returns (out fp64 [T,H,d], lse fp64 [H,T])."""
+    T, H, d = pb.shape
+    out = np.zeros((T, H, d), np.float64)
+    lse = np.full((H, T), np.nan, np.float64)
+    c = pb._c()
+    _check(_load().oracle_attn_fwd(ctypes.byref(c), out.ctypes.data, lse.ctypes.data), "fwd")
+    return out, lse
+
+
+def attn_bwd(pb: Problem, dout: np.ndarray):
+    """Full backward of sum(out*dout). Returns (dq, dk, dv, dtable-or-None), fp64."""
+    T, H, d = pb.shape
+    dout = widen(dout)
+    dq = np.zeros((T, H, d), np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    dtab = np.zeros((pb.num_buckets, H), np.float64) if pb.table is not None else None
+    c = pb._c()
+    _check(_load().oracle_attn_bwd(ctypes.byref(c), dout.ctypes.data, dq.ctypes.data,
+                                   dk.ctypes.data, dv.ctypes.data,
+                                   dtab.ctypes.data if dtab is not None else None), "bwd")
+    return dq, dk, dv, dtab
+
+
+def attn_fwd_rows(pb: Problem, doc: int, head: int, rows: Sequence[int]):
+    """out and lse for query rows (document-local positions) of one (doc, head)."""
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    d = pb.shape[2]
+    out = np.zeros((len(rows), d), np.float64)
+    lse = np.zeros(len(rows), np.float64)
+    c = pb._c()
+    _check(_load().oracle_attn_fwd_rows(ctypes.byref(c), int(doc), int(head), rows.ctypes.data,
+                                        len(rows), out.ctypes.data, lse.ctypes.data), "fwd_rows")
+    return out, lse
+
+
+def attn_bwd_rows(pb: Problem, dout: np.ndarray, doc: int, head: int, qrows: Sequence[int],
+                  krows: Sequence[int], want_dtable: bool = False):
+    """dq for query rows, dk/dv for key rows of one (doc, head) (document-local positions), and
+    optionally this (doc, head)'s contribution to the bucket gradient [nb]."""
+    dout = widen(dout)
+    qrows = np.ascontiguousarray(qrows, dtype=np.int32)
+    krows = np.ascontiguousarray(krows, dtype=np.int32)
+    d = pb.shape[2]
+    dq = np.zeros((len(qrows), d), np.float64)
+    dk = np.zeros((len(krows), d), np.float64)
+    dv = np.zeros((len(krows), d), np.float64)
+    dcol = np.zeros(pb.num_buckets, np.float64) if (want_dtable and pb.table is not None) else None
+    c = pb._c()
+    _check(_load().oracle_attn_bwd_rows(
+        ctypes.byref(c), dout.ctypes.data, int(doc), int(head), qrows.ctypes.data, len(qrows),
+        krows.ctypes.data, len(krows), dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+        dcol.ctypes.data if dcol is not None else None), "bwd_rows")
+    return dq, dk, dv, dcol
