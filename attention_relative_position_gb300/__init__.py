@@ -1,0 +1,221 @@
+"""GB300-native fused attention with an in-kernel relative-position bias (T5 buckets, ALiBi),
+padding-free varlen packing, forward and backward.
+
+This module is a thin ctypes binding over libfatattn.so (C ABI in include/fat_attn.h): it only
+marshals torch tensors into pointers and sizes. Every step of the computation runs in the CUDA
+kernels of the library; there is no other implementation to fall back to, and a missing or
+unloadable library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "FatAttnError", "load", "fat_attn_fwd", "fat_attn_bwd", "fat_attn_bwd_workspace_size",
+    "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
+    "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfatattn.so")
+
+FAT_DEVERR_TIMEOUT_FWD = 1
+FAT_DEVERR_TIMEOUT_BWD = 2
+FAT_DEVERR_SEQLENS = 4
+
+
+class FatAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed: {code} ({fat_attn_strerror(code)})")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("max_seqlen", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("stream", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libfatattn.so (built by __graft_entry__.build()). Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} not found: build the CUDA library first (python -c 'import __graft_entry__ as g; "
+            f"g.build()')")
+    lib = ctypes.CDLL(p)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    S = ctypes.POINTER(_Shape)
+    lib.fat_attn_fwd.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp]
+    lib.fat_attn_fwd.restype = i32
+    lib.fat_attn_bwd_workspace_size.argtypes = [S]
+    lib.fat_attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fat_attn_bwd.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp,
+                                 vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.fat_attn_bwd.restype = i32
+    lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.fat_attn_get_device_error.restype = i32
+    lib.fat_attn_strerror.argtypes = [i32]
+    lib.fat_attn_strerror.restype = ctypes.c_char_p
+    lib.fat_attn_bucket_thresholds.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_int32),
+                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.fat_attn_bucket_thresholds.restype = i32
+    lib.fat_attn_debug_buckets.argtypes = [ctypes.c_longlong, i32, i32, i32, i32, vp, vp]
+    lib.fat_attn_debug_buckets.restype = i32
+    lib.fat_attn_debug_set_watchdog.argtypes = [ctypes.c_longlong, i32]
+    lib.fat_attn_debug_set_watchdog.restype = None
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _shape(total_tokens, num_seqs, max_seqlen, num_heads, head_dim, stream_ptr) -> _Shape:
+    return _Shape(int(total_tokens), int(num_seqs), int(max_seqlen), int(num_heads),
+                  int(head_dim), stream_ptr)
+
+
+def _check_tensor(name, t, dtype, ndim=None):
+    import torch
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def fat_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, bias_table=None, num_buckets: int = 0,
+                 max_distance: int = 0, bidirectional: bool = True, alibi_slopes=None,
+                 causal: bool = False, softmax_scale: float = 1.0, out=None, lse=None,
+                 stream=None):
+    """Forward pass. q, k, v: bf16 [T, H, d] (CUDA, contiguous); cu_seqlens: int32 [n+1] (CUDA).
+    Returns (out bf16 [T, H, d], lse fp32 [H, T])."""
+    import torch
+    lib = load()
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_tensor(name, t, torch.bfloat16, 3)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, 1)
+    _check_tensor("bias_table", bias_table, torch.float32)
+    _check_tensor("alibi_slopes", alibi_slopes, torch.float32)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
+    rc = lib.fat_attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                          int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                          _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                          float(softmax_scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_fwd")
+    return out, lse
+
+
+def fat_attn_bwd_workspace_size(total_tokens: int, num_heads: int, head_dim: int) -> int:
+    lib = load()
+    sh = _shape(total_tokens, 1, 1, num_heads, head_dim, None)
+    return int(lib.fat_attn_bwd_workspace_size(ctypes.byref(sh)))
+
+
+def fat_attn_bwd(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, bias_table=None,
+                 num_buckets: int = 0, max_distance: int = 0, bidirectional: bool = True,
+                 alibi_slopes=None, causal: bool = False, softmax_scale: float = 1.0,
+                 want_dbias: bool = True, workspace=None, dq=None, dk=None, dv=None,
+                 dbias_table=None, stream=None):
+    """Backward pass of sum(out * dout). Returns (dq, dk, dv, dbias_table or None)."""
+    import torch
+    lib = load()
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check_tensor(name, t, torch.bfloat16, 3)
+    _check_tensor("lse", lse, torch.float32, 2)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, 1)
+    _check_tensor("bias_table", bias_table, torch.float32)
+    _check_tensor("alibi_slopes", alibi_slopes, torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dbias_table is None and want_dbias and bias_table is not None:
+        dbias_table = torch.empty_like(bias_table)
+    sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
+    need = int(lib.fat_attn_bwd_workspace_size(ctypes.byref(sh)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.fat_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                          int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                          _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                          float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
+                          _ptr(workspace), int(workspace.numel()), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(dbias_table))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bwd")
+    return dq, dk, dv, dbias_table
+
+
+def fat_attn_get_device_error(stream=None, device=None) -> int:
+    """Synchronise, read and clear the device error word; returns its bits (0 = no error)."""
+    lib = load()
+    bits = ctypes.c_int(0)
+    rc = lib.fat_attn_get_device_error(_stream_ptr(stream, device), ctypes.byref(bits))
+    if rc not in (0, -6):
+        raise FatAttnError(rc, "fat_attn_get_device_error")
+    return int(bits.value)
+
+
+def fat_attn_strerror(code: int) -> str:
+    return load().fat_attn_strerror(int(code)).decode()
+
+
+def fat_attn_bucket_thresholds(num_buckets: int, max_distance: int, bidirectional: bool):
+    """Host-side thresholds the kernels compare distances with: (thresholds list, saturation)."""
+    lib = load()
+    arr = (ctypes.c_int32 * 64)()
+    cnt, sat = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib.fat_attn_bucket_thresholds(int(num_buckets), int(max_distance),
+                                        int(bool(bidirectional)), arr, ctypes.byref(cnt),
+                                        ctypes.byref(sat))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bucket_thresholds")
+    return list(arr[: cnt.value]), int(sat.value)
+
+
+def fat_attn_debug_buckets(delta_lo: int, n: int, num_buckets: int, max_distance: int,
+                           bidirectional: bool, out=None, stream=None, device="cuda"):
+    """Device-side T5 bucket ids for delta_lo .. delta_lo+n-1 (int32 CUDA tensor)."""
+    import torch
+    lib = load()
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=device)
+    rc = lib.fat_attn_debug_buckets(int(delta_lo), int(n), int(num_buckets), int(max_distance),
+                                    int(bool(bidirectional)), _ptr(out),
+                                    _stream_ptr(stream, out.device))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_debug_buckets")
+    return out
+
+
+def fat_attn_debug_set_watchdog(timeout_ns: int = 0, flags: int = 0) -> None:
+    load().fat_attn_debug_set_watchdog(int(timeout_ns), int(flags))

@@ -1,0 +1,414 @@
+// fat_attn_api.cu -- host side of the C ABI declared in include/fat_attn.h: argument checks,
+// exact T5 bucket thresholds, tensor-map encoding, the device error word, and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/fat_attn_debug.h"
+#include "fat_attn_internal.cuh"
+
+// One error word per GPU that loads the library (file-scope device variable; never allocated).
+__device__ int g_fat_device_error;
+
+namespace fat {
+namespace {
+
+std::mutex g_mu;
+long long g_timeout_ns = kDefaultTimeoutNs;
+int g_debug_flags = 0;
+int *g_err_ptr[128] = {nullptr};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_error_ptr(int **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return FAT_ECUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fat_device_error) != cudaSuccess) return FAT_ECUDA;
+    g_err_ptr[dev] = static_cast<int *>(ptr);
+  }
+  *out = g_err_ptr[dev];
+  return FAT_OK;
+}
+
+// ---- exact thresholds: unsigned big integers, base 2^32 ------------------------------------
+struct Big {
+  std::vector<uint32_t> w;  // little-endian limbs
+  explicit Big(uint32_t v) { w.push_back(v); }
+  void mul(uint32_t m) {
+    uint64_t carry = 0;
+    for (auto &x : w) {
+      const uint64_t cur = (uint64_t)x * m + carry;
+      x = (uint32_t)cur;
+      carry = cur >> 32;
+    }
+    if (carry) w.push_back((uint32_t)carry);
+  }
+  void trim() {
+    while (w.size() > 1 && w.back() == 0) w.pop_back();
+  }
+};
+int big_cmp(Big a, Big b) {
+  a.trim();
+  b.trim();
+  if (a.w.size() != b.w.size()) return a.w.size() < b.w.size() ? -1 : 1;
+  for (size_t i = a.w.size(); i-- > 0;)
+    if (a.w[i] != b.w[i]) return a.w[i] < b.w[i] ? -1 : 1;
+  return 0;
+}
+// bucket offset of distance n is at least me + t  <=>  n^E * me^t >= md^t * me^E
+bool reaches(long long n, int me, int E, int md, int t) {
+  Big lhs(1), rhs(1);
+  for (int i = 0; i < E; ++i) lhs.mul((uint32_t)n);
+  for (int i = 0; i < t; ++i) lhs.mul((uint32_t)me);
+  for (int i = 0; i < t; ++i) rhs.mul((uint32_t)md);
+  for (int i = 0; i < E; ++i) rhs.mul((uint32_t)me);
+  return big_cmp(lhs, rhs) >= 0;
+}
+
+int check_buckets(int nb, int md, int bidir, int *nbh_out) {
+  if (bidir && (nb % 2)) return FAT_EINVAL_BUCKETS;
+  const int nbh = bidir ? nb / 2 : nb;
+  if (nbh < 2 || nbh > 128) return FAT_EINVAL_BUCKETS;
+  if (md <= nbh / 2) return FAT_EINVAL_BUCKETS;
+  *nbh_out = nbh;
+  return FAT_OK;
+}
+
+int thresholds(int nbh, int md, int32_t *thr, int *count, int *sat) {
+  const int me = nbh / 2, E = nbh - me;
+  for (int t = 1; t < E; ++t) {
+    long long lo = me, hi = md;  // predicate false below the answer, true at md
+    while (lo < hi) {
+      const long long mid = lo + (hi - lo) / 2;
+      if (reaches(mid, me, E, md, t))
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    thr[t - 1] = (int32_t)lo;
+  }
+  *count = E - 1;
+  *sat = E >= 2 ? thr[E - 2] : me;
+  return FAT_OK;
+}
+
+int fill_bias(BiasParams *b, const float *table, int nb, int md, int bidir, const float *slopes) {
+  *b = BiasParams{};
+  b->table = table;
+  b->slopes = slopes;
+  b->has_bias = (table != nullptr) || (slopes != nullptr);
+  if (table) {
+    int nbh = 0;
+    int rc = check_buckets(nb, md, bidir, &nbh);
+    if (rc) return rc;
+    b->nb = nb;
+    b->bidir = bidir ? 1 : 0;
+    b->nbh = nbh;
+    b->me = nbh / 2;
+    int sat = 0;
+    thresholds(nbh, md, b->thr, &b->n_thr, &sat);
+    b->sat_neg = sat;
+    b->sat_pos = bidir ? sat : 0;
+  }
+  if (b->has_bias) {
+    // a tile spans at most 127 + 127 distinct deltas beyond its corner
+    b->lut_lo = -b->sat_neg - 253;
+    b->lut_len = b->sat_pos + b->sat_neg + 507;
+  }
+  return FAT_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int check_shape(const fat_shape_t *sh) {
+  if (!sh) return FAT_EINVAL_NULL;
+  if (sh->total_tokens < 0 || sh->num_seqs < 0 || sh->max_seqlen < 0 || sh->num_heads <= 0)
+    return FAT_EINVAL_SHAPE;
+  if (sh->head_dim != 64 && sh->head_dim != 128) return FAT_EINVAL_SHAPE;
+  if ((long long)sh->total_tokens * sh->num_heads * sh->head_dim > (1LL << 40)) return FAT_EINVAL_SHAPE;
+  if (sh->num_heads > 65535 || sh->num_seqs > 65535) return FAT_EUNSUPPORTED;
+  return FAT_OK;
+}
+
+int cuda_rc(int e) { return e == 0 ? FAT_OK : FAT_ECUDA; }
+
+}  // namespace
+
+int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return -1;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+}  // namespace fat
+
+using namespace fat;
+
+// ---- preprocessing and finishing kernels of the backward -----------------------------------
+// D[h, t] = sum_c dout[t, h, c] * out[t, h, c] (fp32), the dQ accumulator zeroed, and the
+// table gradient zeroed. One warp per (token, head) row; memory bound.
+template <int D>
+__global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ out,
+                                                           const __nv_bfloat16 *__restrict__ dout,
+                                                           float *__restrict__ dvec,
+                                                           float *__restrict__ dq_acc,
+                                                           float *__restrict__ dbias, int nbias,
+                                                           int T, int H) {
+  constexpr int PER = D / 32;  // bf16 per lane
+  const int lane = threadIdx.x & 31;
+  const long long nrows = (long long)T * H;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  if (dbias && warp0 == 0)
+    for (int i = lane; i < nbias; i += 32) dbias[i] = 0.f;
+  for (long long row = warp0; row < nrows; row += nwarps) {
+    const long long t = row / H, h = row % H;
+    const __nv_bfloat16 *o = out + row * D + lane * PER;
+    const __nv_bfloat16 *g = dout + row * D + lane * PER;
+    float acc = 0.f;
+    if (PER == 2) {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o);
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(g);
+      acc = __bfloat162float(a.x) * __bfloat162float(b.x) + __bfloat162float(a.y) * __bfloat162float(b.y);
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2 *>(o);
+      const uint2 b = *reinterpret_cast<const uint2 *>(g);
+      const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        acc += __bfloat162float(a2[i].x) * __bfloat162float(b2[i].x) +
+               __bfloat162float(a2[i].y) * __bfloat162float(b2[i].y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dvec[h * T + t] = acc;
+    float *z = dq_acc + row * D + lane * PER;
+    if (PER == 2)
+      *reinterpret_cast<float2 *>(z) = make_float2(0.f, 0.f);
+    else
+      *reinterpret_cast<float4 *>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// dq = bf16(dq_acc * softmax_scale), 4 elements per thread step.
+__global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const float4 *__restrict__ acc,
+                                                             uint2 *__restrict__ dq, float scale,
+                                                             long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 a = acc[i];
+    uint2 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    dq[i] = o;
+  }
+}
+
+// ---- C ABI -------------------------------------------------------------------------------------
+extern "C" {
+
+const char *fat_attn_strerror(int code) {
+  switch (code) {
+    case FAT_OK: return "ok";
+    case FAT_EINVAL_NULL: return "a required pointer is NULL";
+    case FAT_EINVAL_SHAPE: return "invalid shape, head_dim or pointer alignment";
+    case FAT_EINVAL_BUCKETS: return "invalid T5 bucket arguments";
+    case FAT_ECUDA: return "a CUDA call failed";
+    case FAT_EUNSUPPORTED: return "unsupported argument combination";
+    case FAT_EDEVICE: return "the device error word was set";
+    default: return "unknown error code";
+  }
+}
+
+int fat_attn_bucket_thresholds(int num_buckets, int max_distance, int bidirectional,
+                               int32_t *thr, int *count, int *saturation) {
+  if (!thr || !count || !saturation) return FAT_EINVAL_NULL;
+  int nbh = 0;
+  int rc = check_buckets(num_buckets, max_distance, bidirectional, &nbh);
+  if (rc) return rc;
+  return thresholds(nbh, max_distance, thr, count, saturation);
+}
+
+void fat_attn_debug_set_watchdog(long long timeout_ns, int flags) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timeout_ns = timeout_ns > 0 ? timeout_ns : kDefaultTimeoutNs;
+  g_debug_flags = flags;
+}
+
+int fat_attn_get_device_error(void *stream, int *bits) {
+  int *ep = nullptr;
+  int rc = device_error_ptr(&ep);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FAT_ECUDA;
+  if (cudaMemcpyAsync(&host, ep, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FAT_ECUDA;
+  if (cudaMemsetAsync(ep, 0, sizeof(int), s) != cudaSuccess) return FAT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FAT_ECUDA;
+  if (bits) *bits = host;
+  return host ? FAT_EDEVICE : FAT_OK;
+}
+
+int fat_attn_fwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                 const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                 const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                 float softmax_scale, void *out, float *lse) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!q || !k || !v || !cu_seqlens || !out) return FAT_EINVAL_NULL;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) ||
+      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
+      misaligned(lse))
+    return FAT_EINVAL_SHAPE;
+  FwdParams p{};
+  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (fwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  if (sh->total_tokens == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0) return FAT_OK;
+  rc = device_error_ptr(&p.err);
+  if (rc) return rc;
+  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens};
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    p.timeout_ns = g_timeout_ns;
+    p.debug_flags = g_debug_flags;
+  }
+  return cuda_rc(launch_fwd(p, sh->head_dim, sh->max_seqlen, q, k, v,
+                            static_cast<cudaStream_t>(sh->stream)));
+}
+
+size_t fat_attn_bwd_workspace_size(const fat_shape_t *sh) {
+  if (check_shape(sh)) return 0;
+  const size_t T = (size_t)sh->total_tokens, H = (size_t)sh->num_heads, d = (size_t)sh->head_dim;
+  const size_t a = (T * H * d * 4 + 255) & ~(size_t)255;
+  const size_t b = (T * H * 4 + 255) & ~(size_t)255;
+  return a + b;
+}
+
+int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                 const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                 const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                 float softmax_scale, const void *out, const float *lse, const void *dout,
+                 void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
+                 float *dbias_table) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!q || !k || !v || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv)
+    return FAT_EINVAL_NULL;
+  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
+      misaligned(dq) || misaligned(dk) || misaligned(dv) || misaligned(lse) ||
+      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
+      misaligned(dbias_table) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FAT_EINVAL_SHAPE;
+  BwdParams p{};
+  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (bwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  const size_t need = fat_attn_bwd_workspace_size(sh);
+  if (!workspace && need) return FAT_EINVAL_NULL;
+  if (workspace_bytes < need) return FAT_EINVAL_SHAPE;
+  cudaStream_t stream = static_cast<cudaStream_t>(sh->stream);
+  const int T = sh->total_tokens, H = sh->num_heads, d = sh->head_dim;
+  if (T == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0) {
+    if (dbias_table && num_buckets > 0)
+      return cuda_rc(cudaMemsetAsync(dbias_table, 0, sizeof(float) * num_buckets * H, stream));
+    return FAT_OK;
+  }
+  rc = device_error_ptr(&p.err);
+  if (rc) return rc;
+  float *dq_acc = static_cast<float *>(workspace);
+  float *dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          (((size_t)T * H * d * 4 + 255) & ~(size_t)255));
+  // 1) D = rowsum(dout * out), zero the dQ accumulator and the table gradient
+  const long long rows = (long long)T * H;
+  const int prep_blocks = (int)std::min<long long>((rows + 7) / 8, 152LL * 16);
+  if (d == 64)
+    fat_bwd_prep_kernel<64><<<prep_blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), dvec,
+        dq_acc, dbias_table, dbias_table ? num_buckets * H : 0, T, H);
+  else
+    fat_bwd_prep_kernel<128><<<prep_blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), dvec,
+        dq_acc, dbias_table, dbias_table ? num_buckets * H : 0, T, H);
+  if (cudaGetLastError() != cudaSuccess) return FAT_ECUDA;
+  // 2) main kernel: one CTA per (document, head, 128-key tile)
+  p.seq = SeqParams{cu_seqlens, sh->num_seqs, H, T};
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.scale = softmax_scale;
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.dbias = dbias_table;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    p.timeout_ns = g_timeout_ns;
+    p.debug_flags = g_debug_flags;
+  }
+  rc = cuda_rc(launch_bwd(p, d, sh->max_seqlen, q, k, v, out, dout, stream));
+  if (rc) return rc;
+  // 3) dq = bf16(scale * dQ accumulator)
+  const long long n4 = rows * d / 4;
+  const int fin_blocks = (int)std::min<long long>((n4 + 255) / 256, 152LL * 16);
+  fat_bwd_finish_kernel<<<fin_blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(dq_acc),
+                                                        static_cast<uint2 *>(dq), softmax_scale,
+                                                        n4);
+  return cudaGetLastError() == cudaSuccess ? FAT_OK : FAT_ECUDA;
+}
+
+int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,
+                           int bidirectional, int32_t *out_dev, void *stream) {
+  if (!out_dev) return FAT_EINVAL_NULL;
+  if (n < 0) return FAT_EINVAL_SHAPE;
+  if (delta_lo < -(1LL << 30) || delta_lo + n > (1LL << 30)) return FAT_EINVAL_SHAPE;
+  BiasParams b{};
+  static const float dummy = 0.f;
+  int rc = fill_bias(&b, &dummy, num_buckets, max_distance, bidirectional, nullptr);
+  if (rc) return rc;
+  if (n == 0) return FAT_OK;
+  return cuda_rc(launch_debug_buckets(b, delta_lo, n, out_dev, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace fat {
+__global__ void fat_debug_buckets_kernel(const BiasParams b, long long lo, int n, int32_t *out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = t5_bucket_dev((int)(lo + i), b);
+}
+int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
+                         cudaStream_t stream) {
+  fat_debug_buckets_kernel<<<(n + 255) / 256, 256, 0, stream>>>(b, lo, n, out);
+  return (int)cudaGetLastError();
+}
+}  // namespace fat

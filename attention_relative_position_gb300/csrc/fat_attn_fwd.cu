@@ -1,0 +1,420 @@
+// fat_attn_fwd.cu -- forward kernel: fused attention with an in-kernel relative-position bias.
+//
+// FAT5 report, "Noyau CUDA" section, second kernel version: Q, K, V are brought from HBM to
+// on-chip memory, S = Q K^T, S' = S + (bias built on the fly from relative positions),
+// P = softmax(S') computed cumulatively (online), O = P V, and O is written back once.
+//
+// GB300 design (one CTA = one document x head x 256 query rows = two 128-row Q tiles):
+//   warp 8      TMA producer: Q tiles once, K/V tiles through an NS-stage shared-memory ring.
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma,
+//               accumulators in tensor memory (TMEM); P_t is read from TMEM where the softmax
+//               warps wrote it over S_t.
+//   warps 0-7   two softmax warpgroups, one per Q tile; thread i owns row i of its tile (TMEM
+//               lane i), so row max/sum need no shuffles. Bias: closed form on tiles that lie
+//               beyond the T5 saturation distance, a per-CTA lookup table over delta on the rest.
+//               The running max is only raised (and O rescaled in TMEM) when it grows by more
+//               than 2^8, which keeps P <= 256 and leaves the final result exact.
+// While one warpgroup computes its softmax, the tensor cores run the other tile's MMAs.
+#include "fat_attn_internal.cuh"
+
+namespace fat {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int DB = D / 64;           // 64-channel blocks (one 128-byte swizzle row)
+  static constexpr int BLK = 128 * 128;       // bytes: 128 rows x 64 bf16
+  static constexpr int TILE = DB * BLK;       // bytes: 128 rows x D bf16
+  static constexpr int NS = (D == 64) ? 3 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int OFF_LUT = OFF_BAR + 256;
+  static constexpr int NTHREADS = 320;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major), K (K-major)
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V (MN-major)
+};
+
+size_t fwd_smem_bytes(int head_dim, int lut_len) {
+  size_t base = head_dim == 64 ? (size_t)FwdCfg<64>::OFF_LUT : (size_t)FwdCfg<128>::OFF_LUT;
+  return 1024 + base + (size_t)lut_len * 4;
+}
+
+// Load S row chunk by chunk from TMEM, form x = S * scale_log2 + bias (log2 units), apply the
+// mask, and return the row maximum.
+//   MODE 0: bias = rowc (constant over the tile)
+//   MODE 1: bias = rowc + kk * j (linear in the key index)
+//   MODE 2: bias = lut_row[j]
+template <int MODE, bool MASK>
+__device__ __forceinline__ float fwd_logits(uint32_t tS, float (&x)[128], float scale_log2,
+                                            float rowc, float kk, const float *lut_row, int lim) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t raw[32];
+    tmem_ld32(tS + c * 32, raw);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int j = c * 32 + i;
+      float b;
+      if (MODE == 0)
+        b = rowc;
+      else if (MODE == 1)
+        b = fmaf(kk, (float)j, rowc);
+      else
+        b = lut_row[j];
+      float v = fmaf(__uint_as_float(raw[i]), scale_log2, b);
+      if (MASK) v = (j < lim) ? v : -INFINITY;
+      x[j] = v;
+      mx[i & 3] = fmaxf(mx[i & 3], v);
+    }
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+template <int D>
+__global__ void __maxnreg__(200)
+    fat_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int doc = blockIdx.z, h = blockIdx.y;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first when causal
+  const int T = p.seq.total_tokens, H = p.seq.num_heads;
+
+  const int seq_start = __ldg(p.seq.cu_seqlens + doc);
+  const int seq_end = __ldg(p.seq.cu_seqlens + doc + 1);
+  if (seq_start < 0 || seq_end > T || seq_end < seq_start) {
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    return;
+  }
+  const int L = seq_end - seq_start;
+  const int q0 = qb * 256;
+  if (q0 >= L) return;  // whole CTA, before any barrier or TMEM allocation
+  const int ntile = (q0 + 128 < L) ? 2 : 1;
+  const int nkv_all = (L + 127) >> 7;
+  const int nkv0 = p.causal ? min((q0 >> 7) + 1, nkv_all) : nkv_all;
+  const int nkv1 = ntile == 2 ? (p.causal ? min((q0 >> 7) + 2, nkv_all) : nkv_all) : 0;
+  const int nkv_max = max(nkv0, nkv1);
+
+  uint8_t *sQ = sm + C::OFF_Q, *sK = sm + C::OFF_K, *sV = sm + C::OFF_V;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = q_full + 1;
+  uint64_t *v_full = k_full + C::NS;
+  uint64_t *k_empty = v_full + C::NS;
+  uint64_t *v_empty = k_empty + C::NS;
+  uint64_t *s_full = v_empty + C::NS;
+  uint64_t *p_ready = s_full + 2;
+  uint64_t *o_ready = p_ready + 2;
+  uint64_t *mma_done = o_ready + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_ready + t, 128);
+      mbar_init(o_ready + t, 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS)
+    lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_k[C::NS], last_v[C::NS];
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) last_k[s] = last_v[s] = -1;
+      bool q_issued = false;
+      if (!(p.debug_flags & 1)) {
+        mbar_arrive_expect_tx(q_full, ntile * C::TILE);
+        for (int t = 0; t < ntile; ++t)
+          for (int b = 0; b < C::DB; ++b)
+            tma_load_3d(&tm_q, q_full, sQ + t * C::TILE + b * C::BLK, 64 * b, h,
+                        seq_start + q0 + 128 * t);
+        q_issued = true;
+        for (int j = 0; j < nkv_max; ++j) {
+          const int s = j % C::NS, u = j / C::NS;
+          if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, wd)) break;
+          mbar_arrive_expect_tx(k_full + s, C::TILE);
+          for (int b = 0; b < C::DB; ++b)
+            tma_load_3d(&tm_k, k_full + s, sK + s * C::TILE + b * C::BLK, 64 * b, h,
+                        seq_start + 128 * j);
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == s) last_k[x] = u;
+          if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, wd)) break;
+          mbar_arrive_expect_tx(v_full + s, C::TILE);
+          for (int b = 0; b < C::DB; ++b)
+            tma_load_3d(&tm_v, v_full + s, sV + s * C::TILE + b * C::BLK, 64 * b, h,
+                        seq_start + 128 * j);
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == s) last_v[x] = u;
+        }
+      }
+      // teardown: every copy this thread issued has landed before the CTA exits
+      if (q_issued) mbar_wait_teardown(q_full, 0, kTeardownNs);
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) {
+        if (last_k[s] >= 0) mbar_wait_teardown(k_full + s, last_k[s] & 1, kTeardownNs);
+        if (last_v[s] >= 0) mbar_wait_teardown(v_full + s, last_v[s] & 1, kTeardownNs);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      auto issue_S = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+          const uint64_t a = sw128_desc(sQa + t * C::TILE + off, 16, 1024);
+          const uint64_t b = sw128_desc(sKa + s * C::TILE + off, 16, 1024);
+          mma_bf16_ss(tmem + 128 * t, a, b, C::IDESC_S, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int t, int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t b = sw128_desc(sVa + s * C::TILE + kk * 2048, C::BLK, 1024);
+          mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, b, C::IDESC_PV,
+                      (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, wd) && mbar_wait(k_full, 0, wd);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < ntile; ++t) {
+          issue_S(t, 0);
+          mma_commit(s_full + t);
+        }
+        mma_commit(k_empty);
+      }
+      for (int j = 0; ok && j < nkv_max; ++j) {
+        const int s = j % C::NS, u = j / C::NS;
+        const int jn = j + 1, sn = jn % C::NS, un = jn / C::NS;
+        if (!mbar_wait(v_full + s, u & 1, wd)) {
+          ok = false;
+          break;
+        }
+        bool k_next = false;
+        for (int t = 0; t < ntile && ok; ++t) {
+          const int nk = t == 0 ? nkv0 : nkv1;
+          if (j >= nk) continue;
+          if (!mbar_wait(p_ready + t, j & 1, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_PV(t, s, j > 0);
+          mma_commit(o_ready + t);
+          if (jn < nk) {
+            if (!k_next) {
+              if (!mbar_wait(k_full + sn, un & 1, wd)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_S(t, sn);
+            mma_commit(s_full + t);
+          }
+        }
+        if (!ok) break;
+        mma_commit(v_empty + s);
+        if (k_next) mma_commit(k_empty + sn);
+      }
+      mma_commit(mma_done);
+      mbar_wait_teardown(mma_done, 0, kTeardownNs);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    if (t < ntile) {
+      const int nk = t == 0 ? nkv0 : nkv1;
+      const int r = tid & 127;
+      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_off + 128 * t;
+      const uint32_t tO = tmem + lane_off + 256 + 128 * t;
+      const int qs = q0 + 128 * t;  // document-local first row of this tile
+      const int qrow = qs + r;
+      const FarBias fb = far_bias_dev(h, H, p.bias);
+      const bool has_slopes = p.bias.slopes != nullptr;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nk; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full + t, j & 1, wd));
+        if (!ok) break;
+        tc_fence_after();
+        const int ks = 128 * j;
+        const int d0 = ks - qs;  // delta of (row 0, key 0) of the tile
+        const bool need_mask = (ks + 128 > L) || (p.causal && d0 + 127 > 0);
+        const int lim = min(L - ks, p.causal ? (qrow - ks + 1) : 128);
+        int mode;
+        float rowc = 0.f, kk = 0.f;
+        if (!p.bias.has_bias) {
+          mode = 0;
+        } else if (d0 - 127 >= p.bias.sat_pos) {
+          kk = fb.k_pos;
+          rowc = fmaf(fb.k_pos, (float)(d0 - r), fb.c_pos);
+          mode = has_slopes ? 1 : 0;
+        } else if (d0 + 127 <= -p.bias.sat_neg) {
+          kk = fb.k_neg;
+          rowc = fmaf(fb.k_neg, (float)(d0 - r), fb.c_neg);
+          mode = has_slopes ? 1 : 0;
+        } else {
+          mode = 2;
+        }
+        const float *lut_row = lut + (d0 - r - p.bias.lut_lo);
+        float x[128];
+        float mx;
+        if (mode == 0)
+          mx = need_mask ? fwd_logits<0, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
+                         : fwd_logits<0, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+        else if (mode == 1)
+          mx = need_mask ? fwd_logits<1, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
+                         : fwd_logits<1, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+        else
+          mx = need_mask ? fwd_logits<2, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
+                         : fwd_logits<2, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+
+        if (j == 0) {
+          m = mx;
+        } else {
+          const bool need = mx > m + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            // O holds sum_{i<j} P_i V_i relative to the old max: rescale it once PV_{j-1} is done
+            ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (j - 1) & 1, wd));
+            if (!ok) break;
+            tc_fence_after();
+            const float f = need ? ex2(m - mx) : 1.0f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+              tmem_st32(tO + c * 32, o);
+            }
+            if (need) {
+              l *= f;
+              m = mx;
+            }
+          }
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = ex2(x[c * 32 + 2 * i] - m_use);
+            const float b = ex2(x[c * 32 + 2 * i + 1] - m_use);
+            sum[i & 3] += a + b;
+            pk[i] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tS + c * 16, pk);  // P (bf16 pairs) over the first 64 columns of S
+        }
+        l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready + t);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (nk - 1) & 1, wd));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const bool valid = qrow < L;
+        __nv_bfloat16 *orow = p.out + ((size_t)(seq_start + qrow) * H + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid && p.lse != nullptr) {
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          p.lse[(size_t)h * T + seq_start + qrow] =
+              l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
+               const void *v, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  if (make_tmap_thd(&mq, q, T, H, head_dim, 128) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
+      make_tmap_thd(&mv, v, T, H, head_dim, 128))
+    return (int)cudaErrorInvalidValue;
+  const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
+  dim3 grid((max_seqlen + 255) / 256, H, p.seq.num_seqs);
+  cudaError_t e;
+  if (head_dim == 64) {
+    e = cudaFuncSetAttribute(fat_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e == cudaSuccess)
+      fat_fwd_kernel<64><<<grid, FwdCfg<64>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
+  } else {
+    e = cudaFuncSetAttribute(fat_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e == cudaSuccess)
+      fat_fwd_kernel<128><<<grid, FwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
+  }
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaGetLastError();
+}
+
+}  // namespace fat

@@ -1,0 +1,131 @@
+// fat_attn_internal.cuh -- parameter blocks and device helpers shared by the forward and
+// backward kernels of the relative-position attention library (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fat_attn.h"
+#include "sm103_ptx.cuh"
+
+namespace fat {
+
+constexpr int kMaxThresholds = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kSmemLimit = 232448;           // 227 KB of dynamic shared memory per block
+constexpr long long kDefaultTimeoutNs = 4000000000LL;
+constexpr long long kTeardownNs = 200000000LL;
+
+// How the additive bias of relative position delta = k - q is formed.
+//   T5 part: table[bucket(delta), h]; the bucket is a pure integer function of delta: exact
+//            region n < me, then the number of host-computed thresholds <= n.
+//   ALiBi part: -slope_h * |delta|.
+// Tiles whose deltas all lie at or beyond the saturation distance on one side get the bias in
+// closed form (constant T5 part + linear ALiBi part); the other tiles read a per-block lookup
+// table over delta in [lut_lo, lut_lo + lut_len).
+struct BiasParams {
+  const float *table;   // [nb, H] fp32 or nullptr
+  const float *slopes;  // [H] fp32 or nullptr
+  int nb, bidir, nbh, me;
+  int n_thr;
+  int thr[kMaxThresholds];
+  int sat_pos;  // every delta >= sat_pos has the same T5 bucket (and |delta| = delta)
+  int sat_neg;  // every delta <= -sat_neg has the same T5 bucket (and |delta| = -delta)
+  int lut_lo, lut_len;
+  int has_bias;
+};
+
+struct SeqParams {
+  const int32_t *cu_seqlens;
+  int num_seqs, num_heads, total_tokens;
+};
+
+__device__ __forceinline__ int t5_bucket_dev(int delta, const BiasParams &b) {
+  int off = 0, n;
+  if (b.bidir) {
+    off = delta > 0 ? b.nbh : 0;
+    n = delta < 0 ? -delta : delta;
+  } else {
+    n = delta < 0 ? -delta : 0;
+  }
+  if (n < b.me) return off + n;
+  int t = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxThresholds; ++i) t += (i < b.n_thr && n >= b.thr[i]) ? 1 : 0;
+  return off + b.me + t;
+}
+
+// Bias of relative position `delta` for head h, in log2 units (natural bias * log2(e)).
+__device__ __forceinline__ float bias_log2_dev(int delta, int h, int H, const BiasParams &b) {
+  float v = 0.f;
+  if (b.table) v += __ldg(b.table + (size_t)t5_bucket_dev(delta, b) * H + h);
+  if (b.slopes) v -= __ldg(b.slopes + h) * (float)(delta < 0 ? -delta : delta);
+  return v * kLog2e;
+}
+
+// Closed-form bias on the far sides, in log2 units: bias(delta) = c + k * delta.
+struct FarBias {
+  float c_pos, k_pos, c_neg, k_neg;
+};
+__device__ __forceinline__ FarBias far_bias_dev(int h, int H, const BiasParams &b) {
+  FarBias f{0.f, 0.f, 0.f, 0.f};
+  if (b.table) {
+    f.c_pos = __ldg(b.table + (size_t)t5_bucket_dev(b.sat_pos, b) * H + h) * kLog2e;
+    f.c_neg = __ldg(b.table + (size_t)t5_bucket_dev(-b.sat_neg, b) * H + h) * kLog2e;
+  }
+  if (b.slopes) {
+    const float s = __ldg(b.slopes + h) * kLog2e;
+    f.k_pos = -s;
+    f.k_neg = s;
+  }
+  return f;
+}
+
+// ---------------------------------------------------------------------------------------------
+// host-side launch descriptors (filled by the API layer)
+// ---------------------------------------------------------------------------------------------
+struct FwdParams {
+  SeqParams seq;
+  BiasParams bias;
+  int causal;
+  float scale_log2;
+  __nv_bfloat16 *out;
+  float *lse;
+  int *err;
+  long long timeout_ns;
+  int debug_flags;
+};
+
+struct BwdParams {
+  SeqParams seq;
+  BiasParams bias;
+  int causal;
+  float scale_log2;
+  float scale;
+  const float *lse;   // [H, T]
+  const float *dvec;  // [H, T]: rowsum(dout * out)
+  float *dq_acc;      // [T, H, d] fp32
+  __nv_bfloat16 *dk, *dv;
+  float *dbias;       // [nb, H] or nullptr
+  int *err;
+  long long timeout_ns;
+  int debug_flags;
+};
+
+// Launchers (defined next to their kernels). Return a cudaError_t value.
+int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
+               const void *v, cudaStream_t stream);
+size_t fwd_smem_bytes(int head_dim, int lut_len);
+int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
+               const void *v, const void *out, const void *dout, cudaStream_t stream);
+size_t bwd_smem_bytes(int head_dim, int lut_len);
+int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
+                         cudaStream_t stream);
+
+// Tensor map over a [T, H, d] bf16 tensor, box = 64 channels x 1 head x box_rows tokens,
+// 128-byte swizzle (the shared-memory layout the tcgen05 descriptors expect).
+int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows);
+
+}  // namespace fat

@@ -1,0 +1,128 @@
+/*
+ * fat_attn.h -- C ABI of the GB300 (sm_103a) fused attention library with an in-kernel
+ * relative-position bias (T5 log-bucket table and/or ALiBi), padding-free varlen packing,
+ * forward and backward.
+ *
+ * What is computed. FAT5 report, "Noyau CUDA" section (second kernel version, "Flash Attention
+ * RPE"): per document and head, S = Q K^T, S' = S + B, P = softmax(S'), O = P V, where B is not
+ * passed in but built inside the kernel from the relative position of each (query, key) pair, so
+ * that memory stays linear in the sequence length. Readings of points the pages leave open:
+ *   - scale: S' = softmax_scale * (Q K^T) + B (the scale does not multiply the bias);
+ *   - relative position: delta = key_position - query_position, positions local to each
+ *     document (they restart at 0 at every cu_seqlens boundary: padding-free packing page);
+ *   - T5 bias: B = bias_table[bucket(delta), head] with the T5 paper's log-bucket function
+ *     (exact real floor; bidirectional: negative deltas use buckets [0, nb/2), positive ones
+ *     [nb/2, nb); causal/unidirectional: only delta <= 0 is distinguished);
+ *   - ALiBi bias: B = -alibi_slopes[head] * |delta|; T5 and ALiBi may be combined (they add);
+ *   - causal: keys with delta > 0 are masked (top-left aligned, self-attention per document);
+ *   - backward: gradients of sum(out * dout) with the standard softmax-attention calculus
+ *     (the pages benchmark the backward, "Benchmark / TFLOPS" section, but give no derivation);
+ *     the bias-table gradient sums dS over all (query, key) pairs that share a bucket.
+ *
+ * Layout (all row-major, contiguous, device memory unless stated):
+ *   q, k, v, out, dout, dq, dk, dv : bf16 [total_tokens, num_heads, head_dim]
+ *   lse                            : fp32 [num_heads, total_tokens], natural-log logsumexp of S'
+ *   cu_seqlens                     : int32 [num_seqs + 1], cu[0] = 0, non-decreasing,
+ *                                    cu[num_seqs] = total_tokens (read on the device only)
+ *   bias_table, dbias_table        : fp32 [num_buckets, num_heads]
+ *   alibi_slopes                   : fp32 [num_heads]
+ * Every pointer must be 16-byte aligned. head_dim must be 64 or 128.
+ *
+ * Ownership and execution. The caller allocates every buffer, including the backward
+ * workspace; the library never allocates device memory. Calls are asynchronous on
+ * shape->stream (a cudaStream_t; NULL = legacy default stream) and return after enqueueing.
+ * The only global state is a device error word per GPU (see fat_attn_get_device_error).
+ *
+ * Errors. Every call returns 0 on success or a negative FAT_E* code; nothing throws, exits or
+ * traps. Argument errors are detected on the host before anything is enqueued. Device-side
+ * problems (a pipeline wait that exceeded its time limit, a cu_seqlens entry outside
+ * [0, total_tokens]) make the kernel skip the remaining work of that block and set a bit in the
+ * device error word, which fat_attn_get_device_error reports.
+ */
+#ifndef FAT_ATTN_H
+#define FAT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FAT_OK 0
+#define FAT_EINVAL_NULL (-1)    /* a required pointer is NULL */
+#define FAT_EINVAL_SHAPE (-2)   /* bad size, head_dim not 64/128, misaligned pointer */
+#define FAT_EINVAL_BUCKETS (-3) /* bad num_buckets / max_distance / bidirectional */
+#define FAT_ECUDA (-4)          /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
+#define FAT_EUNSUPPORTED (-5)   /* valid but unsupported combination (see each call) */
+#define FAT_EDEVICE (-6)        /* the device error word was set (see below) */
+
+/* bits of the device error word */
+#define FAT_DEVERR_TIMEOUT_FWD 1 /* a forward pipeline wait exceeded its time limit */
+#define FAT_DEVERR_TIMEOUT_BWD 2 /* a backward pipeline wait exceeded its time limit */
+#define FAT_DEVERR_SEQLENS 4     /* cu_seqlens had an entry outside [0, total_tokens] or out of order */
+
+typedef struct {
+  int32_t total_tokens; /* T: sum of document lengths (rows of q, k, v) */
+  int32_t num_seqs;     /* n: number of documents; cu_seqlens has n + 1 entries */
+  int32_t max_seqlen;   /* upper bound on every document length (sizes the grid; must not be
+                           smaller than the longest document, which the host cannot check) */
+  int32_t num_heads;    /* H (q, k and v share the head count) */
+  int32_t head_dim;     /* d: 64 or 128 */
+  void *stream;         /* cudaStream_t the work is enqueued on */
+} fat_shape_t;
+
+/*
+ * Forward. out = softmax(softmax_scale * Q K^T + B) V per document and head; lse = logsumexp
+ * of the same logits (natural log). The bias B is the sum of the T5 term (when bias_table is
+ * not NULL: num_buckets, max_distance, bidirectional describe the bucket function; bidirectional
+ * needs an even num_buckets; the buckets per direction nbh must satisfy 2 <= nbh <= 128 and
+ * max_distance > nbh/2) and the ALiBi term (when alibi_slopes is not NULL). Both NULL gives
+ * plain attention. lse may be NULL if the caller does not need it (the backward needs it).
+ * FAT_EUNSUPPORTED: the bucket layout needs a larger in-kernel lookup table than shared memory
+ * holds (saturation distance above about 3800 for head_dim 64 / 2800 for head_dim 128).
+ */
+int fat_attn_fwd(const fat_shape_t *shape, const void *q, const void *k, const void *v,
+                 const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                 const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                 float softmax_scale, void *out, float *lse);
+
+/* Bytes of device workspace fat_attn_bwd needs: an fp32 dQ accumulator [T, H, d] and the fp32
+   row statistics D = rowsum(dout * out) [H, T], each 256-byte aligned. */
+size_t fat_attn_bwd_workspace_size(const fat_shape_t *shape);
+
+/*
+ * Backward of sum(out * dout) for the forward above (same bias, mask and scale arguments).
+ * Inputs: q, k, v, out and lse from the forward, dout. Outputs dq, dk, dv (bf16) and, when
+ * dbias_table is not NULL (requires bias_table), the T5 table gradient, which is OVERWRITTEN
+ * (zeroed by the library, then accumulated with fp32 atomics: bit-exact bucket assignment,
+ * order-dependent rounding). ALiBi slopes receive no gradient. workspace must hold
+ * fat_attn_bwd_workspace_size(shape) bytes; its contents need not be initialised.
+ */
+int fat_attn_bwd(const fat_shape_t *shape, const void *q, const void *k, const void *v,
+                 const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                 const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                 float softmax_scale, const void *out, const float *lse, const void *dout,
+                 void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
+                 float *dbias_table);
+
+/* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
+   FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
+int fat_attn_get_device_error(void *stream, int *bits);
+
+/* Static English description of a FAT_* return code. */
+const char *fat_attn_strerror(int code);
+
+/*
+ * Host-only helper (no GPU needed): the integer thresholds the kernels compare distances with.
+ * For t = 1 .. E-1 (E = nbh - nbh/2 log buckets per direction), thresholds[t-1] is the smallest
+ * distance n with bucket_offset(n) >= nbh/2 + t. *count receives E - 1 and *saturation the
+ * distance from which the bucket no longer changes. `thresholds` needs room for 63 entries.
+ */
+int fat_attn_bucket_thresholds(int num_buckets, int max_distance, int bidirectional,
+                               int32_t *thresholds, int *count, int *saturation);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FAT_ATTN_H */

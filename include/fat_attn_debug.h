@@ -1,0 +1,33 @@
+/*
+ * fat_attn_debug.h -- test hooks of the fused relative-position attention library.
+ * Not needed for normal use; the test-suite uses them to check the device-side bucket mapping
+ * and the bounded pipeline waits without faulting the GPU.
+ */
+#ifndef FAT_ATTN_DEBUG_H
+#define FAT_ATTN_DEBUG_H
+#include <stdint.h>
+#include "fat_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Writes, for delta = delta_lo .. delta_lo + n - 1, the T5 bucket id the attention kernels use
+ * (same device function and host thresholds) into out_dev[0 .. n-1] (device int32). Asynchronous
+ * on `stream`. Errors as in fat_attn.h (FAT_EINVAL_BUCKETS for bad bucket arguments).
+ */
+int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,
+                           int bidirectional, int32_t *out_dev, void *stream);
+
+/*
+ * Process-wide knobs for the watchdog test. timeout_ns: time limit of every pipeline wait
+ * (<= 0 restores the default of 4 s). flags bit 0: the forward producer warp issues no copies,
+ * so the consumers' waits run out, the kernel records FAT_DEVERR_TIMEOUT_FWD and exits cleanly.
+ */
+void fat_attn_debug_set_watchdog(long long timeout_ns, int flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

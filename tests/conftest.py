@@ -4,10 +4,20 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+for _p in (ROOT, os.path.dirname(os.path.abspath(__file__))):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running case")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_libraries():
+    """Compile the CUDA library and the oracle once per session (no-op when up to date)."""
+    from attention_relative_position_gb300 import _build
+    import oracle
+    _build.build()
+    oracle.build()

@@ -1,0 +1,145 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on identical seeded
+bf16 inputs. Small cases are compared element by element over every output; the full-size
+benchmark workloads, run in the benchmark's launch configuration, are compared on sampled rows
+the oracle computes one by one, plus invariants that hold at any size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_relative_position_gb300 import workloads as wl
+from gpu_common import (LSE_ATOL, assert_close, assert_dbias, oracle_problem, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+W = wl.Workload
+SMALL = [
+    wl.WORKLOADS[0],
+    W("t5enc_varlen_ragged_d64", (200, 77, 1, 0, 384), 2, 64, 1.0, (32, 128, True), False, False,
+      0.5, seed=11),
+    W("t5dec_causal_varlen_d64", (130, 16, 1, 257, 2047), 3, 64, 1.0, (32, 128, False), False,
+      True, 0.7, seed=12),
+    W("alibi_causal_d128", (300, 129), 2, 128, 1.0, None, True, True, 128 ** -0.5, seed=13),
+    W("t5_alibi_bidir_d128", (513,), 2, 128, 1.0, (32, 128, True), True, False, 0.3, seed=14),
+    W("plain_d64", (128, 256), 2, 64, 1.0, None, False, False, 0.125, seed=15),
+    W("plain_causal_d128", (257, 3), 2, 128, 1.0, None, False, True, 0.1, seed=16),
+    W("t5enc_long_buckets_d64", (1000,), 1, 64, 0.5, (64, 1024, True), False, False, 1.0,
+      seed=17),
+    W("t5enc_long_buckets_d128", (900, 33), 1, 128, 0.5, (64, 1024, True), False, False, 0.5,
+      seed=18),
+    W("alibi_bidir_d64", (260,), 4, 64, 1.0, None, True, False, 0.125, seed=19),
+    W("t5dec_alibi_causal_d64", (700, 45), 2, 64, 1.0, (32, 128, False), True, True, 0.25,
+      seed=20),
+]
+
+
+def _full_compare(w, x, res):
+    pb = oracle_problem(w, x)
+    ro, rl = oracle.attn_fwd(pb)
+    assert_close("out", res["out"], ro)
+    assert_close("lse", res["lse"], rl, atol=LSE_ATOL, rtol=0)
+    rq, rk, rv, rt = oracle.attn_bwd(pb, wl.bf16_bits(x["dout"]))
+    assert_close("dq", res["dq"], rq)
+    assert_close("dk", res["dk"], rk)
+    assert_close("dv", res["dv"], rv)
+    if rt is not None:
+        assert_dbias(res["dbias"], rt)
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_cases_full(w):
+    x = wl.make_inputs(w, device="cuda")
+    res = run_gpu(w, x)
+    _full_compare(w, x, res)
+
+
+def test_zero_table_equals_plain_attention():
+    w = W("zero_table", (333,), 2, 64, 1.0, (32, 128, True), False, False, 0.125, seed=21)
+    x = wl.make_inputs(w, device="cuda")
+    x["table"].zero_()
+    res = run_gpu(w, x)
+    plain = w.with_(t5=None)
+    xp = dict(x, table=None)
+    res_p = run_gpu(plain, xp)
+    np.testing.assert_array_equal(res["out"], res_p["out"])
+    np.testing.assert_array_equal(res["lse"], res_p["lse"])
+    _full_compare(w, x, res)
+
+
+def test_max_seqlen_larger_than_needed():
+    w = W("oversized_grid", (150, 40), 2, 64, 1.0, (32, 128, True), False, True, 0.5, seed=22)
+    x = wl.make_inputs(w, device="cuda")
+    res = run_gpu(w, x, max_seqlen=1000)
+    _full_compare(w, x, res)
+
+
+def test_repeat_calls_are_deterministic_except_dbias():
+    w = SMALL[1]
+    x = wl.make_inputs(w, device="cuda")
+    a = run_gpu(w, x)
+    b = run_gpu(w, x)
+    for k in ("out", "lse", "dk", "dv"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def _sample_rows(L, n, rng):
+    rows = {0, L - 1, L // 2, min(127, L - 1), min(128, L - 1)}
+    rows |= set(int(r) for r in rng.integers(0, L, size=n))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4], ids=[wl.WORKLOADS[i].name for i in (1, 2, 3, 4)])
+def test_full_size_workloads_sampled(idx):
+    w = wl.WORKLOADS[idx]
+    x = wl.make_inputs(w, device="cuda")
+    res = run_gpu(w, x)
+    pb = oracle_problem(w, x)
+    dout = wl.bf16_bits(x["dout"])
+    rng = np.random.default_rng(100 + idx)
+    cu = x["cu_seqlens"].cpu().numpy()
+    lens = np.diff(cu)
+    docs = sorted({int(np.argmax(lens)), int(rng.integers(0, len(lens)))})
+    heads = sorted({0, w.num_heads - 1})
+    for doc in docs:
+        s, L = int(cu[doc]), int(lens[doc])
+        rows = _sample_rows(L, 6, rng)
+        for h in heads[:1] if L > 4096 else heads:
+            o, l = oracle.attn_fwd_rows(pb, doc, h, rows)
+            assert_close(f"out[{doc},{h}]", res["out"][s + np.array(rows), h], o)
+            assert_close(f"lse[{doc},{h}]", res["lse"][h, s + np.array(rows)], l,
+                         atol=LSE_ATOL, rtol=0)
+            gq, gk, gv, gcol = oracle.attn_bwd_rows(pb, dout, doc, h, rows, rows,
+                                                    want_dtable=len(lens) == 1)
+            assert_close(f"dq[{doc},{h}]", res["dq"][s + np.array(rows), h], gq)
+            assert_close(f"dk[{doc},{h}]", res["dk"][s + np.array(rows), h], gk)
+            assert_close(f"dv[{doc},{h}]", res["dv"][s + np.array(rows), h], gv)
+            if gcol is not None:
+                assert_dbias(res["dbias"][:, h], gcol)
+    # invariants at full size
+    dvs = res["dv"].astype(np.float64)
+    dos = x["dout"].float().cpu().numpy().astype(np.float64)
+    for i in range(len(lens)):
+        s, e = int(cu[i]), int(cu[i + 1])
+        got = dvs[s:e].sum(axis=0)
+        want = dos[s:e].sum(axis=0)
+        # each row of P sums to one, so the dV rows of a document add up to its dO rows
+        assert (np.abs(got - want) <= 1e-2 * np.abs(dvs[s:e]).sum(axis=0) + 1e-2).all(), i
+    if res["dbias"] is not None:
+        col_sum = res["dbias"].sum(axis=0)
+        scale = np.abs(res["dbias"]).sum(axis=0) + 1e-6
+        assert (np.abs(col_sum) <= 1e-2 * scale + 1e-3).all(), col_sum
+
+
+def test_multi_doc_table_gradient_sums_over_documents():
+    """dtable of a packed batch is the sum of the per-document contributions."""
+    w = wl.WORKLOADS[1]
+    x = wl.make_inputs(w, device="cuda")
+    res = run_gpu(w, x)
+    pb = oracle_problem(w, x)
+    dout = wl.bf16_bits(x["dout"])
+    h = 3
+    tot = np.zeros(w.t5[0])
+    for doc in range(len(w.seqlens)):
+        _, _, _, gcol = oracle.attn_bwd_rows(pb, dout, doc, h, [0], [0], want_dtable=True)
+        tot += gcol
+    assert_dbias(res["dbias"][:, h], tot)

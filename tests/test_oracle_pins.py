@@ -10,6 +10,7 @@ rounding, missing mask) fails at least one of them.
 """
 import math
 import os
+import sys
 
 import numpy as np
 import pytest
@@ -21,43 +22,7 @@ from attention_relative_position_gb300 import workloads
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "t5_buckets.txt")
 
 
-# --------------------------------------------------------------------------------------------
-# independent exact bucket function: thresholds from integer E-th roots (threshold form, not the
-# oracle's floor-of-log form)
-# --------------------------------------------------------------------------------------------
-def _iroot_ceil(x: int, e: int) -> int:
-    """Smallest integer n with n**e >= x."""
-    lo, hi = 0, 1
-    while hi ** e < x:
-        hi *= 2
-    while lo < hi:
-        mid = (lo + hi) // 2
-        if mid ** e >= x:
-            hi = mid
-        else:
-            lo = mid + 1
-    return lo
-
-
-def exact_thresholds(nbh: int, md: int):
-    """n_t = smallest n with n >= me*(md/me)^(t/E), t = 1..E-1 (i.e. n^E * me^t >= md^t * me^E)."""
-    me = nbh // 2
-    E = nbh - me
-    return [_iroot_ceil(me ** (E - t) * md ** t, E) for t in range(1, E)]
-
-
-def exact_bucket(delta: int, nb: int, md: int, bidir: bool, thr_cache={}) -> int:
-    nbh = nb // 2 if bidir else nb
-    off = nbh if (bidir and delta > 0) else 0
-    n = abs(delta) if bidir else max(-delta, 0)
-    me = nbh // 2
-    if n < me:
-        return off + n
-    key = (nbh, md)
-    if key not in thr_cache:
-        thr_cache[key] = exact_thresholds(nbh, md)
-    t = sum(1 for th in thr_cache[key] if n >= th)
-    return off + me + t
+from exact_buckets import exact_bucket, exact_thresholds  # noqa: E402
 
 
 BUCKET_CASES = [(32, 128, True), (32, 128, False), (64, 1024, True), (64, 1024, False),
