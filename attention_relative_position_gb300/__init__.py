@@ -15,7 +15,7 @@ from typing import Optional
 __all__ = [
     "FatAttnError", "load", "fat_attn_fwd", "fat_attn_bwd", "fat_attn_bwd_workspace_size",
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
-    "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "LIB_PATH",
+    "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfatattn.so")
@@ -28,7 +28,10 @@ FAT_DEVERR_SEQLENS = 4
 class FatAttnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where} failed: {code} ({fat_attn_strerror(code)})")
+        detail = ""
+        if code == -4:
+            detail = "; " + load().fat_attn_last_error_message().decode()
+        super().__init__(f"{where} failed: {code} ({fat_attn_strerror(code)}{detail})")
 
 
 class _Shape(ctypes.Structure):
@@ -60,10 +63,19 @@ def load(path: Optional[str] = None):
     lib.fat_attn_bwd.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp,
                                  vp, ctypes.c_size_t, vp, vp, vp, vp]
     lib.fat_attn_bwd.restype = i32
+    lib.fat_attn_bwd_preprocess.argtypes = [S, vp, vp, vp, ctypes.c_size_t, vp, i32]
+    lib.fat_attn_bwd_preprocess.restype = i32
+    lib.fat_attn_bwd_main.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp,
+                                      vp, ctypes.c_size_t, vp, vp, vp]
+    lib.fat_attn_bwd_main.restype = i32
+    lib.fat_attn_bwd_finalize.argtypes = [S, vp, ctypes.c_size_t, f32, vp]
+    lib.fat_attn_bwd_finalize.restype = i32
     lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.fat_attn_get_device_error.restype = i32
     lib.fat_attn_strerror.argtypes = [i32]
     lib.fat_attn_strerror.restype = ctypes.c_char_p
+    lib.fat_attn_last_error_message.argtypes = []
+    lib.fat_attn_last_error_message.restype = ctypes.c_char_p
     lib.fat_attn_bucket_thresholds.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_int32),
                                                ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.fat_attn_bucket_thresholds.restype = i32
@@ -172,6 +184,44 @@ def fat_attn_bwd(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, bias_tabl
                           _ptr(dbias_table))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd")
+    return dq, dk, dv, dbias_table
+
+
+def fat_attn_bwd_stages(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, workspace, dq, dk,
+                        dv, dbias_table=None, bias_table=None, num_buckets: int = 0,
+                        max_distance: int = 0, bidirectional: bool = True, alibi_slopes=None,
+                        causal: bool = False, softmax_scale: float = 1.0, stream=None,
+                        between=None):
+    """The backward as its three C-ABI stages (preprocess, main, finalize) with every buffer
+    supplied by the caller. `between(i)` (optional) is called after enqueueing stage i, e.g. to
+    record CUDA events around the main kernel."""
+    lib = load()
+    T, H, d = q.shape
+    sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
+    nbytes = int(workspace.numel() * workspace.element_size())
+    if between is not None:
+        between(-1)
+    rc = lib.fat_attn_bwd_preprocess(ctypes.byref(sh), _ptr(out), _ptr(dout), _ptr(workspace),
+                                     nbytes, _ptr(dbias_table), int(num_buckets))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bwd_preprocess")
+    if between is not None:
+        between(0)
+    rc = lib.fat_attn_bwd_main(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                               int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                               _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                               float(softmax_scale), _ptr(lse), _ptr(dout), _ptr(workspace),
+                               nbytes, _ptr(dk), _ptr(dv), _ptr(dbias_table))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bwd_main")
+    if between is not None:
+        between(1)
+    rc = lib.fat_attn_bwd_finalize(ctypes.byref(sh), _ptr(workspace), nbytes,
+                                   float(softmax_scale), _ptr(dq))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bwd_finalize")
+    if between is not None:
+        between(2)
     return dq, dk, dv, dbias_table
 
 

@@ -2,6 +2,8 @@
 // exact T5 bucket thresholds, tensor-map encoding, the device error word, and kernel launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdio>
 #include <mutex>
 #include <vector>
 
@@ -15,6 +17,7 @@ namespace fat {
 namespace {
 
 std::mutex g_mu;
+thread_local char g_last_error[256] = "";
 long long g_timeout_ns = kDefaultTimeoutNs;
 int g_debug_flags = 0;
 int *g_err_ptr[128] = {nullptr};
@@ -22,11 +25,19 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int device_error_ptr(int **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return FAT_ECUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    set_last_error("cudaGetDevice", (int)e, cudaGetErrorString(e));
+    return FAT_ECUDA;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_err_ptr[dev]) {
     void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_fat_device_error) != cudaSuccess) return FAT_ECUDA;
+    e = cudaGetSymbolAddress(&ptr, g_fat_device_error);
+    if (e != cudaSuccess) {
+      set_last_error("cudaGetSymbolAddress(error word)", (int)e, cudaGetErrorString(e));
+      return FAT_ECUDA;
+    }
     g_err_ptr[dev] = static_cast<int *>(ptr);
   }
   *out = g_err_ptr[dev];
@@ -137,16 +148,23 @@ int cuda_rc(int e) { return e == 0 ? FAT_OK : FAT_ECUDA; }
 
 }  // namespace
 
+void set_last_error(const char *what, int code, const char *text) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: error %d (%s)", what, code, text ? text : "");
+}
+
 int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
       void *fn = nullptr;
       cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                       cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        set_last_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
+                       e != cudaSuccess ? (int)e : (int)q, cudaGetErrorString(e));
         return -1;
+      }
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
   }
@@ -158,7 +176,11 @@ int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int bo
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : -1;
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled", (int)r, "");
+    return -1;
+  }
+  return 0;
 }
 
 }  // namespace fat
@@ -228,6 +250,8 @@ __global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const float4 *__res
 
 // ---- C ABI -------------------------------------------------------------------------------------
 extern "C" {
+
+const char *fat_attn_last_error_message(void) { return g_last_error; }
 
 const char *fat_attn_strerror(int code) {
   switch (code) {
@@ -312,6 +336,126 @@ size_t fat_attn_bwd_workspace_size(const fat_shape_t *sh) {
   return a + b;
 }
 
+namespace {
+struct WorkspaceView {
+  float *dq_acc;
+  float *dvec;
+};
+int check_workspace(const fat_shape_t *sh, const void *ws, size_t bytes, WorkspaceView *view) {
+  const size_t need = fat_attn_bwd_workspace_size(sh);
+  if (!ws && need) return FAT_EINVAL_NULL;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return FAT_EINVAL_SHAPE;
+  if (bytes < need) return FAT_EINVAL_SHAPE;
+  const size_t T = (size_t)sh->total_tokens, H = (size_t)sh->num_heads, d = (size_t)sh->head_dim;
+  view->dq_acc = static_cast<float *>(const_cast<void *>(ws));
+  view->dvec = reinterpret_cast<float *>(static_cast<char *>(const_cast<void *>(ws)) +
+                                         ((T * H * d * 4 + 255) & ~(size_t)255));
+  return FAT_OK;
+}
+bool empty_problem(const fat_shape_t *sh) {
+  return sh->total_tokens == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0;
+}
+int launch_rc(const char *what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return FAT_OK;
+  set_last_error(what, (int)e, cudaGetErrorString(e));
+  return FAT_ECUDA;
+}
+}  // namespace
+
+int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *dout,
+                            void *workspace, size_t workspace_bytes, float *dbias_table,
+                            int num_buckets) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!out || !dout) return FAT_EINVAL_NULL;
+  if (misaligned(out) || misaligned(dout) || misaligned(dbias_table)) return FAT_EINVAL_SHAPE;
+  if (dbias_table && (num_buckets < 2 || num_buckets > 256)) return FAT_EINVAL_BUCKETS;
+  WorkspaceView ws{};
+  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(sh->stream);
+  const int T = sh->total_tokens, H = sh->num_heads, d = sh->head_dim;
+  const int nbias = dbias_table ? num_buckets * H : 0;
+  if (T == 0) {
+    if (!nbias) return FAT_OK;
+    const cudaError_t e = cudaMemsetAsync(dbias_table, 0, sizeof(float) * nbias, stream);
+    if (e != cudaSuccess) set_last_error("cudaMemsetAsync(dbias_table)", (int)e, cudaGetErrorString(e));
+    return cuda_rc((int)e);
+  }
+  const long long rows = (long long)T * H;
+  const int blocks = (int)std::min<long long>((rows + 7) / 8, 152LL * 16);
+  const auto *o = static_cast<const __nv_bfloat16 *>(out);
+  const auto *g = static_cast<const __nv_bfloat16 *>(dout);
+  if (d == 64)
+    fat_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, ws.dq_acc, dbias_table,
+                                                         nbias, T, H);
+  else
+    fat_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, ws.dq_acc, dbias_table,
+                                                          nbias, T, H);
+  return launch_rc("backward preprocess launch");
+}
+
+int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                      const float *bias_table, int num_buckets, int max_distance,
+                      int bidirectional, const float *alibi_slopes, const int32_t *cu_seqlens,
+                      int causal, float softmax_scale, const float *lse, const void *dout,
+                      void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                      float *dbias_table) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!q || !k || !v || !cu_seqlens || !lse || !dout || !dk || !dv) return FAT_EINVAL_NULL;
+  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dout) || misaligned(dk) ||
+      misaligned(dv) || misaligned(lse) || misaligned(cu_seqlens) || misaligned(bias_table) ||
+      misaligned(alibi_slopes) || misaligned(dbias_table))
+    return FAT_EINVAL_SHAPE;
+  BwdParams p{};
+  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (bwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  WorkspaceView ws{};
+  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  if (empty_problem(sh)) return FAT_OK;
+  rc = device_error_ptr(&p.err);
+  if (rc) return rc;
+  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens};
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.scale = softmax_scale;
+  p.lse = lse;
+  p.dvec = ws.dvec;
+  p.dq_acc = ws.dq_acc;
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.dbias = dbias_table;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    p.timeout_ns = g_timeout_ns;
+    p.debug_flags = g_debug_flags;
+  }
+  return cuda_rc(launch_bwd(p, sh->head_dim, sh->max_seqlen, q, k, v, nullptr, dout,
+                           static_cast<cudaStream_t>(sh->stream)));
+}
+
+int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
+                          float softmax_scale, void *dq) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!dq) return FAT_EINVAL_NULL;
+  if (misaligned(dq)) return FAT_EINVAL_SHAPE;
+  WorkspaceView ws{};
+  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  const long long n4 = (long long)sh->total_tokens * sh->num_heads * sh->head_dim / 4;
+  if (n4 == 0) return FAT_OK;
+  const int blocks = (int)std::min<long long>((n4 + 255) / 256, 152LL * 16);
+  fat_bwd_finish_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(sh->stream)>>>(
+      reinterpret_cast<const float4 *>(ws.dq_acc), static_cast<uint2 *>(dq), softmax_scale, n4);
+  return launch_rc("backward finalize launch");
+}
+
 int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
@@ -323,67 +467,25 @@ int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void
   if (!q || !k || !v || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv)
     return FAT_EINVAL_NULL;
   if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
-      misaligned(dq) || misaligned(dk) || misaligned(dv) || misaligned(lse) ||
-      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
-      misaligned(dbias_table) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return FAT_EINVAL_SHAPE;
-  BwdParams p{};
-  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
-  if (rc) return rc;
-  if (bwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
-  const size_t need = fat_attn_bwd_workspace_size(sh);
-  if (!workspace && need) return FAT_EINVAL_NULL;
-  if (workspace_bytes < need) return FAT_EINVAL_SHAPE;
-  cudaStream_t stream = static_cast<cudaStream_t>(sh->stream);
-  const int T = sh->total_tokens, H = sh->num_heads, d = sh->head_dim;
-  if (T == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0) {
-    if (dbias_table && num_buckets > 0)
-      return cuda_rc(cudaMemsetAsync(dbias_table, 0, sizeof(float) * num_buckets * H, stream));
-    return FAT_OK;
-  }
-  rc = device_error_ptr(&p.err);
-  if (rc) return rc;
-  float *dq_acc = static_cast<float *>(workspace);
-  float *dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                          (((size_t)T * H * d * 4 + 255) & ~(size_t)255));
-  // 1) D = rowsum(dout * out), zero the dQ accumulator and the table gradient
-  const long long rows = (long long)T * H;
-  const int prep_blocks = (int)std::min<long long>((rows + 7) / 8, 152LL * 16);
-  if (d == 64)
-    fat_bwd_prep_kernel<64><<<prep_blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), dvec,
-        dq_acc, dbias_table, dbias_table ? num_buckets * H : 0, T, H);
-  else
-    fat_bwd_prep_kernel<128><<<prep_blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), dvec,
-        dq_acc, dbias_table, dbias_table ? num_buckets * H : 0, T, H);
-  if (cudaGetLastError() != cudaSuccess) return FAT_ECUDA;
-  // 2) main kernel: one CTA per (document, head, 128-key tile)
-  p.seq = SeqParams{cu_seqlens, sh->num_seqs, H, T};
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = softmax_scale * kLog2e;
-  p.scale = softmax_scale;
-  p.lse = lse;
-  p.dvec = dvec;
-  p.dq_acc = dq_acc;
-  p.dk = static_cast<__nv_bfloat16 *>(dk);
-  p.dv = static_cast<__nv_bfloat16 *>(dv);
-  p.dbias = dbias_table;
+  // validate everything before enqueueing anything
+  if (misaligned(out) || misaligned(dq)) return FAT_EINVAL_SHAPE;
   {
-    std::lock_guard<std::mutex> lk(g_mu);
-    p.timeout_ns = g_timeout_ns;
-    p.debug_flags = g_debug_flags;
+    BiasParams b{};
+    rc = fill_bias(&b, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+    if (rc) return rc;
+    if (bwd_smem_bytes(sh->head_dim, b.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+    WorkspaceView ws{};
+    rc = check_workspace(sh, workspace, workspace_bytes, &ws);
+    if (rc) return rc;
   }
-  rc = cuda_rc(launch_bwd(p, d, sh->max_seqlen, q, k, v, out, dout, stream));
+  rc = fat_attn_bwd_preprocess(sh, out, dout, workspace, workspace_bytes, dbias_table,
+                               num_buckets);
   if (rc) return rc;
-  // 3) dq = bf16(scale * dQ accumulator)
-  const long long n4 = rows * d / 4;
-  const int fin_blocks = (int)std::min<long long>((n4 + 255) / 256, 152LL * 16);
-  fat_bwd_finish_kernel<<<fin_blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(dq_acc),
-                                                        static_cast<uint2 *>(dq), softmax_scale,
-                                                        n4);
-  return cudaGetLastError() == cudaSuccess ? FAT_OK : FAT_ECUDA;
+  rc = fat_attn_bwd_main(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                         alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
+                         workspace_bytes, dk, dv, dbias_table);
+  if (rc) return rc;
+  return fat_attn_bwd_finalize(sh, workspace, workspace_bytes, softmax_scale, dq);
 }
 
 int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,

@@ -18,12 +18,16 @@
 //                128-byte-swizzled layout the MMAs read; bias-gradient partial sums.
 //   warps 8-11   drain dQ_i from TMEM into the fp32 dQ accumulator with vector reductions, then
 //                write dK, dV.
+//   warps 14-15  idle; with warps 12-13 they form the fourth warpgroup, whose registers go to
+//                the P/dS warpgroups (168 + 168 + 112 + 64 = 512 per SM sub-partition).
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
 // the other tiles add into a shared-memory array indexed by delta (one conflict-free shared
 // reduction per element, consecutive lanes hit consecutive deltas); at the end the CTA maps
 // deltas to buckets and issues one global atomic per (bucket, head).
 // Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, dK and dV fit
 // the 512 TMEM columns together.
+#include <cstdio>
+
 #include "fat_attn_internal.cuh"
 
 namespace fat {
@@ -49,7 +53,7 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
   static constexpr int OFF_BACC = OFF_BAR + 256;        // per-bucket sums, 256 floats
   static constexpr int OFF_LUT = OFF_BACC + 256 * 4;    // lut[lut_len], then diag[lut_len]
-  static constexpr int NTHREADS = 448;
+  static constexpr int NTHREADS = 512;
   static constexpr int COL_S = 0, COL_DP = BQ, COL_DQ = 2 * BQ;
   static constexpr int COL_DK = 512 - 2 * D, COL_DV = 512 - D;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BQ, 0, 0);
@@ -63,7 +67,7 @@ size_t bwd_smem_bytes(int head_dim, int lut_len) {
 }
 
 template <int D>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(512, 1)
     fat_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
@@ -151,6 +155,8 @@ __global__ void __maxnreg__(144)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_BWD, p.timeout_ns};
   float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (softmax warps)
+  if (warp >= 12) regs_dec<64>();
+  else if (warp >= 8) regs_dec<112>();
 
   if (warp == 12) {
     // ------------------------------------------------------------------ producer
@@ -283,6 +289,7 @@ __global__ void __maxnreg__(144)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P / dS warpgroups
+    regs_inc<168>();
     const int wg = warp >> 2;
     const int r = tid & 127;
     const int c0 = wg * C::HALF;
@@ -389,7 +396,7 @@ __global__ void __maxnreg__(144)
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
     }
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------------------------ dQ drain, dK/dV out
     const int dr = tid - 256;  // TMEM lane 0..127
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -436,26 +443,28 @@ __global__ void __maxnreg__(144)
       const bool valid = krow < L;
       __nv_bfloat16 *dkrow = p.dk + ((size_t)(seq_start + krow) * H + h) * D;
       __nv_bfloat16 *dvrow = p.dv + ((size_t)(seq_start + krow) * H + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t a[16];
+        tmem_ld16(tmem + lane_off + C::COL_DK + 16 * c, a);
+        uint32_t pa[8];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + C::COL_DK + 32 * c, a);
-        tmem_ld32(tmem + lane_off + C::COL_DV + 32 * c, b);
-        uint32_t pa[16], pb[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i)
           pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
                               __uint_as_float(a[2 * i + 1]) * p.scale);
-          pb[i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-        }
         if (valid) {
-          uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 32 * c);
-          uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 32 * c);
+          uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 16 * c);
+          dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+        }
+        tmem_ld16(tmem + lane_off + C::COL_DV + 16 * c, a);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            dk4[v4] = make_uint4(pa[4 * v4], pa[4 * v4 + 1], pa[4 * v4 + 2], pa[4 * v4 + 3]);
-            dv4[v4] = make_uint4(pb[4 * v4], pb[4 * v4 + 1], pb[4 * v4 + 2], pb[4 * v4 + 3]);
-          }
+        for (int i = 0; i < 8; ++i)
+          pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+        if (valid) {
+          uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 16 * c);
+          dv4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          dv4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
         }
       }
     }
@@ -515,8 +524,24 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
     if (e == cudaSuccess)
       fat_bwd_kernel<128><<<grid, BwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, p);
   }
-  if (e != cudaSuccess) return (int)e;
-  return (int)cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
+    return (int)e;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    if (head_dim == 64)
+      cudaFuncGetAttributes(&fa, fat_bwd_kernel<64>);
+    else
+      cudaFuncGetAttributes(&fa, fat_bwd_kernel<128>);
+    char msg[160];
+    snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
+             cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
+             smem);
+    set_last_error("kernel launch", (int)e, msg);
+  }
+  return (int)e;
 }
 
 }  // namespace fat

@@ -4,17 +4,22 @@
 // on-chip memory, S = Q K^T, S' = S + (bias built on the fly from relative positions),
 // P = softmax(S') computed cumulatively (online), O = P V, and O is written back once.
 //
-// GB300 design (one CTA = one document x head x 256 query rows = two 128-row Q tiles):
+// GB300 design (one CTA = one document x head x 256 query rows = two 128-row Q tiles; three
+// warpgroups, so that every SM sub-partition holds one warp of each):
 //   warp 8      TMA producer: Q tiles once, K/V tiles through an NS-stage shared-memory ring.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma,
 //               accumulators in tensor memory (TMEM); P_t is read from TMEM where the softmax
 //               warps wrote it over S_t.
+//   warps 10-11 idle (they complete the third warpgroup, which gives its registers to the
+//               softmax warpgroups: 224 + 224 + 56 per sub-partition fits its 512 x 32 registers).
 //   warps 0-7   two softmax warpgroups, one per Q tile; thread i owns row i of its tile (TMEM
 //               lane i), so row max/sum need no shuffles. Bias: closed form on tiles that lie
 //               beyond the T5 saturation distance, a per-CTA lookup table over delta on the rest.
 //               The running max is only raised (and O rescaled in TMEM) when it grows by more
 //               than 2^8, which keeps P <= 256 and leaves the final result exact.
 // While one warpgroup computes its softmax, the tensor cores run the other tile's MMAs.
+#include <cstdio>
+
 #include "fat_attn_internal.cuh"
 
 namespace fat {
@@ -30,7 +35,7 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
   static constexpr int OFF_LUT = OFF_BAR + 256;
-  static constexpr int NTHREADS = 320;
+  static constexpr int NTHREADS = 384;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major), K (K-major)
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V (MN-major)
 };
@@ -73,7 +78,7 @@ __device__ __forceinline__ float fwd_logits(uint32_t tS, float (&x)[128], float 
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(384, 1)
     fat_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
@@ -148,6 +153,8 @@ __global__ void __maxnreg__(200)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+
+  if (warp >= 8) regs_dec<56>();
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -259,8 +266,9 @@ __global__ void __maxnreg__(200)
       mma_commit(mma_done);
       mbar_wait_teardown(mma_done, 0, kTeardownNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
+    regs_inc<224>();
     const int t = warp >> 2;
     if (t < ntile) {
       const int nk = t == 0 ? nkv0 : nkv1;
@@ -413,8 +421,24 @@ int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, 
     if (e == cudaSuccess)
       fat_fwd_kernel<128><<<grid, FwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
   }
-  if (e != cudaSuccess) return (int)e;
-  return (int)cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
+    return (int)e;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    if (head_dim == 64)
+      cudaFuncGetAttributes(&fa, fat_fwd_kernel<64>);
+    else
+      cudaFuncGetAttributes(&fa, fat_fwd_kernel<128>);
+    char msg[160];
+    snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
+             cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
+             smem);
+    set_last_error("kernel launch", (int)e, msg);
+  }
+  return (int)e;
 }
 
 }  // namespace fat

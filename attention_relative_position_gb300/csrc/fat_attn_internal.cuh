@@ -124,6 +124,9 @@ size_t bwd_smem_bytes(int head_dim, int lut_len);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);
 
+// Record a description of the last failing CUDA call of this thread (read by the C ABI).
+void set_last_error(const char *what, int code, const char *text);
+
 // Tensor map over a [T, H, d] bf16 tensor, box = 64 channels x 1 head x box_rows tokens,
 // 128-byte swizzle (the shared-memory layout the tcgen05 descriptors expect).
 int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows);

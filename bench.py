@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Benchmark of the fused relative-position attention on GB300.
+
+One step = the whole hot path on one batch: forward (bias built in-kernel, varlen, online
+softmax) and backward (preprocess, main kernel with the table gradient, finalize), all through
+the library's C ABI. Reports bf16 attention TFLOP/s (4*L^2*d per head and document for the
+forward, halved when causal; 2.5x that for the backward) and the fraction of the measured
+tensor-core peak. Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|INDEX] [--impl reference]
+Under torchrun each rank runs its own replica of the workload (independent problems, no
+collective on the data path: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "bf16 attention TFLOP/s fwd & fwd+bwd (T5-bias, varlen) vs tensor-core peak"
+DEFAULT_WORKLOAD = 1  # T5 encoder, batch 8 x seq 1024, 8 heads, head_dim 64
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true",
+                    help="timed steps only: no e2e, clocks, CPU baseline or extra workloads "
+                         "(for profiler launch lists)")
+    return ap.parse_args()
+
+
+def pick_workload(spec):
+    from attention_relative_position_gb300 import workloads as wl
+    if spec.isdigit():
+        return wl.WORKLOADS[int(spec)]
+    return wl.by_name(spec)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, world, l2_note):
+    return {
+        "workload": w.name,
+        "description": w.description,
+        "num_docs": len(w.seqlens),
+        "tokens_per_gpu": w.total_tokens,
+        "global_tokens": w.total_tokens * world,
+        "max_seqlen": w.max_seqlen,
+        "num_heads": w.num_heads,
+        "head_dim": w.head_dim,
+        "t5_bias": (None if w.t5 is None else
+                    {"num_buckets": w.t5[0], "max_distance": w.t5[1], "bidirectional": w.t5[2]}),
+        "alibi": w.alibi,
+        "causal": w.causal,
+        "softmax_scale": w.scale,
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "l2": l2_note,
+    }
+
+
+# -------------------------------------------------------------------------------------------
+# clocks sampled by nvidia-smi while the timed loop runs
+# -------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, val in zip(names, parts[4:8]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# -------------------------------------------------------------------------------------------
+# the GPU arm
+# -------------------------------------------------------------------------------------------
+def lib_kwargs(w, x):
+    t5 = w.t5 or (0, 0, True)
+    return dict(bias_table=x["table"], alibi_slopes=x["slopes"], causal=w.causal,
+                softmax_scale=w.scale, num_buckets=t5[0], max_distance=t5[1],
+                bidirectional=t5[2])
+
+
+class Runner:
+    """Device-resident inputs, outputs and workspace for one workload; step() enqueues the whole
+    hot path with CUDA events between the kernels."""
+
+    def __init__(self, w, device):
+        import torch
+        import attention_relative_position_gb300 as fa
+        from attention_relative_position_gb300 import workloads as wl
+        self.torch, self.fa, self.w = torch, fa, w
+        self.x = wl.make_inputs(w, device=device)
+        x = self.x
+        self.kw = lib_kwargs(w, x)
+        self.out = torch.empty_like(x["q"])
+        self.lse = torch.empty((w.num_heads, w.total_tokens), dtype=torch.float32, device=device)
+        self.dq = torch.empty_like(x["q"])
+        self.dk = torch.empty_like(x["q"])
+        self.dv = torch.empty_like(x["q"])
+        self.dtab = torch.empty_like(x["table"]) if x["table"] is not None else None
+        nws = fa.fat_attn_bwd_workspace_size(w.total_tokens, w.num_heads, w.head_dim)
+        self.ws = torch.empty(nws, dtype=torch.uint8, device=device)
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.stream = torch.cuda.current_stream(device)
+
+    def step(self, events=None):
+        fa, x, w = self.fa, self.x, self.w
+        if events is not None:
+            events[0].record(self.stream)
+        fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, out=self.out,
+                        lse=self.lse, stream=self.stream, **self.kw)
+        between = None
+        if events is not None:
+            def between(i):
+                if i >= 0:
+                    events[i + 2].record(self.stream)
+                else:
+                    events[1].record(self.stream)
+        fa.fat_attn_bwd_stages(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, self.out,
+                               self.lse, x["dout"], self.ws, self.dq, self.dk, self.dv,
+                               dbias_table=self.dtab, stream=self.stream, between=between,
+                               **self.kw)
+
+    def flush_l2(self):
+        self.flush.zero_()
+
+    LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, backward finalize
+
+
+def time_steps(r, steps, flush=True):
+    """Per-kernel device times (ms) of `steps` steps; L2 flushed between steps (not timed)."""
+    torch = r.torch
+    per = {"fwd": [], "bwd_pre": [], "bwd_main": [], "bwd_fin": [], "step": []}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            r.flush_l2()
+        r.step(evs[i])
+    torch.cuda.synchronize()
+    for e in evs:
+        t = [e[j].elapsed_time(e[j + 1]) for j in range(4)]
+        per["fwd"].append(t[0])
+        per["bwd_pre"].append(t[1])
+        per["bwd_main"].append(t[2])
+        per["bwd_fin"].append(t[3])
+        per["step"].append(sum(t))
+    return per
+
+
+def e2e_steps(w, r, steps):
+    """Same metric through the public API from pinned host buffers: every step copies the
+    inputs host->device, runs forward + backward, and copies out, dq, dk, dv (and the table
+    gradient) back to host."""
+    torch, fa = r.torch, r.fa
+    x = r.x
+    names_in = [n for n in ("q", "k", "v", "dout", "cu_seqlens", "table", "slopes")
+                if x[n] is not None]
+    host_in = {n: x[n].cpu().pin_memory() for n in names_in}
+    dev_in = {n: torch.empty_like(x[n]) for n in names_in}
+    outs = [r.out, r.dq, r.dk, r.dv] + ([r.dtab] if r.dtab is not None else [])
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    s = r.stream
+    t5 = w.t5 or (0, 0, True)
+    kw = dict(alibi_slopes=dev_in.get("slopes"), causal=w.causal, softmax_scale=w.scale,
+              num_buckets=t5[0], max_distance=t5[1], bidirectional=t5[2],
+              bias_table=dev_in.get("table"))
+
+    def one():
+        for n in names_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        out, lse = fa.fat_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["cu_seqlens"],
+                                   w.max_seqlen, out=r.out, lse=r.lse, stream=s, **kw)
+        fa.fat_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["cu_seqlens"],
+                        w.max_seqlen, out, lse, dev_in["dout"], workspace=r.ws, dq=r.dq,
+                        dk=r.dk, dv=r.dv, dbias_table=r.dtab, stream=s, **kw)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        one()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+        ent = table[kernel_key]
+        src = os.path.join(ROOT, "attention_relative_position_gb300", "csrc", ent["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return float(ent["dram_bytes_per_launch"]) if sha == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, seconds=10.0):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample of the workload:
+    whole (document, head) pairs, forward + backward, until `seconds` have elapsed."""
+    import numpy as np
+    import oracle
+    from attention_relative_position_gb300 import workloads as wl
+    x = wl.make_inputs(w, device="cpu")
+    t5 = w.t5 or (0, 0, True)
+    pb = oracle.Problem(wl.bf16_bits(x["q"]), wl.bf16_bits(x["k"]), wl.bf16_bits(x["v"]),
+                        x["cu_seqlens"].numpy(),
+                        table=x["table"].numpy() if x["table"] is not None else None,
+                        num_buckets=t5[0], max_distance=t5[1], bidirectional=t5[2],
+                        slopes=x["slopes"].numpy() if x["slopes"] is not None else None,
+                        causal=w.causal, scale=w.scale, d_from_bf16_out=True)
+    dout = wl.bf16_bits(x["dout"])
+    lens = np.diff(x["cu_seqlens"].numpy())
+    pairs = [(i, h) for i in range(len(lens)) for h in range(w.num_heads) if lens[i] > 0]
+    flops, done, t0 = 0.0, 0, time.perf_counter()
+    for doc, h in pairs:
+        L = int(lens[doc])
+        rows = list(range(L))
+        oracle.attn_fwd_rows(pb, doc, h, rows)
+        oracle.attn_bwd_rows(pb, dout, doc, h, rows, rows, want_dtable=w.t5 is not None)
+        f = 4.0 * L * L * w.head_dim * 3.5
+        flops += f / 2 if w.causal else f
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} of {len(pairs)} (document, head) pairs of {w.name}, forward + "
+                      f"backward of every row, {dt:.1f} s",
+            "seconds": dt}
+
+
+def quick_other(w, device, peaks, steps=10):
+    r = Runner(w, device)
+    for _ in range(3):
+        r.step()
+    per = time_steps(r, steps)
+    f = w.fwd_flops()
+    fwd_ms = statistics.mean(per["fwd"])
+    step_ms = statistics.mean(per["step"])
+    main_ms = statistics.mean(per["bwd_main"])
+    res = {"fwd_tflops": f / fwd_ms / 1e9, "fwd_bwd_tflops": 3.5 * f / step_ms / 1e9,
+           "bwd_main_tflops": 2.5 * f / main_ms / 1e9}
+    res.update({k + "_frac": v / peaks["bf16_tflops"] for k, v in list(res.items())})
+    res = {k: round(v, 4) for k, v in res.items()}
+    res["ms_per_step"] = round(step_ms, 4)
+    del r
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from attention_relative_position_gb300 import _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    device = f"cuda:{local_rank}"
+    torch.cuda.set_device(device)
+    w = pick_workload(args.workload)
+    steps = args.steps if args.steps is not None else (300 if w.fwd_flops() < 1e11 else 30)
+    warmup = max(args.warmup, 1)
+    peaks, peak_src = load_peaks()
+    r = Runner(w, device)
+    for _ in range(warmup):
+        r.step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if not args.quick else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    per = time_steps(r, steps, flush=not args.quick)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    bits = r.fa.fat_attn_get_device_error()
+    if bits:
+        raise RuntimeError(f"device error word {bits}")
+    mean = {k: statistics.mean(v) for k, v in per.items()}
+    step_ms = mean["step"]
+    if world > 1:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    f = w.fwd_flops()
+    value = 3.5 * f * world / step_ms / 1e9  # TFLOP/s
+    kernels = {"fwd": ("fat_fwd_kernel", f, mean["fwd"], "fat_attn_fwd.cu"),
+               "bwd_main": ("fat_bwd_kernel", 2.5 * f, mean["bwd_main"], "fat_attn_bwd.cu")}
+    dom = max(kernels, key=lambda k: kernels[k][2])
+    kname, kflops, kms, ksrc = kernels[dom]
+    achieved = kflops / kms / 1e9
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)-type inputs of the workload's shapes; no dataset)",
+        "config": workload_config(w, world, "flushed between timed steps (256 MiB write, "
+                                            "outside the timed kernels)"),
+        "fwd_tflops": round(f / mean["fwd"] / 1e9, 3),
+        "bwd_tflops": round(2.5 * f / (mean["bwd_pre"] + mean["bwd_main"] + mean["bwd_fin"])
+                            / 1e9, 3),
+        "per_kernel_ms": {k: round(v, 5) for k, v in mean.items()},
+        "roofline": {"kernel": f"{kname}<{w.head_dim}>", "bound": "tensor",
+                     "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_src} bf16 dense (burst; kernel timed alone)",
+                     "traffic": traffic_for(f"{kname}<{w.head_dim}>@{w.name}"),
+                     "algorithmic_flops_per_launch": kflops},
+        "gpu_launches": steps * Runner.LAUNCHES_PER_STEP,
+        "timed_wall_s": round(wall, 4),
+    }
+    if clocks is not None:
+        line["clocks"] = clocks
+    if not args.quick:
+        e_steps = max(3, min(steps, 20))
+        ems, h2d, d2h = e2e_steps(w, r, e_steps)
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        line["e2e"] = {"value": round(3.5 * f * world / ems / 1e9, 3), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(ems, 4)}
+        if rank == 0 and world == 1:
+            from attention_relative_position_gb300 import workloads as wl
+            others = {}
+            for idx in (2, 3, 4):
+                ow = wl.WORKLOADS[idx]
+                if ow.name != w.name:
+                    others[ow.name] = quick_other(ow, device, peaks)
+            line["other_workloads"] = others
+            line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from attention_relative_position_gb300 import workloads as wl
+    oracle.build()
+    w = pick_workload(args.workload)
+    steps = args.steps if args.steps is not None else 3
+    warmup = args.warmup
+    x = wl.make_inputs(w, device="cpu")
+    t5 = w.t5 or (0, 0, True)
+    pb = oracle.Problem(wl.bf16_bits(x["q"]), wl.bf16_bits(x["k"]), wl.bf16_bits(x["v"]),
+                        x["cu_seqlens"].numpy(),
+                        table=x["table"].numpy() if x["table"] is not None else None,
+                        num_buckets=t5[0], max_distance=t5[1], bidirectional=t5[2],
+                        slopes=x["slopes"].numpy() if x["slopes"] is not None else None,
+                        causal=w.causal, scale=w.scale, d_from_bf16_out=True)
+    dout = wl.bf16_bits(x["dout"])
+    lens = np.diff(x["cu_seqlens"].numpy())
+    pairs = [(i, h) for i in range(len(lens)) for h in range(w.num_heads) if lens[i] > 0]
+
+    def one(k):  # one bounded sample: the k-th (document, head) pair, forward + backward
+        doc, h = pairs[k % len(pairs)]
+        L = int(lens[doc])
+        rows = list(range(L))
+        oracle.attn_fwd_rows(pb, doc, h, rows)
+        oracle.attn_bwd_rows(pb, dout, doc, h, rows, rows, want_dtable=w.t5 is not None)
+        f = 3.5 * 4.0 * L * L * w.head_dim
+        return f / 2 if w.causal else f
+
+    for k in range(warmup):
+        one(k)
+    t0 = time.perf_counter()
+    flops = sum(one(warmup + k) for k in range(steps))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, world, "host run (no GPU)"),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": oracle.num_threads(),
+                         "sample": f"each step: one (document, head) pair of {w.name}, "
+                                   f"forward + backward of every row, fp64"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -106,12 +106,38 @@ int fat_attn_bwd(const fat_shape_t *shape, const void *q, const void *k, const v
                  void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
                  float *dbias_table);
 
+/*
+ * The three stages fat_attn_bwd runs, in order, on the same stream and workspace (exposed so
+ * that callers can schedule or time them separately):
+ *   preprocess: D = rowsum(dout * out) (fp32, into the workspace), zero the fp32 dQ
+ *               accumulator, zero dbias_table when given (num_buckets rows);
+ *   main:       dK, dV (written), dQ (accumulated into the workspace) and the table gradient
+ *               (accumulated into dbias_table), one CTA per (document, head, 128-key tile);
+ *   finalize:   dq = bf16(softmax_scale * dQ accumulator).
+ * Arguments mean what they mean for fat_attn_bwd; the same errors apply.
+ */
+int fat_attn_bwd_preprocess(const fat_shape_t *shape, const void *out, const void *dout,
+                            void *workspace, size_t workspace_bytes, float *dbias_table,
+                            int num_buckets);
+int fat_attn_bwd_main(const fat_shape_t *shape, const void *q, const void *k, const void *v,
+                      const float *bias_table, int num_buckets, int max_distance,
+                      int bidirectional, const float *alibi_slopes, const int32_t *cu_seqlens,
+                      int causal, float softmax_scale, const float *lse, const void *dout,
+                      void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                      float *dbias_table);
+int fat_attn_bwd_finalize(const fat_shape_t *shape, const void *workspace,
+                          size_t workspace_bytes, float softmax_scale, void *dq);
+
 /* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
    FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
 int fat_attn_get_device_error(void *stream, int *bits);
 
 /* Static English description of a FAT_* return code. */
 const char *fat_attn_strerror(int code);
+
+/* Description of the last CUDA call that failed in this thread (which call, its error code and
+   text); empty if none has. The string stays valid until the next failing call of the thread. */
+const char *fat_attn_last_error_message(void);
 
 /*
  * Host-only helper (no GPU needed): the integer thresholds the kernels compare distances with.

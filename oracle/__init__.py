@@ -55,6 +55,7 @@ class _Problem(ctypes.Structure):
         ("alibi_slopes", ctypes.c_void_p),
         ("causal", ctypes.c_int),
         ("softmax_scale", ctypes.c_double),
+        ("d_from_bf16_out", ctypes.c_int),
     ]
 
 
@@ -106,6 +107,7 @@ class Problem:
     slopes: Optional[np.ndarray] = None
     causal: bool = False
     scale: float = 1.0
+    d_from_bf16_out: bool = False  # backward row statistic from the bf16-rounded output
 
     def __post_init__(self):
         self.q, self.k, self.v = widen(self.q), widen(self.k), widen(self.v)
@@ -131,6 +133,7 @@ class Problem:
         p.alibi_slopes = self.slopes.ctypes.data if self.slopes is not None else None
         p.causal = int(bool(self.causal))
         p.softmax_scale = float(self.scale)
+        p.d_from_bf16_out = int(bool(self.d_from_bf16_out))
         return p
 
 

@@ -19,7 +19,9 @@
  *   - Causal: S'[p, r] = -inf for r > p. Positions restart at 0 in every document of a packed
  *     batch (padding-free packing page: examples concatenated with per-example boundaries).
  *   - Backward: the loss is sum(out * dout); the gradients are the standard softmax-attention
- *     calculus (the pages only benchmark the backward and give no derivation).
+ *     calculus (the pages only benchmark the backward and give no derivation). The row statistic
+ *     D = sum_r P dP is either exact, or (on request) formed from the output rounded to bf16,
+ *     which is what a backward pass that receives the stored bf16 output computes.
  * All arithmetic is fp64. Inputs arrive as fp64 arrays; the Python wrapper widens the exact bf16
  * and fp32 values the GPU path receives, so both sides start from identical numbers.
  *
@@ -176,6 +178,35 @@ static int *bucket_cache(const oracle_problem_t *pb, int L) {
   return c;
 }
 
+/* round to bf16, nearest-even, via fp32 (NaN/Inf not expected here) */
+static double round_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  u &= 0xFFFF0000u;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* D of one row: either the exact sum_r P dP, or from the bf16-rounded output row */
+static double row_D(const oracle_problem_t *pb, const double *P, const double *dP,
+                    const double *dop, int s, int L, int h) {
+  double D = 0.0;
+  if (!pb->d_from_bf16_out) {
+    for (int r = 0; r < L; ++r) D += P[r] * dP[r];
+    return D;
+  }
+  const int H = pb->num_heads, d = pb->head_dim;
+  for (int c = 0; c < d; ++c) {
+    double o = 0.0;
+    for (int r = 0; r < L; ++r)
+      if (P[r] != 0.0) o += P[r] * pb->v[((size_t)(s + r) * H + h) * d + c];
+    D += dop[c] * round_bf16(o);
+  }
+  return D;
+}
+
 static double dotd(const double *a, const double *b, int d) {
   double s = 0.0;
   for (int c = 0; c < d; ++c) s += a[c] * b[c];
@@ -261,12 +292,11 @@ static void bwd_pair(const oracle_problem_t *pb, const double *dout, int s, int 
     logits_row(pb, bk, s, L, h, p, P);
     softmax_row(P, L);
     const double *dop = dout + ((size_t)(s + p) * H + h) * d;
-    double D = 0.0;
     for (int r = 0; r < L; ++r) {
       const double *vr = pb->v + ((size_t)(s + r) * H + h) * d;
       dP[r] = dotd(dop, vr, d);
-      D += P[r] * dP[r];
     }
+    const double D = row_D(pb, P, dP, dop, s, L, h);
     const double *qp = pb->q + ((size_t)(s + p) * H + h) * d;
     double *dqp = dq ? dq + ((size_t)(s + p) * H + h) * d : NULL;
     for (int r = 0; r < L; ++r) {
@@ -406,15 +436,9 @@ int oracle_attn_bwd_rows(const oracle_problem_t *pb, const double *dout, int doc
       logits_row(pb, bk, s, L, head, p, P);
       softmax_row(P, L);
       const double *dop = dout + ((size_t)(s + p) * H + head) * d;
-      double D = 0.0;
-      for (int r = 0; r < L; ++r) {
-        if (P[r] == 0.0) {
-          dP[r] = 0.0;
-          continue;
-        }
-        dP[r] = dotd(dop, pb->v + ((size_t)(s + r) * H + head) * d, d);
-        D += P[r] * dP[r];
-      }
+      for (int r = 0; r < L; ++r)
+        dP[r] = (P[r] == 0.0) ? 0.0 : dotd(dop, pb->v + ((size_t)(s + r) * H + head) * d, d);
+      const double D = row_D(pb, P, dP, dop, s, L, head);
       const double *qp = pb->q + ((size_t)(s + p) * H + head) * d;
       if (qpos[p] >= 0 && dq_rows) {
         double *o = dq_rows + (size_t)qpos[p] * d;

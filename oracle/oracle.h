@@ -29,6 +29,10 @@ typedef struct {
   const double *alibi_slopes;
   int causal;
   double softmax_scale;
+  /* 0: D_p = sum_r P[p,r] dP[p,r] (exact calculus). 1: D_p = sum_c dO[p,c] * bf16(O[p,c]), the
+     row statistic formed from the forward output as stored in bf16 (the backward's inputs are
+     the bf16 output, as in FlashAttention-style backward passes). */
+  int d_from_bf16_out;
 } oracle_problem_t;
 
 int oracle_t5_bucket(long long delta, int num_buckets, int max_distance, int bidirectional);

@@ -7,12 +7,16 @@ import attention_relative_position_gb300 as fa
 import oracle
 from attention_relative_position_gb300 import workloads as wl
 
-# Tolerances (GPU vs fp64 oracle on identical bf16 inputs).
-#   out, dq, dk, dv: |gpu - ref| <= ATOL + RTOL * |ref|. ATOL is the 2e-2 max-abs bar; RTOL covers
-#     the bf16 storage of the outputs (half an ulp is 2^-9 relative) and the bf16 rounding of P
-#     and dS before the tensor-core contractions, which matters for gradients whose magnitude
-#     exceeds 1 (unscaled T5 logits with N(0,1) inputs give |dq| of several units).
-#   lse: 1e-3 absolute. dbias: norm-wise relative 1e-2, and per bucket 1e-2 * max|ref| + 1e-3.
+# Backward reference: the exact-calculus oracle. The backward receives the forward output as
+# stored in bf16 and forms D = rowsum(dout * out) from it (as FlashAttention-style backward
+# passes do), so D carries an error |delta_q| <= u * sum_c |dO_qc O_qc| with u = 2^-8 (the bf16
+# rounding of out, plus the GPU's out differing from the exact one by up to a bf16 ulp through
+# the bf16 P of its P V product). dS moves by P * delta (pinned in test_oracle_pins), hence
+#   |d dq_qc| <= scale * |delta_q| * sum_k P_qk |K_kc|
+#   |d dk_kc| <= scale * sum_q P_qk |delta_q| |Q_qc|
+# Both sums are oracle outputs (a forward with V := |K|, a backward's dV with dout := bound*|Q|);
+# they are added to the tolerance of dq and dk. For unscaled T5 logits (std 8) they reach ~0.1.
+U_D = 2.0 ** -8
 ATOL = 2e-2
 RTOL = 1e-2
 LSE_ATOL = 1e-3
@@ -46,7 +50,7 @@ def run_gpu(w, x, with_bwd=True, max_seqlen=None, want_dbias=True):
     return {k: (v.float().cpu().numpy() if v is not None else None) for k, v in res.items()}
 
 
-def oracle_problem(w, x):
+def oracle_problem(w, x, d_from_bf16_out=False):
     a = t5_args(w)
     return oracle.Problem(
         wl.bf16_bits(x["q"]), wl.bf16_bits(x["k"]), wl.bf16_bits(x["v"]),
@@ -55,12 +59,12 @@ def oracle_problem(w, x):
         num_buckets=a["num_buckets"], max_distance=a["max_distance"],
         bidirectional=a["bidirectional"],
         slopes=x["slopes"].cpu().numpy() if x["slopes"] is not None else None,
-        causal=w.causal, scale=w.scale)
+        causal=w.causal, scale=w.scale, d_from_bf16_out=d_from_bf16_out)
 
 
-def assert_close(name, got, ref, atol=ATOL, rtol=RTOL):
+def assert_close(name, got, ref, atol=ATOL, rtol=RTOL, slack=0.0):
     err = np.abs(got - ref)
-    lim = atol + rtol * np.abs(ref)
+    lim = atol + rtol * np.abs(ref) + slack
     bad = err > lim
     if bad.any():
         idx = np.unravel_index(np.argmax(err - lim), err.shape)
@@ -77,3 +81,34 @@ def assert_dbias(got, ref):
     lim = 1e-2 * np.abs(ref).max() + 1e-3
     assert (per <= lim).all(), f"dbias per-bucket error {per.max():.3e} > {lim:.3e}"
     return rel
+
+
+def _with(pb, **kw):
+    d = dict(q=pb.q, k=pb.k, v=pb.v, cu_seqlens=pb.cu_seqlens, table=pb.table,
+             num_buckets=pb.num_buckets, max_distance=pb.max_distance,
+             bidirectional=pb.bidirectional, slopes=pb.slopes, causal=pb.causal, scale=pb.scale)
+    d.update(kw)
+    return oracle.Problem(**d)
+
+
+def grad_bounds_full(pb, dout_f64, out_ref):
+    """Per-element slack for dq and dk from the bf16 output entering D (see above)."""
+    b1 = U_D * np.abs(dout_f64 * out_ref).sum(-1)  # [T, H] bound on |delta|
+    pk, _ = oracle.attn_fwd(_with(pb, v=np.abs(pb.k)))
+    dq_slack = pb.scale * b1[..., None] * pk
+    _, _, dk_w, _ = oracle.attn_bwd(pb, b1[..., None] * np.abs(pb.q))
+    return dq_slack, pb.scale * dk_w
+
+
+def grad_bounds_rows(pb, dout_f64, doc, h, qrows, krows):
+    """Same slack for sampled rows of one (doc, head)."""
+    s, e = int(pb.cu_seqlens[doc]), int(pb.cu_seqlens[doc + 1])
+    L = e - s
+    o_all, _ = oracle.attn_fwd_rows(pb, doc, h, list(range(L)))
+    b1 = U_D * np.abs(dout_f64[s:e, h] * o_all).sum(-1)  # [L]
+    pk, _ = oracle.attn_fwd_rows(_with(pb, v=np.abs(pb.k)), doc, h, qrows)
+    dq_slack = pb.scale * b1[np.array(qrows)][:, None] * pk
+    w = np.zeros_like(pb.q)
+    w[s:e, h] = b1[:, None] * np.abs(pb.q[s:e, h])
+    _, _, dk_w, _ = oracle.attn_bwd_rows(pb, w, doc, h, [0], krows)
+    return dq_slack, pb.scale * dk_w

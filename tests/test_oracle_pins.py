@@ -365,3 +365,48 @@ def test_oracle_argument_errors():
     pb = _rand_problem([4], 1, 4, seed=16, t5=(8, 2, True))
     with pytest.raises(ValueError):
         oracle.attn_fwd(pb)  # max_distance inside the exact region
+
+
+@pytest.mark.parametrize("causal,alibi", [(False, False), (True, True)])
+def test_backward_with_bf16_output_statistic_identity(causal, alibi):
+    """With D formed from the bf16-rounded output, the gradients differ from the exact ones by
+    terms linear in delta = D_exact - D_rounded: dq by scale*delta*(P K), dk by
+    scale*sum_q P delta Q, the table gradient by sum of P*delta per bucket; dv is unchanged."""
+    pb = _rand_problem([11, 6], 2, 5, seed=40, t5=(8, 16, not causal), alibi=alibi,
+                       causal=causal, scale=0.9)
+    rng = np.random.default_rng(41)
+    dout = rng.standard_normal(pb.shape)
+    out, _ = oracle.attn_fwd(pb)
+    dq0, dk0, dv0, dt0 = oracle.attn_bwd(pb, dout)
+    pb.d_from_bf16_out = True
+    dq1, dk1, dv1, dt1 = oracle.attn_bwd(pb, dout)
+    pb.d_from_bf16_out = False
+    out_b = torch.from_numpy(out).to(torch.bfloat16).double().numpy()
+    delta = (dout * out).sum(-1) - (dout * out_b).sum(-1)  # [T, H]
+    assert np.abs(delta).max() > 0
+    np.testing.assert_array_equal(dv1, dv0)
+    pk = oracle.Problem(pb.q, pb.k, pb.k, pb.cu_seqlens, table=pb.table,
+                        num_buckets=pb.num_buckets, max_distance=pb.max_distance,
+                        bidirectional=pb.bidirectional, slopes=pb.slopes, causal=causal,
+                        scale=pb.scale)
+    PK, _ = oracle.attn_fwd(pk)
+    np.testing.assert_allclose(dq1 - dq0, pb.scale * delta[..., None] * PK, atol=1e-12)
+    _, _, dv_w, _ = oracle.attn_bwd(pb, delta[..., None] * pb.q)
+    np.testing.assert_allclose(dk1 - dk0, pb.scale * dv_w, atol=1e-12)
+    want = np.zeros_like(dt0)
+    cu = pb.cu_seqlens
+    for i in range(len(cu) - 1):
+        s, e = cu[i], cu[i + 1]
+        L = e - s
+        for h in range(pb.shape[1]):
+            B = _bias_matrix(pb, L, h)
+            S = pb.scale * pb.q[s:e, h] @ pb.k[s:e, h].T + B
+            if causal:
+                S = np.where(np.triu(np.ones((L, L), bool), 1), -np.inf, S)
+            P = np.exp(S - S.max(1, keepdims=True))
+            P /= P.sum(1, keepdims=True)
+            for p in range(L):
+                for r in range(L):
+                    b = exact_bucket(r - p, pb.num_buckets, pb.max_distance, pb.bidirectional)
+                    want[b, h] += P[p, r] * delta[s + p, h]
+    np.testing.assert_allclose(dt1 - dt0, want, atol=1e-12)
