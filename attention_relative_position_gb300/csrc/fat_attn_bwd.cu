@@ -14,16 +14,17 @@
 //                tcgen05 with fp32 accumulators in TMEM; dK and dV stay in TMEM for the whole
 //                walk.
 //   warps 0-7    two warpgroups, each owning half of the query columns: P^T = 2^(x - lse),
-//                written to TMEM as bf16; dS^T = P^T (dP^T - D), written to shared memory in the
-//                128-byte-swizzled layout the MMAs read; bias-gradient partial sums.
+//                written to TMEM as bf16 (own columns, for dV) and fp32 (over S^T);
+//                dS^T = P^T (dP^T - D), written to shared memory in the 128-byte-swizzled
+//                layout the MMAs read; bias-gradient partial sums.
 //   warps 8-11   drain dQ_i from TMEM into the fp32 dQ accumulator with vector reductions, then
 //                write dK, dV.
 //   warps 14-15  idle; with warps 12-13 they form the fourth warpgroup, whose registers go to
-//                the P/dS warpgroups (168 + 168 + 112 + 64 = 512 per SM sub-partition).
+//                the P/dS warpgroups (152 + 152 + 120 + 88 = 512 per SM sub-partition).
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
-// the other tiles add into a shared-memory array indexed by delta (one conflict-free shared
-// reduction per element, consecutive lanes hit consecutive deltas); at the end the CTA maps
-// deltas to buckets and issues one global atomic per (bucket, head).
+// the other tiles reduce each 32 x 32 block along its diagonals with warp shuffles and add the
+// sums into a shared-memory array indexed by delta; at the end the CTA maps deltas to buckets
+// and issues one global atomic per (bucket, head).
 // Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, dK and dV fit
 // the 512 TMEM columns together.
 #include <cstdio>
@@ -32,7 +33,7 @@
 
 namespace fat {
 
-template <int D>
+template <int D, int NSTAGES>
 struct BwdCfg {
   static constexpr int BQ = (D == 64) ? 128 : 64;
   static constexpr int HALF = BQ / 2;           // query columns per softmax warpgroup
@@ -41,7 +42,7 @@ struct BwdCfg {
   static constexpr int KTILE = DB * KBLK;       // K or V tile: 128 keys x D
   static constexpr int QBLK = BQ * 128;         // BQ rows x 64 bf16
   static constexpr int QTILE = DB * QBLK;       // Q_i or dO_i tile
-  static constexpr int NS = 2;
+  static constexpr int NS = NSTAGES;  // Q/dO ring depth
   static constexpr int DSBLK = 128 * 128;       // 128 keys x 64 queries bf16
   static constexpr int DSTILE = (BQ / 64) * DSBLK;
   static constexpr int OFF_K = 0;
@@ -54,24 +55,107 @@ struct BwdCfg {
   static constexpr int OFF_BACC = OFF_BAR + 256;        // per-bucket sums, 256 floats
   static constexpr int OFF_LUT = OFF_BACC + 256 * 4;    // lut[lut_len], then diag[lut_len]
   static constexpr int NTHREADS = 512;
-  static constexpr int COL_S = 0, COL_DP = BQ, COL_DQ = 2 * BQ;
+  // TMEM columns: S^T and dP^T (BQ each), dQ (64), P^T as packed bf16 pairs (BQ/2), dK, dV.
+  // P has its own columns so that the next S^T product cannot overwrite it while the dS pass
+  // still reads it.
+  static constexpr int COL_S = 0, COL_DP = BQ, COL_DQ = 2 * BQ, COL_P = 2 * BQ + 64;
   static constexpr int COL_DK = 512 - 2 * D, COL_DV = 512 - D;
+  static_assert(COL_P + BQ / 2 <= COL_DK, "TMEM column budget");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BQ, 0, 0);
   static constexpr uint32_t IDESC_DKV = idesc_bf16_f32(128, D, 0, 1);
   static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 64, 1, 1);
 };
 
+template <int D, int NS>
+size_t bwd_smem_bytes_t(int lut_len) {
+  return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 8;
+}
+// Three Q/dO stages when they fit next to the bias table, else two.
+int bwd_stages(int head_dim, int lut_len) {
+  const size_t three = head_dim == 64 ? bwd_smem_bytes_t<64, 3>(lut_len)
+                                      : bwd_smem_bytes_t<128, 3>(lut_len);
+  return three <= (size_t)kSmemLimit ? 3 : 2;
+}
 size_t bwd_smem_bytes(int head_dim, int lut_len) {
-  size_t base = head_dim == 64 ? (size_t)BwdCfg<64>::OFF_LUT : (size_t)BwdCfg<128>::OFF_LUT;
-  return 1024 + base + (size_t)lut_len * 8;
+  const int ns = bwd_stages(head_dim, lut_len);
+  if (head_dim == 64)
+    return ns == 3 ? bwd_smem_bytes_t<64, 3>(lut_len) : bwd_smem_bytes_t<64, 2>(lut_len);
+  return ns == 3 ? bwd_smem_bytes_t<128, 3>(lut_len) : bwd_smem_bytes_t<128, 2>(lut_len);
 }
 
-template <int D>
+// P^T of one 32-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
+// Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Bias forms are compile-time so
+// the unrolled element loop carries no branches: BIAS 0 = lookup table (lut_row[-j]),
+// 1 = constant rowc, 2 = rowc + kq * j.
+template <int BIAS, bool MASK>
+__device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[32], uint32_t (&pk)[16],
+                                            const float4 *lse4, const float *lut_row, int jc,
+                                            float rowc, float kq, float scale_log2, int lo_j,
+                                            int hi_j) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 l4 = lse4[g];
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * g + e;
+      const int j = jc + t;
+      float b;
+      if (BIAS == 0)
+        b = lut_row[-j];
+      else if (BIAS == 1)
+        b = rowc;
+      else
+        b = fmaf(kq, (float)j, rowc);
+      float x = fmaf(__uint_as_float(raw[t]), scale_log2, b);
+      if (MASK) x = (j >= lo_j && j < hi_j) ? x : -INFINITY;
+      pr[e] = ex2(x - lv[e]);
+    }
+    pk[2 * g] = pack_bf16x2(pr[0], pr[1]);
+    pk[2 * g + 1] = pack_bf16x2(pr[2], pr[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) raw[4 * g + e] = __float_as_uint(pr[e]);
+  }
+}
+
+// dS^T of one 32-column chunk: ds = P (dP - D), packed to bf16 pairs; returns the chunk's sum.
+// NEAR also reduces the 32 x 32 block along its diagonals: lane m ends with the sum over
+// delta = base + m in acc_a and over delta = base + m - 32 in acc_b.
+template <bool NEAR>
+__device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[32], const uint32_t (&dp)[32],
+                                              const float4 *dvs4, uint32_t (&pk)[16], int lane,
+                                              float &acc_a, float &acc_b) {
+  float part = 0.f;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 d4 = dvs4[g];
+    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+    float ds[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * g + e;
+      ds[e] = __uint_as_float(pf[t]) * (__uint_as_float(dp[t]) - dv[e]);
+      if (NEAR) {
+        const float y = __shfl_sync(0xffffffffu, ds[e], (lane + t) & 31);
+        const bool lo = lane + t < 32;
+        acc_a += lo ? y : 0.f;
+        acc_b += lo ? 0.f : y;
+      }
+    }
+    part += (ds[0] + ds[1]) + (ds[2] + ds[3]);
+    pk[2 * g] = pack_bf16x2(ds[0], ds[1]);
+    pk[2 * g + 1] = pack_bf16x2(ds[2], ds[3]);
+  }
+  return part;
+}
+
+template <int D, int NSTAGES>
 __global__ void __launch_bounds__(512, 1)
     fat_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, NSTAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -155,12 +239,14 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_BWD, p.timeout_ns};
   float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (softmax warps)
-  if (warp >= 12) regs_dec<64>();
-  else if (warp >= 8) regs_dec<112>();
+  if (warp >= 12) regs_dec<88>();
+  else if (warp >= 8) regs_dec<120>();
 
   if (warp == 12) {
     // ------------------------------------------------------------------ producer
-    int last_q[C::NS] = {-1, -1};
+    int last_q[C::NS];
+#pragma unroll
+    for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
     bool kv_issued = false;
     if (!(p.debug_flags & 2)) {
       if (lane == 0) {
@@ -173,14 +259,21 @@ __global__ void __launch_bounds__(512, 1)
       }
       for (int it = 0; it < nq; ++it) {
         const int st = it % C::NS, u = it / C::NS;
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(qd_empty + st, (u - 1) & 1, wd))) break;
         const int qs = (i0 + it) * C::BQ;
-        for (int c = lane; c < C::BQ; c += 32) {
-          const int q = qs + c;
-          const bool valid = q < L;
+        // fetch this tile's row statistics before waiting for the stage to be free
+        float lv[C::BQ / 32], dv[C::BQ / 32];
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          const int q = qs + lane + 32 * k;
           const size_t idx = (size_t)h * T + seq_start + q;
-          s_lse2[st * C::BQ + c] = valid ? __ldg(p.lse + idx) * kLog2e : 0.f;
-          s_dvec[st * C::BQ + c] = valid ? __ldg(p.dvec + idx) : 0.f;
+          lv[k] = q < L ? __ldg(p.lse + idx) * kLog2e : 0.f;
+          dv[k] = q < L ? __ldg(p.dvec + idx) : 0.f;
+        }
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(qd_empty + st, (u - 1) & 1, wd))) break;
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          s_lse2[st * C::BQ + lane + 32 * k] = lv[k];
+          s_dvec[st * C::BQ + lane + 32 * k] = dv[k];
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(qd_full + st, 2 * C::QTILE);
@@ -190,7 +283,9 @@ __global__ void __launch_bounds__(512, 1)
             tma_load_3d(&tm_do, qd_full + st, sDO + st * C::QTILE + b * C::QBLK, 64 * b, h,
                         seq_start + qs);
           }
-          if (st == 0) last_q[0] = u; else last_q[1] = u;
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == st) last_q[x] = u;
         } else {
           mbar_arrive(qd_full + st);
         }
@@ -198,8 +293,9 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (lane == 0) {
       if (kv_issued) mbar_wait_teardown(kv_full, 0, kTeardownNs);
-      if (last_q[0] >= 0) mbar_wait_teardown(qd_full, last_q[0] & 1, kTeardownNs);
-      if (last_q[1] >= 0) mbar_wait_teardown(qd_full + 1, last_q[1] & 1, kTeardownNs);
+#pragma unroll
+      for (int x = 0; x < C::NS; ++x)
+        if (last_q[x] >= 0) mbar_wait_teardown(qd_full + x, last_q[x] & 1, kTeardownNs);
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------------ MMA issuer
@@ -220,7 +316,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int k16 = 0; k16 < C::BQ / 16; ++k16) {
           const int q0 = 16 * k16;
-          const uint32_t a_t = tmem + C::COL_S + (q0 / C::HALF) * C::HALF + (q0 % C::HALF) / 2;
+          const uint32_t a_t = tmem + C::COL_P + q0 / 2;
           const uint64_t b = sw128_desc(aDO + st * C::QTILE + k16 * 2048, C::QBLK, 1024);
           mma_bf16_ts(tmem + C::COL_DV, a_t, b, C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
         }
@@ -255,20 +351,25 @@ __global__ void __launch_bounds__(512, 1)
         issue_qk(aV, aDO, C::COL_DP);
         mma_commit(dp_full);
       }
+      // Per query tile: dV as soon as P^T is in TMEM; once dS^T is in shared memory (so S^T
+      // and dP^T have been consumed) the next tile's S^T and dP^T go first, then dK and dQ,
+      // so the P/dS warpgroups wait for one product only.
       for (int it = 0; ok && it < nq; ++it) {
         const int st = it % C::NS;
         const int stn = (it + 1) % C::NS, un = (it + 1) / C::NS;
         if (!mbar_wait(p_ready, it & 1, wd)) { ok = false; break; }
         tc_fence_after();
         issue_dv(st, it > 0);
+        if (!mbar_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+        tc_fence_after();
         if (it + 1 < nq) {
           if (!mbar_wait(qd_full + stn, un & 1, wd)) { ok = false; break; }
           tc_fence_after();
           issue_qk(aK, aQ + stn * C::QTILE, C::COL_S);
           mma_commit(s_full);
+          issue_qk(aV, aDO + stn * C::QTILE, C::COL_DP);
+          mma_commit(dp_full);
         }
-        if (!mbar_wait(ds_ready, it & 1, wd)) { ok = false; break; }
-        tc_fence_after();
         issue_dk(it & 1, st, it > 0);
         if (it >= 1) {
           if (!mbar_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
@@ -278,10 +379,6 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(dq_full);
         mma_commit(ds_empty + (it & 1));
         mma_commit(qd_empty + st);
-        if (it + 1 < nq) {
-          issue_qk(aV, aDO + stn * C::QTILE, C::COL_DP);
-          mma_commit(dp_full);
-        }
       }
       if (ok) mma_commit(dkdv_done);
       mma_commit(mma_done);
@@ -289,18 +386,18 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P / dS warpgroups
-    regs_inc<168>();
+    regs_inc<152>();
     const int wg = warp >> 2;
     const int r = tid & 127;
     const int c0 = wg * C::HALF;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::COL_S + c0;
+    const uint32_t tP = tmem + lane_off + C::COL_P + c0 / 2;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + c0;
     const int krow = ks + r;
     const bool row_valid = krow < L;
     const FarBias fb = far_bias_dev(h, H, p.bias);
     const bool has_slopes = p.bias.slopes != nullptr;
-    float pv[C::HALF];
     for (int it = 0; it < nq; ++it) {
       const int st = it % C::NS;
       const int qs = (i0 + it) * C::BQ;
@@ -329,61 +426,63 @@ __global__ void __launch_bounds__(512, 1)
       }
       const bool linear = has_slopes && (side == 1 || side == 2);
       const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
-      const float *lse2 = s_lse2 + st * C::BQ;
-      const float *dvs = s_dvec + st * C::BQ;
+      const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
+      const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
       // ---- P^T = 2^(x - lse2) for this warpgroup's query columns
+      const int bias_mode = side == 0 ? 0 : (linear ? 2 : 1);
+      const float *lut_row = lut + lut_base;
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t raw[32];
+        uint32_t raw[32], pk[16];
         tmem_ld32(tS + 32 * c, raw);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int j = c0 + 32 * c + i;
-          float b;
-          if (side == 0)
-            b = lut[lut_base - j];
-          else
-            b = linear ? fmaf(kq, (float)j, rowc) : rowc;
-          float x = fmaf(__uint_as_float(raw[i]), p.scale_log2, b);
-          if (need_mask) x = (j >= lo_j && j < hi_j) ? x : -INFINITY;
-          const float pr = ex2(x - lse2[j]);
-          pv[32 * c + i] = pr;
-          if (i & 1) pk[i >> 1] = pack_bf16x2(pv[32 * c + i - 1], pr);
+        const int jc = c0 + 32 * c;
+        const float4 *l4 = lse4 + 8 * c;
+        const float sl = p.scale_log2;
+        switch (bias_mode * 2 + (need_mask ? 1 : 0)) {
+          case 0: bwd_p_chunk<0, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          case 1: bwd_p_chunk<0, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          case 2: bwd_p_chunk<1, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          case 3: bwd_p_chunk<1, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          case 4: bwd_p_chunk<2, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          default: bwd_p_chunk<2, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
         }
-        tmem_st16(tS + 16 * c, pk);
+        tmem_st16(tP + 16 * c, pk);   // bf16 P^T: A operand of the dV product
+        tmem_st32(tS + 32 * c, raw);  // fp32 P^T over S^T: read back by the dS pass
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
-      // ---- dS^T = P^T (dP^T - D), to shared memory (bf16, swizzled) for the dK / dQ MMAs
+      // ---- dS^T = P^T (dP^T - D), to shared memory (bf16, swizzled) for the dK / dQ MMAs.
+      // P^T is read back in fp32 from where S^T was (the next S^T is issued only after this
+      // pass). Table gradient: far tiles add into one register per side; near tiles sum each
+      // 32 x 32 block along its diagonals with warp shuffles (lane m collects deltas base + m
+      // and base + m - 32) and add two values per lane into the per-delta array.
       if (!__all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd))) break;
       if (it >= 2 &&
           !__all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)))
         break;
       tc_fence_after();
       uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
+      const bool near_db = do_dbias && side == 0;
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t raw[32];
+        uint32_t raw[32], pf[32];
+        tmem_ld32(tS + 32 * c, pf);
         tmem_ld32(tDP + 32 * c, raw);
-        float dsv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int j = c0 + 32 * c + i;
-          dsv[i] = pv[32 * c + i] * (__uint_as_float(raw[i]) - dvs[j]);
-          if (do_dbias) {
-            if (side == 0)
-              red_add_shared(diag + (lut_base - j), dsv[i]);
-            else if (side == 1)
-              acc_pos += dsv[i];
-            else
-              acc_neg += dsv[i];
-          }
-        }
         uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(dsv[2 * i], dsv[2 * i + 1]);
+        float acc_a = 0.f, acc_b = 0.f;
+        const float part = near_db ? bwd_ds_chunk<true>(pf, raw, dvs4 + 8 * c, pk, lane, acc_a, acc_b)
+                                   : bwd_ds_chunk<false>(pf, raw, dvs4 + 8 * c, pk, lane, acc_a, acc_b);
+        if (near_db) {
+          // delta of (row of lane m, column t) = base + m - t
+          const int base = d0 + 32 * (warp & 3) - (c0 + 32 * c) - p.bias.lut_lo;
+          red_add_shared(diag + base + lane, acc_a);
+          if (lane > 0) red_add_shared(diag + base + lane - 32, acc_b);
+        } else if (side == 1) {
+          acc_pos += part;
+        } else if (side == 2) {
+          acc_neg += part;
+        }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {  // 4 groups of 8 queries = 16 bytes each
           const int j0 = c0 + 32 * c + 8 * g;
@@ -506,23 +605,22 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   (void)out;
   CUtensorMap mq, mk, mv, mdo;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
-  const int bq = head_dim == 64 ? BwdCfg<64>::BQ : BwdCfg<128>::BQ;
+  const int bq = head_dim == 64 ? BwdCfg<64, 2>::BQ : BwdCfg<128, 2>::BQ;
   if (make_tmap_thd(&mq, q, T, H, head_dim, bq) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
       make_tmap_thd(&mv, v, T, H, head_dim, 128) || make_tmap_thd(&mdo, dout, T, H, head_dim, bq))
     return (int)cudaErrorInvalidValue;
   const size_t smem = bwd_smem_bytes(head_dim, p.bias.lut_len);
+  const int ns = bwd_stages(head_dim, p.bias.lut_len);
   dim3 grid((max_seqlen + 127) / 128, H, p.seq.num_seqs);
   cudaError_t e;
+  auto go = [&](auto kernel) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) kernel<<<grid, 512, smem, stream>>>(mq, mk, mv, mdo, p);
+  };
   if (head_dim == 64) {
-    e = cudaFuncSetAttribute(fat_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e == cudaSuccess)
-      fat_bwd_kernel<64><<<grid, BwdCfg<64>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
   } else {
-    e = cudaFuncSetAttribute(fat_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e == cudaSuccess)
-      fat_bwd_kernel<128><<<grid, BwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (ns == 3) go(fat_bwd_kernel<128, 3>); else go(fat_bwd_kernel<128, 2>);
   }
   if (e != cudaSuccess) {
     set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
@@ -532,9 +630,9 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
     if (head_dim == 64)
-      cudaFuncGetAttributes(&fa, fat_bwd_kernel<64>);
+      cudaFuncGetAttributes(&fa, fat_bwd_kernel<64, 3>);
     else
-      cudaFuncGetAttributes(&fa, fat_bwd_kernel<128>);
+      cudaFuncGetAttributes(&fa, fat_bwd_kernel<128, 3>);
     char msg[160];
     snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
              cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,

@@ -11,7 +11,7 @@
 //               accumulators in tensor memory (TMEM); P_t is read from TMEM where the softmax
 //               warps wrote it over S_t.
 //   warps 10-11 idle (they complete the third warpgroup, which gives its registers to the
-//               softmax warpgroups: 224 + 224 + 56 per sub-partition fits its 512 x 32 registers).
+//               softmax warpgroups: 216 + 216 + 72 per sub-partition fits its 512 x 32 registers).
 //   warps 0-7   two softmax warpgroups, one per Q tile; thread i owns row i of its tile (TMEM
 //               lane i), so row max/sum need no shuffles. Bias: closed form on tiles that lie
 //               beyond the T5 saturation distance, a per-CTA lookup table over delta on the rest.
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
 
-  if (warp >= 8) regs_dec<56>();
+  if (warp >= 8) regs_dec<72>();
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
-    regs_inc<224>();
+    regs_inc<216>();
     const int t = warp >> 2;
     if (t < ntile) {
       const int nk = t == 0 ? nkv0 : nkv1;
