@@ -70,6 +70,9 @@ def load(path: Optional[str] = None):
     lib.fat_attn_bwd_main.restype = i32
     lib.fat_attn_bwd_finalize.argtypes = [S, vp, ctypes.c_size_t, f32, vp]
     lib.fat_attn_bwd_finalize.restype = i32
+    lib.fat_attn_bwd_noalloc.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp,
+                                         vp, vp, vp, vp, vp, vp]
+    lib.fat_attn_bwd_noalloc.restype = i32
     lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.fat_attn_get_device_error.restype = i32
     lib.fat_attn_strerror.argtypes = [i32]
@@ -222,6 +225,26 @@ def fat_attn_bwd_stages(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, wo
         raise FatAttnError(rc, "fat_attn_bwd_finalize")
     if between is not None:
         between(2)
+    return dq, dk, dv, dbias_table
+
+
+def fat_attn_bwd_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, dq, dk, dv,
+                         dbias_table=None, bias_table=None, num_buckets: int = 0,
+                         max_distance: int = 0, bidirectional: bool = True, alibi_slopes=None,
+                         causal: bool = False, softmax_scale: float = 1.0, stream=None):
+    """The backward with the library's built-in scratch instead of a workspace, for callers that
+    cannot allocate device memory (see fat_attn_bwd_noalloc in include/fat_attn.h). All output
+    buffers are supplied by the caller; nothing is allocated here."""
+    lib = load()
+    T, H, d = q.shape
+    sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
+    rc = lib.fat_attn_bwd_noalloc(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                                  int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                                  _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                                  float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias_table))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_attn_bwd_noalloc")
     return dq, dk, dv, dbias_table
 
 

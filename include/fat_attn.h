@@ -128,6 +128,31 @@ int fat_attn_bwd_main(const fat_shape_t *shape, const void *q, const void *k, co
 int fat_attn_bwd_finalize(const fat_shape_t *shape, const void *workspace,
                           size_t workspace_bytes, float softmax_scale, void *dq);
 
+/*
+ * Backward for callers that cannot allocate device memory (no counterpart in the paper; an
+ * addition of this library). Examples: an application that owns every allocation on the GPU and
+ * hands libraries only fixed, caller-owned buffers, or a plug-in inside a framework whose
+ * allocator must not be bypassed and which offers no way to request scratch space. Such a caller
+ * cannot provide the workspace fat_attn_bwd needs, so this entry point uses a scratch array of
+ * FAT_NOALLOC_SCRATCH_BYTES that the library keeps in device memory: every GPU that loads the
+ * library holds it until the process exits. Otherwise it is fat_attn_bwd (same arguments minus
+ * the workspace, same results, same errors); it allocates nothing and calls nothing that does.
+ *   - Limit: problems whose fat_attn_bwd_workspace_size() exceeds FAT_NOALLOC_SCRATCH_BYTES are
+ *     rejected with FAT_EUNSUPPORTED before any work is enqueued (fat_attn_last_error_message
+ *     says why); e.g. T * H * (d + 1) * 4 bytes must fit, about 8 M elements of q at d = 64.
+ *   - The first call on a device looks up the array's device address with that device current;
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps whatever the last call left there
+ *     (each call zeroes the part that must start at zero). Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on it and must be serialised by the caller.
+ */
+#define FAT_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fat_attn_bwd_noalloc(const fat_shape_t *shape, const void *q, const void *k, const void *v,
+                         const float *bias_table, int num_buckets, int max_distance,
+                         int bidirectional, const float *alibi_slopes, const int32_t *cu_seqlens,
+                         int causal, float softmax_scale, const void *out, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, float *dbias_table);
+
 /* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
    FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
 int fat_attn_get_device_error(void *stream, int *bits);
