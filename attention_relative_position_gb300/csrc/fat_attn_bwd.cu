@@ -7,26 +7,25 @@
 //
 // GB300 design: one CTA per (document, head, 128-key tile); it walks the query tiles of the
 // document (only those at or after the key tile when causal). Everything is computed in the
-// key-major frame (TMEM lane = key row):
-//   warp 12      TMA producer: K, V once; Q_i, dO_i (and lse_i, D_i) through a 2-stage ring.
-//   warp 13      MMA issuer: S^T = K Q_i^T, dP^T = V dO_i^T, dV += P^T dO_i (P^T from TMEM),
+// key-major frame (TMEM lane = key row). Five warpgroups, one warp of each per SM
+// sub-partition:
+//   warps 0-15   four P/dS warpgroups, each owning a quarter of the query columns of a tile:
+//                P^T = 2^(x - lse) written to TMEM as bf16 (own columns, the A operand of dV)
+//                and fp32 (over S^T, read back by the dS pass); dS^T = P^T (dP^T - D) written
+//                to shared memory in the 128-byte-swizzled layout the MMAs read; table-gradient
+//                partial sums; a quarter of each dQ tile drained from TMEM into the fp32 dQ
+//                accumulator with vector reductions; a quarter of dK, dV at the end.
+//   warp 16      TMA producer: K, V once; Q_i, dO_i (and lse_i, D_i) through a 2-3 stage ring.
+//   warp 17      MMA issuer: S^T = K Q_i^T, dP^T = V dO_i^T, dV += P^T dO_i (P^T from TMEM),
 //                dK += dS^T Q_i, and dQ_i = dS K (d = 64) or dQ_i^T = K^T dS^T (d = 128), all
-//                tcgen05 with fp32 accumulators in TMEM; dK and dV stay in TMEM for the whole
-//                walk.
-//   warps 0-7    two warpgroups, each owning half of the query columns: P^T = 2^(x - lse),
-//                written to TMEM as bf16 (own columns, for dV) and fp32 (over S^T);
-//                dS^T = P^T (dP^T - D), written to shared memory in the 128-byte-swizzled
-//                layout the MMAs read; bias-gradient partial sums.
-//   warps 8-11   drain dQ_i from TMEM into the fp32 dQ accumulator with vector reductions, then
-//                write dK, dV.
-//   warps 14-15  idle; with warps 12-13 they form the fourth warpgroup, whose registers go to
-//                the P/dS warpgroups (152 + 152 + 120 + 88 = 512 per SM sub-partition).
+//                tcgen05 with fp32 accumulators in TMEM; dK and dV stay in TMEM for the walk.
+//   warps 18-19  idle (they complete the fifth warpgroup).
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
-// the other tiles reduce each 32 x 32 block along its diagonals with warp shuffles and add the
+// the other tiles reduce each 32-row block along its diagonals with warp shuffles and add the
 // sums into a shared-memory array indexed by delta; at the end the CTA maps deltas to buckets
 // and issues one global atomic per (bucket, head).
-// Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, dK and dV fit
-// the 512 TMEM columns together.
+// Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, P, dK and dV
+// fit the 512 TMEM columns together.
 #include <cstdio>
 
 #include "fat_attn_internal.cuh"
@@ -36,13 +35,13 @@ namespace fat {
 template <int D, int NSTAGES>
 struct BwdCfg {
   static constexpr int BQ = (D == 64) ? 128 : 64;
-  static constexpr int HALF = BQ / 2;           // query columns per softmax warpgroup
+  static constexpr int QW = BQ / 4;             // query columns per P/dS warpgroup
   static constexpr int DB = D / 64;
   static constexpr int KBLK = 128 * 128;        // 128 rows x 64 bf16
   static constexpr int KTILE = DB * KBLK;       // K or V tile: 128 keys x D
   static constexpr int QBLK = BQ * 128;         // BQ rows x 64 bf16
   static constexpr int QTILE = DB * QBLK;       // Q_i or dO_i tile
-  static constexpr int NS = NSTAGES;  // Q/dO ring depth
+  static constexpr int NS = NSTAGES;            // Q/dO ring depth
   static constexpr int DSBLK = 128 * 128;       // 128 keys x 64 queries bf16
   static constexpr int DSTILE = (BQ / 64) * DSBLK;
   static constexpr int OFF_K = 0;
@@ -54,10 +53,11 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
   static constexpr int OFF_BACC = OFF_BAR + 256;        // per-bucket sums, 256 floats
   static constexpr int OFF_LUT = OFF_BACC + 256 * 4;    // lut[lut_len], then diag[lut_len]
-  static constexpr int NTHREADS = 512;
+  static constexpr int NTHREADS = 640;
+  static constexpr int NCOMP = 512;                     // threads of the P/dS warpgroups
   // TMEM columns: S^T and dP^T (BQ each), dQ (64), P^T as packed bf16 pairs (BQ/2), dK, dV.
-  // P has its own columns so that the next S^T product cannot overwrite it while the dS pass
-  // still reads it.
+  // P has its own columns so that the next S^T product cannot overwrite it while the dV
+  // product may still read it.
   static constexpr int COL_S = 0, COL_DP = BQ, COL_DQ = 2 * BQ, COL_P = 2 * BQ + 64;
   static constexpr int COL_DK = 512 - 2 * D, COL_DV = 512 - D;
   static_assert(COL_P + BQ / 2 <= COL_DK, "TMEM column budget");
@@ -83,17 +83,35 @@ size_t bwd_smem_bytes(int head_dim, int lut_len) {
   return ns == 3 ? bwd_smem_bytes_t<128, 3>(lut_len) : bwd_smem_bytes_t<128, 2>(lut_len);
 }
 
-// P^T of one 32-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
+// TMEM <-> registers for W columns (W = 16 or 32) of this warp's 32 lanes.
+template <int W>
+__device__ __forceinline__ void tmem_ldw(uint32_t taddr, uint32_t (&r)[W]) {
+  if constexpr (W == 32)
+    tmem_ld32(taddr, r);
+  else
+    tmem_ld16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_stw(uint32_t taddr, const uint32_t (&r)[W]) {
+  if constexpr (W == 32)
+    tmem_st32(taddr, r);
+  else if constexpr (W == 16)
+    tmem_st16(taddr, r);
+  else
+    tmem_st8(taddr, r);
+}
+
+// P^T of one W-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
 // Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Bias forms are compile-time so
 // the unrolled element loop carries no branches: BIAS 0 = lookup table (lut_row[-j]),
 // 1 = constant rowc, 2 = rowc + kq * j.
-template <int BIAS, bool MASK>
-__device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[32], uint32_t (&pk)[16],
+template <int W, int BIAS, bool MASK>
+__device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W / 2],
                                             const float4 *lse4, const float *lut_row, int jc,
                                             float rowc, float kq, float scale_log2, int lo_j,
                                             int hi_j) {
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
+  for (int g = 0; g < W / 4; ++g) {
     const float4 l4 = lse4[g];
     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
     float pr[4];
@@ -119,16 +137,17 @@ __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[32], uint32_t (&pk)[
   }
 }
 
-// dS^T of one 32-column chunk: ds = P (dP - D), packed to bf16 pairs; returns the chunk's sum.
-// NEAR also reduces the 32 x 32 block along its diagonals: lane m ends with the sum over
-// delta = base + m in acc_a and over delta = base + m - 32 in acc_b.
-template <bool NEAR>
-__device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[32], const uint32_t (&dp)[32],
-                                              const float4 *dvs4, uint32_t (&pk)[16], int lane,
-                                              float &acc_a, float &acc_b) {
+// dS^T of one W-column chunk (columns T0 .. T0+W-1 of a 32-column group): ds = P (dP - D),
+// packed to bf16 pairs; returns the chunk's sum. NEAR also reduces the 32-row block along its
+// diagonals: lane m accumulates the sum over delta = base + m in acc_a and over
+// delta = base + m - 32 in acc_b (base = delta of lane 0, column 0 of the group).
+template <int W, bool NEAR, int T0>
+__device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uint32_t (&dp)[W],
+                                              const float4 *dvs4, uint32_t (&pk)[W / 2],
+                                              int lane, float &acc_a, float &acc_b) {
   float part = 0.f;
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
+  for (int g = 0; g < W / 4; ++g) {
     const float4 d4 = dvs4[g];
     const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
     float ds[4];
@@ -137,8 +156,8 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[32], const ui
       const int t = 4 * g + e;
       ds[e] = __uint_as_float(pf[t]) * (__uint_as_float(dp[t]) - dv[e]);
       if (NEAR) {
-        const float y = __shfl_sync(0xffffffffu, ds[e], (lane + t) & 31);
-        const bool lo = lane + t < 32;
+        const float y = __shfl_sync(0xffffffffu, ds[e], (lane + T0 + t) & 31);
+        const bool lo = lane + T0 + t < 32;
         acc_a += lo ? y : 0.f;
         acc_b += lo ? 0.f : y;
       }
@@ -151,11 +170,12 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[32], const ui
 }
 
 template <int D, int NSTAGES>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(640, 1)
     fat_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
   using C = BwdCfg<D, NSTAGES>;
+  constexpr int QW = C::QW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -206,22 +226,22 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 256);
-    mbar_init(ds_ready, 256);
+    mbar_init(p_ready, C::NCOMP);
+    mbar_init(ds_ready, C::NCOMP);
     mbar_init(ds_empty, 1);
     mbar_init(ds_empty + 1, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, C::NCOMP);
     mbar_init(dkdv_done, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == 17) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 12 && lane == 0) {
+  if (warp == 16 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -238,11 +258,9 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_BWD, p.timeout_ns};
-  float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (softmax warps)
-  if (warp >= 12) regs_dec<88>();
-  else if (warp >= 8) regs_dec<120>();
+  float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (P/dS warps)
 
-  if (warp == 12) {
+  if (warp == 16) {
     // ------------------------------------------------------------------ producer
     int last_q[C::NS];
 #pragma unroll
@@ -297,7 +315,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int x = 0; x < C::NS; ++x)
         if (last_q[x] >= 0) mbar_wait_teardown(qd_full + x, last_q[x] & 1, kTeardownNs);
     }
-  } else if (warp == 13) {
+  } else if (warp == 17) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO);
@@ -315,10 +333,9 @@ __global__ void __launch_bounds__(512, 1)
         // dV[key][c] += sum_q P^T[key][q] dO[q][c]; A = P^T in TMEM, B = dO MN-major
 #pragma unroll
         for (int k16 = 0; k16 < C::BQ / 16; ++k16) {
-          const int q0 = 16 * k16;
-          const uint32_t a_t = tmem + C::COL_P + q0 / 2;
           const uint64_t b = sw128_desc(aDO + st * C::QTILE + k16 * 2048, C::QBLK, 1024);
-          mma_bf16_ts(tmem + C::COL_DV, a_t, b, C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b, C::IDESC_DKV,
+                      (acc || k16 > 0) ? 1u : 0u);
         }
       };
       auto issue_dk = [&](int buf, int st, bool acc) {
@@ -384,25 +401,56 @@ __global__ void __launch_bounds__(512, 1)
       mma_commit(mma_done);
       mbar_wait_teardown(mma_done, 0, kTeardownNs);
     }
-  } else if (warp < 8) {
+  } else if (warp < 16) {
     // ------------------------------------------------------------------ P / dS warpgroups
-    regs_inc<152>();
     const int wg = warp >> 2;
     const int r = tid & 127;
-    const int c0 = wg * C::HALF;
+    const int c0 = wg * QW;  // this warpgroup's first query column
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::COL_S + c0;
     const uint32_t tP = tmem + lane_off + C::COL_P + c0 / 2;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + c0;
+    const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
     const int krow = ks + r;
     const bool row_valid = krow < L;
     const FarBias fb = far_bias_dev(h, H, p.bias);
     const bool has_slopes = p.bias.slopes != nullptr;
+
+    // dQ tile `it` (quarter of its 64 columns) into the fp32 accumulator
+    auto drain_dq = [&](int it) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wd))) return false;
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tDQ, v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int qs = (i0 + it) * C::BQ;
+      if (D == 64) {  // lane = query row, columns = channels 16*wg ..
+        const int q = qs + r;
+        if (q < L) {
+          float *dst = p.dq_acc + ((size_t)(seq_start + q) * H + h) * D + 16 * wg;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            red_add_v4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                       __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        }
+      } else {  // lane = channel, columns = query rows 16*wg ..
+        float *dst = p.dq_acc + ((size_t)(seq_start + qs + 16 * wg) * H + h) * D + r;
+        const size_t step = (size_t)H * D;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (qs + 16 * wg + j < L) red_add(dst + j * step, __uint_as_float(v[j]));
+      }
+      return true;
+    };
+
+    bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int st = it % C::NS;
       const int qs = (i0 + it) * C::BQ;
-      if (!__all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd))) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
+           __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd));
+      if (!ok) break;
       tc_fence_after();
       const int d0 = ks - qs;  // delta of (key row 0, query column 0)
       const bool need_mask = (ks + 128 > L) || (qs + C::BQ > L) || (p.causal && d0 + 127 > 0);
@@ -428,26 +476,28 @@ __global__ void __launch_bounds__(512, 1)
       const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
       const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
       const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
-      // ---- P^T = 2^(x - lse2) for this warpgroup's query columns
-      const int bias_mode = side == 0 ? 0 : (linear ? 2 : 1);
-      const float *lut_row = lut + lut_base;
-#pragma unroll
-      for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t raw[32], pk[16];
-        tmem_ld32(tS + 32 * c, raw);
-        const int jc = c0 + 32 * c;
-        const float4 *l4 = lse4 + 8 * c;
+      // ---- P^T = 2^(x - lse2) for this warpgroup's query columns, 16 at a time
+      {
+        const float *lut_row = lut + lut_base;
         const float sl = p.scale_log2;
-        switch (bias_mode * 2 + (need_mask ? 1 : 0)) {
-          case 0: bwd_p_chunk<0, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          case 1: bwd_p_chunk<0, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          case 2: bwd_p_chunk<1, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          case 3: bwd_p_chunk<1, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          case 4: bwd_p_chunk<2, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          default: bwd_p_chunk<2, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+        const int mode = (side == 0 ? 0 : (linear ? 2 : 1)) * 2 + (need_mask ? 1 : 0);
+#pragma unroll
+        for (int sub = 0; sub < QW / 16; ++sub) {
+          uint32_t raw[16], pk[8];
+          tmem_ld16(tS + 16 * sub, raw);
+          const float4 *l4 = lse4 + 4 * sub;
+          const int jc = c0 + 16 * sub;
+          switch (mode) {
+            case 0: bwd_p_chunk<16, 0, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+            case 1: bwd_p_chunk<16, 0, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+            case 2: bwd_p_chunk<16, 1, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+            case 3: bwd_p_chunk<16, 1, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+            case 4: bwd_p_chunk<16, 2, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+            default: bwd_p_chunk<16, 2, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
+          }
+          tmem_st8(tP + 8 * sub, pk);     // bf16 P^T: A operand of the dV product
+          tmem_st16(tS + 16 * sub, raw);  // fp32 P^T over S^T: read back by the dS pass
         }
-        tmem_st16(tP + 16 * c, pk);   // bf16 P^T: A operand of the dV product
-        tmem_st32(tS + 32 * c, raw);  // fp32 P^T over S^T: read back by the dS pass
       }
       tmem_st_wait();
       tc_fence_before();
@@ -455,27 +505,42 @@ __global__ void __launch_bounds__(512, 1)
       // ---- dS^T = P^T (dP^T - D), to shared memory (bf16, swizzled) for the dK / dQ MMAs.
       // P^T is read back in fp32 from where S^T was (the next S^T is issued only after this
       // pass). Table gradient: far tiles add into one register per side; near tiles sum each
-      // 32 x 32 block along its diagonals with warp shuffles (lane m collects deltas base + m
+      // 32-row block along its diagonals with warp shuffles (lane m collects deltas base + m
       // and base + m - 32) and add two values per lane into the per-delta array.
-      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd))) break;
-      if (it >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)))
-        break;
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
+           (it < 2 ||
+            __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
+      if (!ok) break;
       tc_fence_after();
-      uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
-      const bool near_db = do_dbias && side == 0;
+      {
+        uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
+        const bool near_db = do_dbias && side == 0;
+        float acc_a = 0.f, acc_b = 0.f, part = 0.f;
+        // 16 columns at a time (keeps the P and dP chunks in registers)
 #pragma unroll
-      for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t raw[32], pf[32];
-        tmem_ld32(tS + 32 * c, pf);
-        tmem_ld32(tDP + 32 * c, raw);
-        uint32_t pk[16];
-        float acc_a = 0.f, acc_b = 0.f;
-        const float part = near_db ? bwd_ds_chunk<true>(pf, raw, dvs4 + 8 * c, pk, lane, acc_a, acc_b)
-                                   : bwd_ds_chunk<false>(pf, raw, dvs4 + 8 * c, pk, lane, acc_a, acc_b);
+        for (int sub = 0; sub < QW / 16; ++sub) {
+          uint32_t pf[16], dp[16], pk[8];
+          tmem_ld16(tS + 16 * sub, pf);
+          tmem_ld16(tDP + 16 * sub, dp);
+          const float4 *d4 = dvs4 + 4 * sub;
+          if (sub == 0)
+            part += near_db ? bwd_ds_chunk<16, true, 0>(pf, dp, d4, pk, lane, acc_a, acc_b)
+                            : bwd_ds_chunk<16, false, 0>(pf, dp, d4, pk, lane, acc_a, acc_b);
+          else
+            part += near_db ? bwd_ds_chunk<16, true, 16>(pf, dp, d4, pk, lane, acc_a, acc_b)
+                            : bwd_ds_chunk<16, false, 16>(pf, dp, d4, pk, lane, acc_a, acc_b);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
+            const int j0 = c0 + 16 * sub + 8 * g;
+            const int chunk = (j0 & 63) >> 3;
+            uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4 *>(dst) =
+                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+          }
+        }
         if (near_db) {
           // delta of (row of lane m, column t) = base + m - t
-          const int base = d0 + 32 * (warp & 3) - (c0 + 32 * c) - p.bias.lut_lo;
+          const int base = d0 + 32 * (warp & 3) - c0 - p.bias.lut_lo;
           red_add_shared(diag + base + lane, acc_a);
           if (lane > 0) red_add_shared(diag + base + lane - 32, acc_b);
         } else if (side == 1) {
@@ -483,69 +548,28 @@ __global__ void __launch_bounds__(512, 1)
         } else if (side == 2) {
           acc_neg += part;
         }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {  // 4 groups of 8 queries = 16 bytes each
-          const int j0 = c0 + 32 * c + 8 * g;
-          const int chunk = (j0 & 63) >> 3;
-          uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4 *>(dst) =
-              make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-        }
       }
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
-    }
-  } else if (warp < 12) {
-    // ------------------------------------------------------------------ dQ drain, dK/dV out
-    const int dr = tid - 256;  // TMEM lane 0..127
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int it = 0; it < nq; ++it) {
-      const int qs = (i0 + it) * C::BQ;
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wd));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t va[32], vb[32];
-      tmem_ld32(tmem + lane_off + C::COL_DQ, va);
-      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, vb);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      if (D == 64) {  // lane = query row, columns = channels
-        const int q = qs + dr;
-        if (q < L) {
-          float *dst = p.dq_acc + ((size_t)(seq_start + q) * H + h) * D;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            red_add_v4(dst + 4 * c, __uint_as_float(va[4 * c]), __uint_as_float(va[4 * c + 1]),
-                       __uint_as_float(va[4 * c + 2]), __uint_as_float(va[4 * c + 3]));
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            red_add_v4(dst + 32 + 4 * c, __uint_as_float(vb[4 * c]),
-                       __uint_as_float(vb[4 * c + 1]), __uint_as_float(vb[4 * c + 2]),
-                       __uint_as_float(vb[4 * c + 3]));
-        }
-      } else {  // lane = channel, columns = query rows
-        float *dst = p.dq_acc + ((size_t)(seq_start + qs) * H + h) * D + dr;
-        const size_t step = (size_t)H * D;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (qs + j < L) red_add(dst + j * step, __uint_as_float(va[j]));
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (qs + 32 + j < L) red_add(dst + (32 + j) * step, __uint_as_float(vb[j]));
+      // ---- the previous tile's dQ (its product was issued after this tile's S^T and dP^T)
+      if (it >= 1 && !drain_dq(it - 1)) {
+        ok = false;
+        break;
       }
     }
+    if (ok && nq >= 1) ok = drain_dq(nq - 1);
+    // ---- dK, dV: this warpgroup's quarter of the channels
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
     if (ok) {
       tc_fence_after();
-      const int krow = ks + dr;
       const bool valid = krow < L;
-      __nv_bfloat16 *dkrow = p.dk + ((size_t)(seq_start + krow) * H + h) * D;
-      __nv_bfloat16 *dvrow = p.dv + ((size_t)(seq_start + krow) * H + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
+      const int cb = wg * (D / 4);
+      __nv_bfloat16 *dkrow = p.dk + ((size_t)(seq_start + krow) * H + h) * D + cb;
+      __nv_bfloat16 *dvrow = p.dv + ((size_t)(seq_start + krow) * H + h) * D + cb;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t a[16];
-        tmem_ld16(tmem + lane_off + C::COL_DK + 16 * c, a);
+        tmem_ld16(tmem + lane_off + C::COL_DK + cb + 16 * c, a);
         uint32_t pa[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -556,7 +580,7 @@ __global__ void __launch_bounds__(512, 1)
           dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
           dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
         }
-        tmem_ld16(tmem + lane_off + C::COL_DV + 16 * c, a);
+        tmem_ld16(tmem + lane_off + C::COL_DV + cb + 16 * c, a);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
@@ -571,7 +595,7 @@ __global__ void __launch_bounds__(512, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -582,7 +606,7 @@ __global__ void __launch_bounds__(512, 1)
       const float v = diag[i];
       if (v != 0.f) atomicAdd(bacc + t5_bucket_dev(p.bias.lut_lo + i, p.bias), v);
     }
-    if (warp < 8) {
+    if (warp < 16) {
       float a = acc_pos, b = acc_neg;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -615,7 +639,7 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   cudaError_t e;
   auto go = [&](auto kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) kernel<<<grid, 512, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (e == cudaSuccess) kernel<<<grid, BwdCfg<64, 2>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, p);
   };
   if (head_dim == 64) {
     if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
