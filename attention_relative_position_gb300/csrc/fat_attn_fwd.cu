@@ -7,10 +7,10 @@
 // GB300 design (one CTA = one document x head x 256 query rows = two 128-row Q tiles; three
 // warpgroups, so that every SM sub-partition holds one warp of each):
 //   warp 8      TMA producer: Q tiles once, K/V tiles through an NS-stage shared-memory ring.
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma,
-//               accumulators in tensor memory (TMEM); P_t is read from TMEM where the softmax
-//               warps wrote it over S_t.
-//   warps 10-11 idle (they complete the third warpgroup, which gives its registers to the
+//   warps 9-10  MMA issuers: S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma, accumulators
+//               in tensor memory (TMEM). d = 64: one issuing thread per Q tile, P_t in its own
+//               TMEM columns; d = 128: warp 9 issues for both tiles, P_t written over S_t.
+//   warp 11     idle (it completes the third warpgroup, which gives its registers to the
 //               softmax warpgroups: 216 + 216 + 72 per sub-partition fits its 512 x 32 registers).
 //   warps 0-7   two softmax warpgroups, one per Q tile; thread i owns row i of its tile (TMEM
 //               lane i), so row max/sum need no shuffles. Bias: closed form on tiles that lie
@@ -36,6 +36,13 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
   static constexpr int OFF_LUT = OFF_BAR + 256;
   static constexpr int NTHREADS = 384;
+  // TMEM columns: S_t at 128 t, O_t at 256 + O_STRIDE t. With d = 64 the O_t take 64 columns
+  // each and P_t (bf16 pairs) gets its own 64 columns at 384 + 64 t, so S_t of the next key tile
+  // can be computed while P_t is still being produced and consumed; with d = 128 P_t is written
+  // over S_t.
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr uint32_t COL_S0 = 0, COL_O0 = 256, O_STRIDE = SEP_P ? 64 : 128, COL_P0 = 384;
+  static_assert(!SEP_P || COL_O0 + 2 * O_STRIDE <= COL_P0, "TMEM column budget");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major), K (K-major)
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V (MN-major)
 };
@@ -115,8 +122,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t *s_full = v_empty + C::NS;
   uint64_t *p_ready = s_full + 2;
   uint64_t *o_ready = p_ready + 2;
-  uint64_t *mma_done = o_ready + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  uint64_t *s_free = o_ready + 2;  // S_t has been read into registers (separate-P layout)
+  uint64_t *mma_done = s_free + 2;  // [2], one per issuer
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
 
@@ -125,15 +133,17 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(v_full + s, 1);
-      mbar_init(k_empty + s, 1);
-      mbar_init(v_empty + s, 1);
+      mbar_init(k_empty + s, C::SEP_P ? ntile : 1);  // one release per MMA issuer
+      mbar_init(v_empty + s, C::SEP_P ? ntile : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
       mbar_init(p_ready + t, 128);
       mbar_init(o_ready + t, 1);
+      mbar_init(s_free + t, 128);
     }
     mbar_init(mma_done, 1);
+    mbar_init(mma_done + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -198,8 +208,9 @@ __global__ void __launch_bounds__(384, 1)
         if (last_v[s] >= 0) mbar_wait_teardown(v_full + s, last_v[s] & 1, kTeardownNs);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 && !C::SEP_P) {
+    // ------------------------------------------------------------------ MMA issuer (d = 128)
+    // One thread issues for both Q tiles (S_t is overwritten only after P_t V is issued).
     if (lane == 0) {
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
       auto issue_S = [&](int t, int s) {
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t b = sw128_desc(sVa + s * C::TILE + kk * 2048, C::BLK, 1024);
-          mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, b, C::IDESC_PV,
+          mma_bf16_ts(tmem + C::COL_O0 + C::O_STRIDE * t, tmem + 128 * t + kk * 8, b, C::IDESC_PV,
                       (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -266,6 +277,83 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(mma_done);
       mbar_wait_teardown(mma_done, 0, kTeardownNs);
     }
+  } else if (C::SEP_P && (warp == 9 || warp == 10)) {
+    // ------------------------------------------------------------------ MMA issuers (d = 64)
+    // One issuing thread per Q tile, so neither tile's hand-offs wait behind the other's.
+    // Each K/V stage is released once per active issuer (the barriers count ntile arrivals).
+    const int t = warp - 9;
+    if (lane == 0 && t < ntile) {
+      const int nk = t == 0 ? nkv0 : nkv1;
+      const uint32_t dS_t = tmem + C::COL_S0 + 128 * t;
+      const uint32_t dO_t = tmem + C::COL_O0 + C::O_STRIDE * t;
+      const uint32_t aP_t = C::SEP_P ? tmem + C::COL_P0 + 64 * t : dS_t;
+      // descriptors built once; moving the start address by b bytes adds b >> 4
+      const uint64_t dQd = sw128_desc(smem_u32(sQ) + t * C::TILE, 16, 1024);
+      const uint64_t dKd = sw128_desc(smem_u32(sK), 16, 1024);
+      const uint64_t dVd = sw128_desc(smem_u32(sV), C::BLK, 1024);
+      auto issue_S = [&](int st) {
+        const uint64_t kd = dKd + ((st * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::BLK + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(dS_t, dQd + off, kd + off, C::IDESC_S, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int st, bool acc) {
+        const uint64_t vd = dVd + ((st * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(dO_t, aP_t + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_PV,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, wd) && mbar_wait(k_full, 0, wd);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+        mma_commit(s_full + t);
+        mma_commit(k_empty);
+      }
+      for (int j = 0; ok && j < nk; ++j) {
+        const int s = j % C::NS, u = j / C::NS;
+        const int jn = j + 1, sn = jn % C::NS, un = jn / C::NS;
+        if (C::SEP_P) {  // next key tile's S_t as soon as the softmax has read S_t
+          if (!mbar_wait(s_free + t, j & 1, wd)) { ok = false; break; }
+          if (jn < nk) {
+            if (!mbar_wait(k_full + sn, un & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_S(sn);
+            mma_commit(s_full + t);
+            mma_commit(k_empty + sn);
+          }
+        }
+        if (!mbar_wait(v_full + s, u & 1, wd) || !mbar_wait(p_ready + t, j & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_PV(s, j > 0);
+        mma_commit(o_ready + t);
+        mma_commit(v_empty + s);
+        if (!C::SEP_P && jn < nk) {  // S_t is overwritten only after P_t V is issued
+          if (!mbar_wait(k_full + sn, un & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          issue_S(sn);
+          mma_commit(s_full + t);
+          mma_commit(k_empty + sn);
+        }
+      }
+      // key tiles this Q tile does not need (causal): release them once they have been loaded,
+      // in order, so each release lands in the phase of its stage
+      for (int j = nk; ok && j < nkv_max; ++j) {
+        const int s = j % C::NS, u = j / C::NS;
+        if (!mbar_wait(k_full + s, u & 1, wd)) { ok = false; break; }
+        mbar_arrive(k_empty + s);
+        if (!mbar_wait(v_full + s, u & 1, wd)) { ok = false; break; }
+        mbar_arrive(v_empty + s);
+      }
+      mma_commit(mma_done + t);
+      mbar_wait_teardown(mma_done + t, 0, kTeardownNs);
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
     regs_inc<216>();
@@ -274,8 +362,9 @@ __global__ void __launch_bounds__(384, 1)
       const int nk = t == 0 ? nkv0 : nkv1;
       const int r = tid & 127;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + lane_off + 128 * t;
-      const uint32_t tO = tmem + lane_off + 256 + 128 * t;
+      const uint32_t tS = tmem + lane_off + C::COL_S0 + 128 * t;
+      const uint32_t tO = tmem + lane_off + C::COL_O0 + C::O_STRIDE * t;
+      const uint32_t tP = C::SEP_P ? tmem + lane_off + C::COL_P0 + 64 * t : tS;
       const int qs = q0 + 128 * t;  // document-local first row of this tile
       const int qrow = qs + r;
       const FarBias fb = far_bias_dev(h, H, p.bias);
@@ -318,15 +407,26 @@ __global__ void __launch_bounds__(384, 1)
           mx = need_mask ? fwd_logits<2, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
                          : fwd_logits<2, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
 
+        if (C::SEP_P) {  // S_t is in registers: the next S_t may be computed
+          tc_fence_before();
+          mbar_arrive(s_free + t);
+        }
         if (j == 0) {
           m = mx;
         } else {
           const bool need = mx > m + 8.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            // O holds sum_{i<j} P_i V_i relative to the old max: rescale it once PV_{j-1} is done
+          if (C::SEP_P) {  // P_t and O_t are still read by PV_{j-1}
             ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (j - 1) & 1, wd));
             if (!ok) break;
             tc_fence_after();
+          }
+          if (__any_sync(0xffffffffu, need)) {
+            // O holds sum_{i<j} P_i V_i relative to the old max: rescale it once PV_{j-1} is done
+            if (!C::SEP_P) {
+              ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (j - 1) & 1, wd));
+              if (!ok) break;
+              tc_fence_after();
+            }
             const float f = need ? ex2(m - mx) : 1.0f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -354,7 +454,7 @@ __global__ void __launch_bounds__(384, 1)
             sum[i & 3] += a + b;
             pk[i] = pack_bf16x2(a, b);
           }
-          tmem_st16(tS + c * 16, pk);  // P (bf16 pairs) over the first 64 columns of S
+          tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
         }
         l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         tmem_st_wait();
