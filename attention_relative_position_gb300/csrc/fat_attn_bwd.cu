@@ -16,10 +16,11 @@
 //                partial sums; a quarter of each dQ tile drained from TMEM into the fp32 dQ
 //                accumulator with vector reductions; a quarter of dK, dV at the end.
 //   warp 16      TMA producer: K, V once; Q_i, dO_i (and lse_i, D_i) through a 2-3 stage ring.
-//   warp 17      MMA issuer: S^T = K Q_i^T, dP^T = V dO_i^T, dV += P^T dO_i (P^T from TMEM),
-//                dK += dS^T Q_i, and dQ_i = dS K (d = 64) or dQ_i^T = K^T dS^T (d = 128), all
-//                tcgen05 with fp32 accumulators in TMEM; dK and dV stay in TMEM for the walk.
-//   warps 18-19  idle (they complete the fifth warpgroup).
+//   warp 17      MMA issuer for S^T = K Q_i^T, dP^T = V dO_i^T and dV += P^T dO_i (P^T from
+//                TMEM), tcgen05 with fp32 accumulators in TMEM.
+//   warp 18      MMA issuer for dK += dS^T Q_i and dQ_i = dS K (d = 64) or dQ_i^T = K^T dS^T
+//                (d = 128); dK and dV stay in TMEM for the whole walk.
+//   warp 19      idle (it completes the fifth warpgroup).
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
 // the other tiles reduce each 32-row block along its diagonals with warp shuffles and add the
 // sums into a shared-memory array indexed by delta; at the end the CTA maps deltas to buckets
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *dq_full = ds_empty + 2;
   uint64_t *dq_empty = dq_full + 1;
   uint64_t *dkdv_done = dq_empty + 1;
-  uint64_t *mma_done = dkdv_done + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  uint64_t *mma_done = dkdv_done + 1;  // [2], one per issuer
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *bacc = reinterpret_cast<float *>(sm + C::OFF_BACC);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(qd_full + s, 32);
-      mbar_init(qd_empty + s, 1);
+      mbar_init(qd_empty + s, 2);  // both MMA issuers release a stage
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -232,8 +233,9 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(ds_empty + 1, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::NCOMP);
-    mbar_init(dkdv_done, 1);
+    mbar_init(dkdv_done, 2);
     mbar_init(mma_done, 1);
+    mbar_init(mma_done + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -315,91 +317,106 @@ __global__ void __launch_bounds__(640, 1)
       for (int x = 0; x < C::NS; ++x)
         if (last_q[x] >= 0) mbar_wait_teardown(qd_full + x, last_q[x] & 1, kTeardownNs);
     }
-  } else if (warp == 17) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 17 || warp == 18) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 17 issues the products that feed and consume P (S^T, dP^T, dV); warp 18 those that
+    // consume dS (dK, dQ). Two threads, so that neither chain of hand-offs waits behind the
+    // other; each Q/dO stage is released by both (the barrier counts two commits).
     if (lane == 0) {
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      const uint32_t aDS = smem_u32(sDS);
-      auto issue_qk = [&](uint32_t a_base, uint32_t b_base, uint32_t dcol) {
+      // descriptors built once; moving the start address by b bytes adds b >> 4
+      const uint64_t dKk = sw128_desc(smem_u32(sK), 16, 1024);         // K, K-major
+      const uint64_t dVk = sw128_desc(smem_u32(sV), 16, 1024);         // V, K-major
+      const uint64_t dQk = sw128_desc(smem_u32(sQ), 16, 1024);         // Q_i, K-major
+      const uint64_t dDOk = sw128_desc(smem_u32(sDO), 16, 1024);       // dO_i, K-major
+      const uint64_t dQm = sw128_desc(smem_u32(sQ), C::QBLK, 1024);    // Q_i, MN-major
+      const uint64_t dDOm = sw128_desc(smem_u32(sDO), C::QBLK, 1024);  // dO_i, MN-major
+      const uint64_t dDSk = sw128_desc(smem_u32(sDS), 16, 1024);       // dS^T, K-major
+      const uint64_t dDSm = sw128_desc(smem_u32(sDS), C::DSBLK, 1024); // dS^T, MN-major
+      const uint64_t dKm = sw128_desc(smem_u32(sK), C::KBLK, 1024);    // K, MN-major
+      auto issue_qk = [&](uint64_t a0, uint64_t b0, uint32_t dcol) {
         // D[key][q] = sum_c A[key][c] * B[q][c]; A, B K-major
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sw128_desc(a_base + (kk >> 2) * C::KBLK + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sw128_desc(b_base + (kk >> 2) * C::QBLK + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + dcol, a, b, C::IDESC_S, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + dcol, a0 + (((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4),
+                      b0 + (((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4), C::IDESC_S, kk > 0);
       };
-      auto issue_dv = [&](int st, bool acc) {
-        // dV[key][c] += sum_q P^T[key][q] dO[q][c]; A = P^T in TMEM, B = dO MN-major
+      bool ok = true;
+      if (warp == 17) {
+        auto issue_dv = [&](int st, bool acc) {
+          // dV[key][c] += sum_q P^T[key][q] dO[q][c]; A = P^T in TMEM, B = dO MN-major
+          const uint64_t b0 = dDOm + ((st * C::QTILE) >> 4);
 #pragma unroll
-        for (int k16 = 0; k16 < C::BQ / 16; ++k16) {
-          const uint64_t b = sw128_desc(aDO + st * C::QTILE + k16 * 2048, C::QBLK, 1024);
-          mma_bf16_ts(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b, C::IDESC_DKV,
-                      (acc || k16 > 0) ? 1u : 0u);
-        }
-      };
-      auto issue_dk = [&](int buf, int st, bool acc) {
-        // dK[key][c] += sum_q dS^T[key][q] Q[q][c]; A = dS^T K-major, B = Q MN-major
-#pragma unroll
-        for (int k16 = 0; k16 < C::BQ / 16; ++k16) {
-          const int q0 = 16 * k16;
-          const uint64_t a = sw128_desc(
-              aDS + buf * C::DSTILE + (q0 >> 6) * C::DSBLK + ((q0 & 63) >> 4) * 32, 16, 1024);
-          const uint64_t b = sw128_desc(aQ + st * C::QTILE + k16 * 2048, C::QBLK, 1024);
-          mma_bf16_ss(tmem + C::COL_DK, a, b, C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
-        }
-      };
-      auto issue_dq = [&](int buf) {
-#pragma unroll
-        for (int k16 = 0; k16 < 8; ++k16) {  // 128 keys
-          const uint64_t ds = sw128_desc(aDS + buf * C::DSTILE + k16 * 2048, C::DSBLK, 1024);
-          const uint64_t kk = sw128_desc(aK + k16 * 2048, C::KBLK, 1024);
-          if (D == 64)  // dQ[q][c] = sum_key dS[q][key] K[key][c]
-            mma_bf16_ss(tmem + C::COL_DQ, ds, kk, C::IDESC_DQ, k16 > 0);
-          else          // dQ^T[c][q] = sum_key K[key][c] dS^T[key][q]
-            mma_bf16_ss(tmem + C::COL_DQ, kk, ds, C::IDESC_DQ, k16 > 0);
-        }
-      };
-      bool ok = mbar_wait(kv_full, 0, wd) && mbar_wait(qd_full, 0, wd);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(aK, aQ, C::COL_S);
-        mma_commit(s_full);
-        issue_qk(aV, aDO, C::COL_DP);
-        mma_commit(dp_full);
-      }
-      // Per query tile: dV as soon as P^T is in TMEM; once dS^T is in shared memory (so S^T
-      // and dP^T have been consumed) the next tile's S^T and dP^T go first, then dK and dQ,
-      // so the P/dS warpgroups wait for one product only.
-      for (int it = 0; ok && it < nq; ++it) {
-        const int st = it % C::NS;
-        const int stn = (it + 1) % C::NS, un = (it + 1) / C::NS;
-        if (!mbar_wait(p_ready, it & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-        issue_dv(st, it > 0);
-        if (!mbar_wait(ds_ready, it & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-        if (it + 1 < nq) {
-          if (!mbar_wait(qd_full + stn, un & 1, wd)) { ok = false; break; }
+          for (int k16 = 0; k16 < C::BQ / 16; ++k16)
+            mma_bf16_ts(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b0 + ((k16 * 2048) >> 4),
+                        C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
+        };
+        ok = mbar_wait(kv_full, 0, wd) && mbar_wait(qd_full, 0, wd);
+        if (ok) {
           tc_fence_after();
-          issue_qk(aK, aQ + stn * C::QTILE, C::COL_S);
+          issue_qk(dKk, dQk, C::COL_S);
           mma_commit(s_full);
-          issue_qk(aV, aDO + stn * C::QTILE, C::COL_DP);
+          issue_qk(dVk, dDOk, C::COL_DP);
           mma_commit(dp_full);
         }
-        issue_dk(it & 1, st, it > 0);
-        if (it >= 1) {
-          if (!mbar_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
+        // dV as soon as P^T is in TMEM; the next tile's S^T and dP^T once dS^T is in shared
+        // memory (S^T and dP^T have then been consumed).
+        for (int it = 0; ok && it < nq; ++it) {
+          const int st = it % C::NS;
+          const int stn = (it + 1) % C::NS, un = (it + 1) / C::NS;
+          if (!mbar_wait(p_ready, it & 1, wd)) { ok = false; break; }
           tc_fence_after();
+          issue_dv(st, it > 0);
+          mma_commit(qd_empty + st);  // this issuer is done with Q_i / dO_i
+          if (it + 1 < nq) {
+            if (!mbar_wait(ds_ready, it & 1, wd) || !mbar_wait(qd_full + stn, un & 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(dKk, dQk + ((stn * C::QTILE) >> 4), C::COL_S);
+            mma_commit(s_full);
+            issue_qk(dVk, dDOk + ((stn * C::QTILE) >> 4), C::COL_DP);
+            mma_commit(dp_full);
+          }
         }
-        issue_dq(it & 1);
-        mma_commit(dq_full);
-        mma_commit(ds_empty + (it & 1));
-        mma_commit(qd_empty + st);
+      } else {
+        auto issue_dk = [&](int buf, int st, bool acc) {
+          // dK[key][c] += sum_q dS^T[key][q] Q[q][c]; A = dS^T K-major, B = Q MN-major
+          const uint64_t a0 = dDSk + ((buf * C::DSTILE) >> 4);
+          const uint64_t b0 = dQm + ((st * C::QTILE) >> 4);
+#pragma unroll
+          for (int k16 = 0; k16 < C::BQ / 16; ++k16)
+            mma_bf16_ss(tmem + C::COL_DK,
+                        a0 + ((((16 * k16) >> 6) * C::DSBLK + (((16 * k16) & 63) >> 4) * 32) >> 4),
+                        b0 + ((k16 * 2048) >> 4), C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
+        };
+        auto issue_dq = [&](int buf) {
+          const uint64_t ds0 = dDSm + ((buf * C::DSTILE) >> 4);
+#pragma unroll
+          for (int k16 = 0; k16 < 8; ++k16) {  // 128 keys
+            if (D == 64)  // dQ[q][c] = sum_key dS[q][key] K[key][c]
+              mma_bf16_ss(tmem + C::COL_DQ, ds0 + ((k16 * 2048) >> 4), dKm + ((k16 * 2048) >> 4),
+                          C::IDESC_DQ, k16 > 0);
+            else          // dQ^T[c][q] = sum_key K[key][c] dS^T[key][q]
+              mma_bf16_ss(tmem + C::COL_DQ, dKm + ((k16 * 2048) >> 4), ds0 + ((k16 * 2048) >> 4),
+                          C::IDESC_DQ, k16 > 0);
+          }
+        };
+        for (int it = 0; ok && it < nq; ++it) {
+          const int st = it % C::NS;
+          if (!mbar_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+          if (it >= 1 && !mbar_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          issue_dq(it & 1);
+          mma_commit(dq_full);
+          issue_dk(it & 1, st, it > 0);
+          mma_commit(ds_empty + (it & 1));
+          mma_commit(qd_empty + st);
+        }
       }
       if (ok) mma_commit(dkdv_done);
-      mma_commit(mma_done);
-      mbar_wait_teardown(mma_done, 0, kTeardownNs);
+      mma_commit(mma_done + (warp - 17));
+      mbar_wait_teardown(mma_done + (warp - 17), 0, kTeardownNs);
     }
   } else if (warp < 16) {
     // ------------------------------------------------------------------ P / dS warpgroups
