@@ -103,38 +103,46 @@ __device__ __forceinline__ void tmem_stw(uint32_t taddr, const uint32_t (&r)[W])
 }
 
 // P^T of one W-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
-// Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Bias forms are compile-time so
-// the unrolled element loop carries no branches: BIAS 0 = lookup table (lut_row[-j]),
-// 1 = constant rowc, 2 = rowc + kq * j.
+// Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Works on column pairs with
+// packed fp32x2 arithmetic. Bias forms are compile-time so the unrolled loop carries no
+// branches: BIAS 0 = lookup table (lut_row[-j]), 1 = constant rowc, 2 = rowc + kq * j.
 template <int W, int BIAS, bool MASK>
 __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W / 2],
                                             const float4 *lse4, const float *lut_row, int jc,
                                             float rowc, float kq, float scale_log2, int lo_j,
                                             int hi_j) {
+  const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t rc2 = f2_pack(rowc, rowc);
+  const uint64_t kq2 = f2_pack(kq, kq);
+  const float jcf = (float)jc;
 #pragma unroll
   for (int g = 0; g < W / 4; ++g) {
     const float4 l4 = lse4[g];
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-    float pr[4];
+    const uint64_t lv2[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * g + e;
+    for (int h = 0; h < 2; ++h) {
+      const int t = 4 * g + 2 * h;
       const int j = jc + t;
-      float b;
+      uint64_t b2;
       if (BIAS == 0)
-        b = lut_row[-j];
+        b2 = f2_pack(lut_row[-j], lut_row[-j - 1]);
       else if (BIAS == 1)
-        b = rowc;
+        b2 = rc2;
       else
-        b = fmaf(kq, (float)j, rowc);
-      float x = fmaf(__uint_as_float(raw[t]), scale_log2, b);
-      if (MASK) x = (j >= lo_j && j < hi_j) ? x : -INFINITY;
-      pr[e] = ex2(x - lv[e]);
+        b2 = f2_fma(kq2, f2_pack(jcf + (float)t, jcf + (float)(t + 1)), rc2);
+      const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(raw[t]), __uint_as_float(raw[t + 1])),
+                                 sl2, b2);
+      float x0, x1;
+      f2_unpack(f2_sub(x2, lv2[h]), x0, x1);
+      if (MASK) {
+        x0 = (j >= lo_j && j < hi_j) ? x0 : -INFINITY;
+        x1 = (j + 1 >= lo_j && j + 1 < hi_j) ? x1 : -INFINITY;
+      }
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      pk[t / 2] = pack_bf16x2(p0, p1);
+      raw[t] = __float_as_uint(p0);
+      raw[t + 1] = __float_as_uint(p1);
     }
-    pk[2 * g] = pack_bf16x2(pr[0], pr[1]);
-    pk[2 * g + 1] = pack_bf16x2(pr[2], pr[3]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) raw[4 * g + e] = __float_as_uint(pr[e]);
   }
 }
 
@@ -146,28 +154,35 @@ template <int W, bool NEAR, int T0>
 __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uint32_t (&dp)[W],
                                               const float4 *dvs4, uint32_t (&pk)[W / 2],
                                               int lane, float &acc_a, float &acc_b) {
-  float part = 0.f;
+  uint64_t part2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int g = 0; g < W / 4; ++g) {
     const float4 d4 = dvs4[g];
-    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-    float ds[4];
+    const uint64_t dv2[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * g + e;
-      ds[e] = __uint_as_float(pf[t]) * (__uint_as_float(dp[t]) - dv[e]);
+    for (int h = 0; h < 2; ++h) {
+      const int t = 4 * g + 2 * h;
+      const uint64_t p2 = f2_pack(__uint_as_float(pf[t]), __uint_as_float(pf[t + 1]));
+      const uint64_t dp2 = f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1]));
+      const uint64_t ds2 = f2_mul(p2, f2_sub(dp2, dv2[h]));
+      part2 = f2_add(part2, ds2);
+      float ds[2];
+      f2_unpack(ds2, ds[0], ds[1]);
+      pk[t / 2] = pack_bf16x2(ds[0], ds[1]);
       if (NEAR) {
-        const float y = __shfl_sync(0xffffffffu, ds[e], (lane + T0 + t) & 31);
-        const bool lo = lane + T0 + t < 32;
-        acc_a += lo ? y : 0.f;
-        acc_b += lo ? 0.f : y;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float y = __shfl_sync(0xffffffffu, ds[e], (lane + T0 + t + e) & 31);
+          const bool lo = lane + T0 + t + e < 32;
+          acc_a += lo ? y : 0.f;
+          acc_b += lo ? 0.f : y;
+        }
       }
     }
-    part += (ds[0] + ds[1]) + (ds[2] + ds[3]);
-    pk[2 * g] = pack_bf16x2(ds[0], ds[1]);
-    pk[2 * g + 1] = pack_bf16x2(ds[2], ds[3]);
   }
-  return part;
+  float p0, p1;
+  f2_unpack(part2, p0, p1);
+  return p0 + p1;
 }
 
 template <int D, int NSTAGES>
@@ -194,6 +209,13 @@ __global__ void __launch_bounds__(640, 1)
   if (ks >= L) return;
   const int i0 = p.causal ? ks / C::BQ : 0;
   const int nq = (L + C::BQ - 1) / C::BQ - i0;
+  // Query tiles are walked starting at a per-CTA offset, so the key-tile CTAs of one head do not
+  // all add into the same dQ rows at the same time (same-address reductions serialise in L2).
+  const int qrot = nq > 0 ? kb % nq : 0;
+  auto qtile_start = [&](int it) {
+    const int k = it + qrot;
+    return (i0 + (k >= nq ? k - nq : k)) * C::BQ;
+  };
   const bool do_dbias = p.dbias != nullptr && p.bias.table != nullptr;
 
   uint8_t *sK = sm + C::OFF_K, *sV = sm + C::OFF_V, *sQ = sm + C::OFF_Q, *sDO = sm + C::OFF_DO;
@@ -279,7 +301,7 @@ __global__ void __launch_bounds__(640, 1)
       }
       for (int it = 0; it < nq; ++it) {
         const int st = it % C::NS, u = it / C::NS;
-        const int qs = (i0 + it) * C::BQ;
+        const int qs = qtile_start(it);
         // fetch this tile's row statistics before waiting for the stage to be free
         float lv[C::BQ / 32], dv[C::BQ / 32];
 #pragma unroll
@@ -441,7 +463,7 @@ __global__ void __launch_bounds__(640, 1)
       tmem_ld16(tDQ, v);
       tc_fence_before();
       mbar_arrive(dq_empty);
-      const int qs = (i0 + it) * C::BQ;
+      const int qs = qtile_start(it);
       if (D == 64) {  // lane = query row, columns = channels 16*wg ..
         const int q = qs + r;
         if (q < L) {
@@ -464,7 +486,7 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int st = it % C::NS;
-      const int qs = (i0 + it) * C::BQ;
+      const int qs = qtile_start(it);
       ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
            __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd));
       if (!ok) break;
