@@ -152,22 +152,28 @@ void set_last_error(const char *what, int code, const char *text) {
   snprintf(g_last_error, sizeof g_last_error, "%s: error %d (%s)", what, code, text ? text : "");
 }
 
-int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_encode) {
-      void *fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                       cudaEnableDefault, &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
-        set_last_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
-                       e != cudaSuccess ? (int)e : (int)q, cudaGetErrorString(e));
-        return -1;
-      }
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+namespace {
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
+bool resolve_encode() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+      set_last_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
+                     e != cudaSuccess ? (int)e : (int)q, cudaGetErrorString(e));
+      return false;
     }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return true;
+}
+}  // namespace
+
+int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows) {
+  if (!resolve_encode()) return -1;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
@@ -178,6 +184,24 @@ int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int bo
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_last_error("cuTensorMapEncodeTiled", (int)r, "");
+    return -1;
+  }
+  return 0;
+}
+
+int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_c,
+                      int box_rows) {
+  if (!resolve_encode()) return -1;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled(fp32)", (int)r, "");
     return -1;
   }
   return 0;

@@ -50,7 +50,12 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + KTILE;
   static constexpr int OFF_DO = OFF_Q + NS * QTILE;
   static constexpr int OFF_DS = OFF_DO + NS * QTILE;
-  static constexpr int OFF_STAT = OFF_DS + 2 * DSTILE;  // lse2[NS][BQ] then dvec[NS][BQ]
+  // d = 64: each warpgroup stages its 16-channel slice of a dQ tile (128 rows x 64 bytes) here
+  // and hands it to the TMA engine as one bulk reduction.
+  static constexpr bool DQ_TMA = (D == 64);
+  static constexpr int DQS_SLICE = 128 * 16 * 4;
+  static constexpr int OFF_DQS = OFF_DS + 2 * DSTILE;
+  static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 4 * DQS_SLICE : 0);  // lse2, dvec
   static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
   static constexpr int OFF_BACC = OFF_BAR + 256;        // per-bucket sums, 256 floats
   static constexpr int OFF_LUT = OFF_BACC + 256 * 4;    // lut[lut_len], then diag[lut_len]
@@ -189,7 +194,7 @@ template <int D, int NSTAGES>
 __global__ void __launch_bounds__(640, 1)
     fat_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D, NSTAGES>;
   constexpr int QW = C::QW;
   extern __shared__ uint8_t smem_raw[];
@@ -220,6 +225,7 @@ __global__ void __launch_bounds__(640, 1)
 
   uint8_t *sK = sm + C::OFF_K, *sV = sm + C::OFF_V, *sQ = sm + C::OFF_Q, *sDO = sm + C::OFF_DO;
   uint8_t *sDS = sm + C::OFF_DS;
+  uint8_t *sDQS = sm + C::OFF_DQS;
   float *s_lse2 = reinterpret_cast<float *>(sm + C::OFF_STAT);
   float *s_dvec = s_lse2 + C::NS * C::BQ;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
@@ -235,7 +241,8 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *dq_empty = dq_full + 1;
   uint64_t *dkdv_done = dq_empty + 1;
   uint64_t *mma_done = dkdv_done + 1;  // [2], one per issuer
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
+  uint64_t *dqs_bar = mma_done + 2;    // [4][2]: dQ staging slice free / written, per warpgroup
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dqs_bar + 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *bacc = reinterpret_cast<float *>(sm + C::OFF_BACC);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(dkdv_done, 2);
     mbar_init(mma_done, 1);
     mbar_init(mma_done + 1, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(dqs_bar + i, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -464,15 +472,30 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_before();
       mbar_arrive(dq_empty);
       const int qs = qtile_start(it);
-      if (D == 64) {  // lane = query row, columns = channels 16*wg ..
-        const int q = qs + r;
-        if (q < L) {
-          float *dst = p.dq_acc + ((size_t)(seq_start + q) * H + h) * D + 16 * wg;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            red_add_v4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                       __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+      if (C::DQ_TMA) {  // lane = query row, columns = channels 16*wg ..: stage, bulk-reduce
+        uint8_t *slice = sDQS + wg * C::DQS_SLICE;
+        uint64_t *bar_free = dqs_bar + 2 * wg, *bar_written = bar_free + 1;
+        if (it >= 1) {  // the previous bulk reduction of this slice has finished reading
+          if (r == 0) bulk_wait_read_all();
+          mbar_arrive(bar_free);
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_free, (it - 1) & 1, wd))) return false;
         }
+        uint4 *dst = reinterpret_cast<uint4 *>(slice + r * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dst[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar_written);
+        // rows past the document end carry zeros (their dS is masked), rows past T are clipped
+        bool issued = true;
+        if (r == 0) {
+          issued = mbar_wait(bar_written, it & 1, wd);
+          if (issued) {
+            tma_reduce_add_3d(&tm_dq, slice, 16 * wg, h, seq_start + qs);
+            bulk_commit_group();
+          }
+        }
+        return __all_sync(0xffffffffu, issued);  // same answer for the whole warp
       } else {  // lane = channel, columns = query rows 16*wg ..
         float *dst = p.dq_acc + ((size_t)(seq_start + qs + 16 * wg) * H + h) * D + r;
         const size_t step = (size_t)H * D;
@@ -597,6 +620,7 @@ __global__ void __launch_bounds__(640, 1)
       }
     }
     if (ok && nq >= 1) ok = drain_dq(nq - 1);
+    if (C::DQ_TMA && r == 0) bulk_wait_all();  // reductions complete before shared memory is released
     // ---- dK, dV: this warpgroup's quarter of the channels
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
     if (ok) {
@@ -666,11 +690,12 @@ __global__ void __launch_bounds__(640, 1)
 int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
                const void *v, const void *out, const void *dout, cudaStream_t stream) {
   (void)out;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
   const int bq = head_dim == 64 ? BwdCfg<64, 2>::BQ : BwdCfg<128, 2>::BQ;
   if (make_tmap_thd(&mq, q, T, H, head_dim, bq) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
-      make_tmap_thd(&mv, v, T, H, head_dim, 128) || make_tmap_thd(&mdo, dout, T, H, head_dim, bq))
+      make_tmap_thd(&mv, v, T, H, head_dim, 128) || make_tmap_thd(&mdo, dout, T, H, head_dim, bq) ||
+      make_tmap_thd_f32(&mdq, p.dq_acc, T, H, head_dim, 16, 128))
     return (int)cudaErrorInvalidValue;
   const size_t smem = bwd_smem_bytes(head_dim, p.bias.lut_len);
   const int ns = bwd_stages(head_dim, p.bias.lut_len);
@@ -678,7 +703,8 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   cudaError_t e;
   auto go = [&](auto kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) kernel<<<grid, BwdCfg<64, 2>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (e == cudaSuccess)
+      kernel<<<grid, BwdCfg<64, 2>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
   };
   if (head_dim == 64) {
     if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);

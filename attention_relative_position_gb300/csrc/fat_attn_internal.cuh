@@ -130,5 +130,9 @@ void set_last_error(const char *what, int code, const char *text);
 // Tensor map over a [T, H, d] bf16 tensor, box = 64 channels x 1 head x box_rows tokens,
 // 128-byte swizzle (the shared-memory layout the tcgen05 descriptors expect).
 int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows);
+// Tensor map over a [T, H, d] fp32 tensor, box = box_c channels x 1 head x box_rows tokens, no
+// swizzle (for bulk reductions from a row-major shared-memory tile).
+int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_c,
+                      int box_rows);
 
 }  // namespace fat
