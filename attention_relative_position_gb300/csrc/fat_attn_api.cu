@@ -213,63 +213,92 @@ using namespace fat;
 
 // ---- preprocessing and finishing kernels of the backward -----------------------------------
 // D[h, t] = sum_c dout[t, h, c] * out[t, h, c] (fp32), the dQ accumulator zeroed, and the
-// table gradient zeroed. One warp per (token, head) row; memory bound.
+// table gradient zeroed. Memory bound: each lane loads 16 bytes of out and of dout (D/8 lanes per
+// (token, head) row, two row groups in flight per thread), and the zeroing is a separate flat
+// sweep of 16-byte stores over the accumulator.
 template <int D>
-__global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ out,
-                                                           const __nv_bfloat16 *__restrict__ dout,
+__global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restrict__ out,
+                                                           const uint4 *__restrict__ dout,
                                                            float *__restrict__ dvec,
-                                                           float *__restrict__ dq_acc,
+                                                           float4 *__restrict__ dq_acc,
                                                            float *__restrict__ dbias, int nbias,
                                                            int T, int H) {
-  constexpr int PER = D / 32;  // bf16 per lane
+  constexpr int LPR = D / 8;         // lanes per row, 8 bf16 each
+  constexpr int RPW = 32 / LPR;      // rows per warp step
   const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, part = lane % LPR;
   const long long nrows = (long long)T * H;
-  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long gtid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long warp0 = gtid >> 5, nwarps = nthreads >> 5;
   if (dbias && warp0 == 0)
     for (int i = lane; i < nbias; i += 32) dbias[i] = 0.f;
-  for (long long row = warp0; row < nrows; row += nwarps) {
-    const long long t = row / H, h = row % H;
-    const __nv_bfloat16 *o = out + row * D + lane * PER;
-    const __nv_bfloat16 *g = dout + row * D + lane * PER;
+  auto dot8 = [](uint4 a, uint4 b) {
+    const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
     float acc = 0.f;
-    if (PER == 2) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o);
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(g);
-      acc = __bfloat162float(a.x) * __bfloat162float(b.x) + __bfloat162float(a.y) * __bfloat162float(b.y);
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2 *>(o);
-      const uint2 b = *reinterpret_cast<const uint2 *>(g);
-      const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
-      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        acc += __bfloat162float(a2[i].x) * __bfloat162float(b2[i].x) +
-               __bfloat162float(a2[i].y) * __bfloat162float(b2[i].y);
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(b2[i]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
     }
+    return acc;
+  };
+  // Row groups of RPW rows; each warp takes two groups per step so that four 16-byte loads per
+  // lane are in flight.
+  const long long ngroups = (nrows + RPW - 1) / RPW;
+  for (long long g = warp0 * 2; g < ngroups; g += nwarps * 2) {
+    const long long r0 = g * RPW + sub, r1 = (g + 1) * RPW + sub;
+    const bool v0 = r0 < nrows, v1 = r1 < nrows;
+    uint4 a0 = make_uint4(0, 0, 0, 0), b0 = a0, a1 = a0, b1 = a0;
+    if (v0) { a0 = out[r0 * LPR + part]; b0 = dout[r0 * LPR + part]; }
+    if (v1) { a1 = out[r1 * LPR + part]; b1 = dout[r1 * LPR + part]; }
+    float s0 = dot8(a0, b0), s1 = dot8(a1, b1);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) dvec[h * T + t] = acc;
-    float *z = dq_acc + row * D + lane * PER;
-    if (PER == 2)
-      *reinterpret_cast<float2 *>(z) = make_float2(0.f, 0.f);
-    else
-      *reinterpret_cast<float4 *>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int off = LPR / 2; off > 0; off >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    if (part == 0) {
+      if (v0) dvec[(r0 % H) * (long long)T + r0 / H] = s0;
+      if (v1) dvec[(r1 % H) * (long long)T + r1 / H] = s1;
+    }
   }
+  const long long n4 = nrows * (D / 4);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  long long i = gtid;
+  for (; i + 3 * nthreads < n4; i += 4 * nthreads) {
+    dq_acc[i] = z;
+    dq_acc[i + nthreads] = z;
+    dq_acc[i + 2 * nthreads] = z;
+    dq_acc[i + 3 * nthreads] = z;
+  }
+  for (; i < n4; i += nthreads) dq_acc[i] = z;
 }
 
-// dq = bf16(dq_acc * softmax_scale), 4 elements per thread step.
+// dq = bf16(dq_acc * softmax_scale): eight accumulator values in, one 16-byte store out per
+// thread step; n8 = element count / 8 (the element count is a multiple of 64).
 __global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const float4 *__restrict__ acc,
-                                                             uint2 *__restrict__ dq, float scale,
-                                                             long long n4) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float4 a = acc[i];
-    uint2 o;
+                                                             uint4 *__restrict__ dq, float scale,
+                                                             long long n8) {
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  auto cvt = [scale](float4 a, float4 b) {
+    uint4 o;
     o.x = pack_bf16x2(a.x * scale, a.y * scale);
     o.y = pack_bf16x2(a.z * scale, a.w * scale);
-    dq[i] = o;
+    o.z = pack_bf16x2(b.x * scale, b.y * scale);
+    o.w = pack_bf16x2(b.z * scale, b.w * scale);
+    return o;
+  };
+  for (; i + nthreads < n8; i += 2 * nthreads) {
+    const float4 a0 = acc[2 * i], b0 = acc[2 * i + 1];
+    const float4 a1 = acc[2 * (i + nthreads)], b1 = acc[2 * (i + nthreads) + 1];
+    dq[i] = cvt(a0, b0);
+    dq[i + nthreads] = cvt(a1, b1);
   }
+  if (i < n8) dq[i] = cvt(acc[2 * i], acc[2 * i + 1]);
 }
 
 // ---- C ABI -------------------------------------------------------------------------------------
@@ -408,15 +437,17 @@ int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *
     return cuda_rc((int)e);
   }
   const long long rows = (long long)T * H;
-  const int blocks = (int)std::min<long long>((rows + 7) / 8, 152LL * 16);
-  const auto *o = static_cast<const __nv_bfloat16 *>(out);
-  const auto *g = static_cast<const __nv_bfloat16 *>(dout);
+  // Enough warps for every (token, head) row group, at most eight 256-thread blocks per SM.
+  const int blocks = (int)std::min<long long>((rows + 63) / 64, 152LL * 8);
+  const auto *o = static_cast<const uint4 *>(out);
+  const auto *g = static_cast<const uint4 *>(dout);
+  float4 *acc4 = reinterpret_cast<float4 *>(ws.dq_acc);
   if (d == 64)
-    fat_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, ws.dq_acc, dbias_table,
-                                                         nbias, T, H);
+    fat_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, acc4, dbias_table, nbias,
+                                                         T, H);
   else
-    fat_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, ws.dq_acc, dbias_table,
-                                                          nbias, T, H);
+    fat_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, acc4, dbias_table, nbias,
+                                                          T, H);
   return launch_rc("backward preprocess launch");
 }
 
@@ -472,11 +503,11 @@ int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t w
   WorkspaceView ws{};
   rc = check_workspace(sh, workspace, workspace_bytes, &ws);
   if (rc) return rc;
-  const long long n4 = (long long)sh->total_tokens * sh->num_heads * sh->head_dim / 4;
-  if (n4 == 0) return FAT_OK;
-  const int blocks = (int)std::min<long long>((n4 + 255) / 256, 152LL * 16);
+  const long long n8 = (long long)sh->total_tokens * sh->num_heads * sh->head_dim / 8;
+  if (n8 == 0) return FAT_OK;
+  const int blocks = (int)std::min<long long>((n8 + 255) / 256, 152LL * 8);
   fat_bwd_finish_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(sh->stream)>>>(
-      reinterpret_cast<const float4 *>(ws.dq_acc), static_cast<uint2 *>(dq), softmax_scale, n4);
+      reinterpret_cast<const float4 *>(ws.dq_acc), static_cast<uint4 *>(dq), softmax_scale, n8);
   return launch_rc("backward finalize launch");
 }
 

@@ -52,36 +52,47 @@ size_t fwd_smem_bytes(int head_dim, int lut_len) {
   return 1024 + base + (size_t)lut_len * 4;
 }
 
-// Load S row chunk by chunk from TMEM, form x = S * scale_log2 + bias (log2 units), apply the
+// Load the S row from TMEM (all four 32-column loads in flight), form
+// x = S * scale_log2 + bias (log2 units) two columns per packed fp32x2 instruction, apply the
 // mask, and return the row maximum.
 //   MODE 0: bias = rowc (constant over the tile)
 //   MODE 1: bias = rowc + kk * j (linear in the key index)
 //   MODE 2: bias = lut_row[j]
 template <int MODE, bool MASK>
-__device__ __forceinline__ float fwd_logits(uint32_t tS, float (&x)[128], float scale_log2,
+__device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], float scale_log2,
                                             float rowc, float kk, const float *lut_row, int lim) {
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32_issue(tS + c * 32, x[c]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32_fence(x[c]);
+  const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t rc2 = f2_pack(rowc, rowc);
+  float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t raw[32];
-    tmem_ld32(tS + c * 32, raw);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 32; i += 2) {
       const int j = c * 32 + i;
-      float b;
+      uint64_t b2;
       if (MODE == 0)
-        b = rowc;
+        b2 = rc2;
       else if (MODE == 1)
-        b = fmaf(kk, (float)j, rowc);
+        b2 = f2_pack(fmaf(kk, (float)j, rowc), fmaf(kk, (float)(j + 1), rowc));
       else
-        b = lut_row[j];
-      float v = fmaf(__uint_as_float(raw[i]), scale_log2, b);
-      if (MASK) v = (j < lim) ? v : -INFINITY;
-      x[j] = v;
-      mx[i & 3] = fmaxf(mx[i & 3], v);
+        b2 = f2_pack(lut_row[j], lut_row[j + 1]);
+      float v0, v1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c][i]), __uint_as_float(x[c][i + 1])), sl2, b2),
+                v0, v1);
+      if (MASK) {
+        v0 = (j < lim) ? v0 : -INFINITY;
+        v1 = (j + 1 < lim) ? v1 : -INFINITY;
+      }
+      x[c][i] = __float_as_uint(v0);
+      x[c][i + 1] = __float_as_uint(v1);
+      mx[(i >> 1) & 1] = fmax3(mx[(i >> 1) & 1], v0, v1);
     }
   }
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  return fmaxf(mx[0], mx[1]);
 }
 
 template <int D>
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(384, 1)
           mode = 2;
         }
         const float *lut_row = lut + (d0 - r - p.bias.lut_lo);
-        float x[128];
+        uint32_t x[4][32];
         float mx;
         if (mode == 0)
           mx = need_mask ? fwd_logits<0, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
@@ -443,20 +454,30 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t m2 = f2_pack(m_use, m_use);
+        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = ex2(x[c * 32 + 2 * i] - m_use);
-            const float b = ex2(x[c * 32 + 2 * i + 1] - m_use);
-            sum[i & 3] += a + b;
+            float a, b;
+            f2_unpack(f2_sub(f2_pack(__uint_as_float(x[c][2 * i]), __uint_as_float(x[c][2 * i + 1])),
+                             m2),
+                      a, b);
+            a = ex2(a);
+            b = ex2(b);
             pk[i] = pack_bf16x2(a, b);
+            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a, b));
           }
           tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
         }
-        l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(sum2[0], s0, s1);
+          f2_unpack(sum2[1], s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_ready + t);
