@@ -57,8 +57,9 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + 2 * DSTILE;
   static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 4 * DQS_SLICE : 0);  // lse2, dvec
   static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
-  static constexpr int OFF_BACC = OFF_BAR + 256;        // per-bucket sums, 256 floats
-  static constexpr int OFF_LUT = OFF_BACC + 256 * 4;    // lut[lut_len], then diag[lut_len]
+  // lut[lut_len] (bias, log2 units), diag[lut_len] (bias-gradient sums per delta), then the
+  // bucket of each delta as bytes
+  static constexpr int OFF_LUT = OFF_BAR + 256;
   static constexpr int NTHREADS = 640;
   static constexpr int NCOMP = 512;                     // threads of the P/dS warpgroups
   // TMEM columns: S^T and dP^T (BQ each), dQ (64), P^T as packed bf16 pairs (BQ/2), dK, dV.
@@ -74,7 +75,7 @@ struct BwdCfg {
 
 template <int D, int NS>
 size_t bwd_smem_bytes_t(int lut_len) {
-  return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 8;
+  return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 9 + 16;
 }
 // Three Q/dO stages when they fit next to the bias table, else two.
 int bwd_stages(int head_dim, int lut_len) {
@@ -244,47 +245,79 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *dqs_bar = mma_done + 2;    // [4][2]: dQ staging slice free / written, per warpgroup
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dqs_bar + 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  float *bacc = reinterpret_cast<float *>(sm + C::OFF_BACC);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
   float *diag = lut + p.bias.lut_len;
+  uint8_t *lbk = reinterpret_cast<uint8_t *>(diag + p.bias.lut_len);
 
-  if (tid == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(qd_full + s, 32);
-      mbar_init(qd_empty + s, 2);  // both MMA issuers release a stage
+  // The producer warp sets up the barriers and completes its first step (K, V, the first Q/dO
+  // tile and its row statistics) before the rest of the block builds its tables, so the load
+  // latency overlaps them.
+  const bool early_q = !(p.debug_flags & 2);
+  if (warp == 16) {
+    if (lane == 0) {
+      mbar_init(kv_full, 1);
+      for (int s = 0; s < C::NS; ++s) {
+        mbar_init(qd_full + s, 32);
+        mbar_init(qd_empty + s, 2);  // both MMA issuers release a stage
+      }
+      mbar_init(s_full, 1);
+      mbar_init(dp_full, 1);
+      mbar_init(p_ready, C::NCOMP);
+      mbar_init(ds_ready, C::NCOMP);
+      mbar_init(ds_empty, 1);
+      mbar_init(ds_empty + 1, 1);
+      mbar_init(dq_full, 1);
+      mbar_init(dq_empty, C::NCOMP);
+      mbar_init(dkdv_done, 2);
+      mbar_init(mma_done, 1);
+      mbar_init(mma_done + 1, 1);
+      for (int i = 0; i < 8; ++i) mbar_init(dqs_bar + i, 128);
+      *abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
     }
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_ready, C::NCOMP);
-    mbar_init(ds_ready, C::NCOMP);
-    mbar_init(ds_empty, 1);
-    mbar_init(ds_empty + 1, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, C::NCOMP);
-    mbar_init(dkdv_done, 2);
-    mbar_init(mma_done, 1);
-    mbar_init(mma_done + 1, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(dqs_bar + i, 128);
-    *abort_flag = 0;
-    fence_mbar_init();
+    __syncwarp();
+    if (early_q) {
+      const int qs0 = qtile_start(0);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
+        for (int b = 0; b < C::DB; ++b) {
+          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, h, seq_start + ks);
+          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, h, seq_start + ks);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < C::BQ / 32; ++k) {
+        const int q = qs0 + lane + 32 * k;
+        const size_t idx = (size_t)h * T + seq_start + q;
+        s_lse2[lane + 32 * k] = q < L ? __ldg(p.lse + idx) * kLog2e : 0.f;
+        s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + idx) : 0.f;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qd_full, 2 * C::QTILE);
+        for (int b = 0; b < C::DB; ++b) {
+          tma_load_3d(&tm_q, qd_full, sQ + b * C::QBLK, 64 * b, h, seq_start + qs0);
+          tma_load_3d(&tm_do, qd_full, sDO + b * C::QBLK, 64 * b, h, seq_start + qs0);
+        }
+      } else {
+        mbar_arrive(qd_full);
+      }
+    }
   }
   if (warp == 17) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 16 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
-  }
   for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
     lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
-    if (do_dbias) diag[i] = 0.f;
+    if (do_dbias) {
+      diag[i] = 0.f;
+      lbk[i] = static_cast<uint8_t>(t5_bucket_dev(p.bias.lut_lo + i, p.bias));
+    }
   }
-  if (do_dbias)
-    for (int i = tid; i < 256; i += C::NTHREADS) bacc[i] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,17 +330,10 @@ __global__ void __launch_bounds__(640, 1)
     int last_q[C::NS];
 #pragma unroll
     for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
-    bool kv_issued = false;
-    if (!(p.debug_flags & 2)) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
-        for (int b = 0; b < C::DB; ++b) {
-          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, h, seq_start + ks);
-          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, h, seq_start + ks);
-        }
-        kv_issued = true;
-      }
-      for (int it = 0; it < nq; ++it) {
+    const bool kv_issued = early_q && lane == 0;
+    if (early_q) {
+      if (lane == 0) last_q[0] = 0;  // step 0 was done with the block set-up
+      for (int it = 1; it < nq; ++it) {
         const int st = it % C::NS, u = it / C::NS;
         const int qs = qtile_start(it);
         // fetch this tile's row statistics before waiting for the stage to be free
@@ -663,13 +689,27 @@ __global__ void __launch_bounds__(640, 1)
     tmem_dealloc(tmem, 512);
   }
   if (do_dbias && !*abort_flag) {
-    // fold the per-delta and per-side partial sums into per-bucket sums, then one global
-    // atomic per (bucket, head)
-    for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
-      const float v = diag[i];
-      if (v != 0.f) atomicAdd(bacc + t5_bucket_dev(p.bias.lut_lo + i, p.bias), v);
+    // Per-delta sums to per-bucket sums: each warp takes 32 consecutive deltas, runs of equal
+    // buckets are summed with a segmented scan, and each run adds once to the global gradient.
+    for (int base = warp * 32; base < p.bias.lut_len; base += C::NTHREADS) {
+      const int i = base + lane;
+      const bool in = i < p.bias.lut_len;
+      float v = in ? diag[i] : 0.f;
+      const int b = in ? static_cast<int>(lbk[i]) : -1;
+      const int b_prev = __shfl_up_sync(0xffffffffu, b, 1);
+      const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || b_prev != b);
+      const int seg = __popc(heads & (0xffffffffu >> (31 - lane)));  // run index of this lane
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float vo = __shfl_up_sync(0xffffffffu, v, off);
+        const int so = __shfl_up_sync(0xffffffffu, seg, off);
+        if (lane >= off && so == seg) v += vo;
+      }
+      const int seg_next = __shfl_down_sync(0xffffffffu, seg, 1);
+      if (in && (lane == 31 || seg_next != seg) && v != 0.f)
+        red_add(p.dbias + (size_t)b * H + h, v);
     }
-    if (warp < 16) {
+    if (warp < 16) {  // far tiles: one bucket per side
       float a = acc_pos, b = acc_neg;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -677,13 +717,10 @@ __global__ void __launch_bounds__(640, 1)
         b += __shfl_xor_sync(0xffffffffu, b, off);
       }
       if (lane == 0) {
-        if (a != 0.f) atomicAdd(bacc + t5_bucket_dev(p.bias.sat_pos, p.bias), a);
-        if (b != 0.f) atomicAdd(bacc + t5_bucket_dev(-p.bias.sat_neg, p.bias), b);
+        if (a != 0.f) red_add(p.dbias + (size_t)t5_bucket_dev(p.bias.sat_pos, p.bias) * H + h, a);
+        if (b != 0.f) red_add(p.dbias + (size_t)t5_bucket_dev(-p.bias.sat_neg, p.bias) * H + h, b);
       }
     }
-    __syncthreads();
-    for (int b = tid; b < p.bias.nb; b += C::NTHREADS)
-      if (bacc[b] != 0.f) atomicAdd(p.dbias + (size_t)b * H + h, bacc[b]);
   }
 }
 

@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(384, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
 
-  if (tid == 0) {
+  // The producer thread sets up the barriers and starts the first copies (Q, K_0, V_0) before
+  // the block builds its bias table, so the load latency overlaps it.
+  const bool early = !(p.debug_flags & 1);
+  if (warp == 8 && lane == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(k_full + s, 1);
@@ -157,15 +160,26 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(mma_done + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if (early) {
+      mbar_arrive_expect_tx(q_full, ntile * C::TILE);
+      for (int t = 0; t < ntile; ++t)
+        for (int b = 0; b < C::DB; ++b)
+          tma_load_3d(&tm_q, q_full, sQ + t * C::TILE + b * C::BLK, 64 * b, h,
+                      seq_start + q0 + 128 * t);
+      mbar_arrive_expect_tx(k_full, C::TILE);
+      for (int b = 0; b < C::DB; ++b)
+        tma_load_3d(&tm_k, k_full, sK + b * C::BLK, 64 * b, h, seq_start);
+      mbar_arrive_expect_tx(v_full, C::TILE);
+      for (int b = 0; b < C::DB; ++b)
+        tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, h, seq_start);
+    }
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
-  }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
   }
   for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS)
     lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
@@ -183,15 +197,10 @@ __global__ void __launch_bounds__(384, 1)
       int last_k[C::NS], last_v[C::NS];
 #pragma unroll
       for (int s = 0; s < C::NS; ++s) last_k[s] = last_v[s] = -1;
-      bool q_issued = false;
-      if (!(p.debug_flags & 1)) {
-        mbar_arrive_expect_tx(q_full, ntile * C::TILE);
-        for (int t = 0; t < ntile; ++t)
-          for (int b = 0; b < C::DB; ++b)
-            tma_load_3d(&tm_q, q_full, sQ + t * C::TILE + b * C::BLK, 64 * b, h,
-                        seq_start + q0 + 128 * t);
-        q_issued = true;
-        for (int j = 0; j < nkv_max; ++j) {
+      const bool q_issued = early;
+      if (early) {
+        last_k[0] = last_v[0] = 0;  // Q, K_0 and V_0 were started with the block set-up
+        for (int j = 1; j < nkv_max; ++j) {
           const int s = j % C::NS, u = j / C::NS;
           if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, wd)) break;
           mbar_arrive_expect_tx(k_full + s, C::TILE);
