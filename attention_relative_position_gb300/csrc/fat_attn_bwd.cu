@@ -53,15 +53,17 @@ struct BwdCfg {
   // d = 64: each warpgroup stages its 16-channel slice of a dQ tile (128 rows x 64 bytes) here
   // and hands it to the TMA engine as one bulk reduction.
   static constexpr bool DQ_TMA = (D == 64);
-  static constexpr int DQS_SLICE = 128 * 16 * 4;
+  static constexpr int DQS_SLICE = 32 * 16 * 4;  // one warp: 32 rows x 16 channels fp32
   static constexpr int OFF_DQS = OFF_DS + 2 * DSTILE;
-  static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 4 * DQS_SLICE : 0);  // lse2, dvec
+  static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 16 * DQS_SLICE : 0);  // lse2, dvec
   static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
   // lut[lut_len] (bias, log2 units), diag[lut_len] (bias-gradient sums per delta), then the
   // bucket of each delta as bytes
   static constexpr int OFF_LUT = OFF_BAR + 256;
   static constexpr int NTHREADS = 640;
   static constexpr int NCOMP = 512;                     // threads of the P/dS warpgroups
+  // MMA issuers, one thread each, on three schedulers: S, dP, dV / dQ / dK
+  static constexpr int WARP_A = 19, WARP_B = 18, WARP_C = 17;
   // TMEM columns: S^T and dP^T (BQ each), dQ (64), P^T as packed bf16 pairs (BQ/2), dK, dV.
   // P has its own columns so that the next S^T product cannot overwrite it while the dV
   // product may still read it.
@@ -241,18 +243,20 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *dq_full = ds_empty + 2;
   uint64_t *dq_empty = dq_full + 1;
   uint64_t *dkdv_done = dq_empty + 1;
-  uint64_t *mma_done = dkdv_done + 1;  // [2], one per issuer
-  uint64_t *dqs_bar = mma_done + 2;    // [4][2]: dQ staging slice free / written, per warpgroup
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dqs_bar + 8);
+  uint64_t *mma_done = dkdv_done + 1;  // [3], one per issuer
+  uint64_t *s_consumed = mma_done + 3;  // S^T and dP^T of the tile are in registers
+  uint64_t *p_free = s_consumed + 1;    // the dV product has read P^T
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(p_free + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
   float *diag = lut + p.bias.lut_len;
   uint8_t *lbk = reinterpret_cast<uint8_t *>(diag + p.bias.lut_len);
 
-  // The producer warp sets up the barriers and completes its first step (K, V, the first Q/dO
-  // tile and its row statistics) before the rest of the block builds its tables, so the load
-  // latency overlaps them.
+  // The producer warp sets up the barriers and starts its first step (K, V, the first Q/dO tile
+  // and the loads of its row statistics) before the rest of the block builds its tables, so the
+  // load latency overlaps them. The statistics are stored and announced after the block sync.
   const bool early_q = !(p.debug_flags & 2);
+  float lv0[C::BQ / 32], dv0[C::BQ / 32];
   if (warp == 16) {
     if (lane == 0) {
       mbar_init(kv_full, 1);
@@ -264,14 +268,14 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(dp_full, 1);
       mbar_init(p_ready, C::NCOMP);
       mbar_init(ds_ready, C::NCOMP);
-      mbar_init(ds_empty, 1);
-      mbar_init(ds_empty + 1, 1);
+      mbar_init(ds_empty, 2);  // the dQ and dK products both read dS
+      mbar_init(ds_empty + 1, 2);
       mbar_init(dq_full, 1);
       mbar_init(dq_empty, C::NCOMP);
       mbar_init(dkdv_done, 2);
-      mbar_init(mma_done, 1);
-      mbar_init(mma_done + 1, 1);
-      for (int i = 0; i < 8; ++i) mbar_init(dqs_bar + i, 128);
+      for (int i = 0; i < 3; ++i) mbar_init(mma_done + i, 1);
+      mbar_init(s_consumed, C::NCOMP);
+      mbar_init(p_free, 1);
       *abort_flag = 0;
       fence_mbar_init();
       tma_prefetch_desc(&tm_q);
@@ -293,17 +297,15 @@ __global__ void __launch_bounds__(640, 1)
       for (int k = 0; k < C::BQ / 32; ++k) {
         const int q = qs0 + lane + 32 * k;
         const size_t idx = (size_t)h * T + seq_start + q;
-        s_lse2[lane + 32 * k] = q < L ? __ldg(p.lse + idx) * kLog2e : 0.f;
-        s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + idx) : 0.f;
+        lv0[k] = q < L ? __ldg(p.lse + idx) : 0.f;
+        dv0[k] = q < L ? __ldg(p.dvec + idx) : 0.f;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(qd_full, 2 * C::QTILE);
+        mbar_expect_tx(qd_full, 2 * C::QTILE);  // the warp's 32 arrivals follow the block sync
         for (int b = 0; b < C::DB; ++b) {
           tma_load_3d(&tm_q, qd_full, sQ + b * C::QBLK, 64 * b, h, seq_start + qs0);
           tma_load_3d(&tm_do, qd_full, sDO + b * C::QBLK, 64 * b, h, seq_start + qs0);
         }
-      } else {
-        mbar_arrive(qd_full);
       }
     }
   }
@@ -332,7 +334,14 @@ __global__ void __launch_bounds__(640, 1)
     for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
     const bool kv_issued = early_q && lane == 0;
     if (early_q) {
-      if (lane == 0) last_q[0] = 0;  // step 0 was done with the block set-up
+      // step 0: copies started with the block set-up; store its statistics and arrive
+#pragma unroll
+      for (int k = 0; k < C::BQ / 32; ++k) {
+        s_lse2[lane + 32 * k] = lv0[k] * kLog2e;
+        s_dvec[lane + 32 * k] = dv0[k];
+      }
+      mbar_arrive(qd_full);
+      if (lane == 0) last_q[0] = 0;
       for (int it = 1; it < nq; ++it) {
         const int st = it % C::NS, u = it / C::NS;
         const int qs = qtile_start(it);
@@ -373,12 +382,13 @@ __global__ void __launch_bounds__(640, 1)
       for (int x = 0; x < C::NS; ++x)
         if (last_q[x] >= 0) mbar_wait_teardown(qd_full + x, last_q[x] & 1, kTeardownNs);
     }
-  } else if (warp == 17 || warp == 18) {
+  } else if (warp == C::WARP_A || warp == C::WARP_B || warp == C::WARP_C) {
     // ------------------------------------------------------------------ MMA issuers
-    // Warp 17 issues the products that feed and consume P (S^T, dP^T, dV); warp 18 those that
-    // consume dS (dK, dQ). Two threads, so that neither chain of hand-offs waits behind the
-    // other; each Q/dO stage is released by both (the barrier counts two commits).
-    if (lane == 0) {
+    // Three warps on three schedulers: A issues the products that feed and consume P (S^T,
+    // dP^T, dV), B the dQ product and C the dK product, so that no chain of hand-offs waits
+    // behind another and the issue cost is spread; each Q/dO stage is released by A and C, each
+    // dS buffer by B and C.
+    {  // the whole warp runs the loop; one elected lane issues each instruction
       // descriptors built once; moving the start address by b bytes adds b >> 4
       const uint64_t dKk = sw128_desc(smem_u32(sK), 16, 1024);         // K, K-major
       const uint64_t dVk = sw128_desc(smem_u32(sV), 16, 1024);         // V, K-major
@@ -393,47 +403,48 @@ __global__ void __launch_bounds__(640, 1)
         // D[key][q] = sum_c A[key][c] * B[q][c]; A, B K-major
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + dcol, a0 + (((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4),
+          mma_bf16_ss_e(tmem + dcol, a0 + (((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4),
                       b0 + (((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4), C::IDESC_S, kk > 0);
       };
       bool ok = true;
-      if (warp == 17) {
+      if (warp == C::WARP_A) {
         auto issue_dv = [&](int st, bool acc) {
           // dV[key][c] += sum_q P^T[key][q] dO[q][c]; A = P^T in TMEM, B = dO MN-major
           const uint64_t b0 = dDOm + ((st * C::QTILE) >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < C::BQ / 16; ++k16)
-            mma_bf16_ts(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b0 + ((k16 * 2048) >> 4),
+            mma_bf16_ts_e(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b0 + ((k16 * 2048) >> 4),
                         C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
         };
-        ok = mbar_wait(kv_full, 0, wd) && mbar_wait(qd_full, 0, wd);
+        ok = warp_wait(kv_full, 0, wd) && warp_wait(qd_full, 0, wd);
         if (ok) {
           tc_fence_after();
           issue_qk(dKk, dQk, C::COL_S);
-          mma_commit(s_full);
+          mma_commit_e(s_full);
           issue_qk(dVk, dDOk, C::COL_DP);
-          mma_commit(dp_full);
+          mma_commit_e(dp_full);
         }
-        // dV as soon as P^T is in TMEM; the next tile's S^T and dP^T once dS^T is in shared
-        // memory (S^T and dP^T have then been consumed).
+        // The next tile's S^T and dP^T as soon as this tile's have been read into registers
+        // (they run while the P/dS pass computes); dV once P^T is in TMEM.
         for (int it = 0; ok && it < nq; ++it) {
           const int st = it % C::NS;
           const int stn = (it + 1) % C::NS, un = (it + 1) / C::NS;
-          if (!mbar_wait(p_ready, it & 1, wd)) { ok = false; break; }
-          tc_fence_after();
-          issue_dv(st, it > 0);
-          mma_commit(qd_empty + st);  // this issuer is done with Q_i / dO_i
           if (it + 1 < nq) {
-            if (!mbar_wait(ds_ready, it & 1, wd) || !mbar_wait(qd_full + stn, un & 1, wd)) {
+            if (!warp_wait(s_consumed, it & 1, wd) || !warp_wait(qd_full + stn, un & 1, wd)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_qk(dKk, dQk + ((stn * C::QTILE) >> 4), C::COL_S);
-            mma_commit(s_full);
+            mma_commit_e(s_full);
             issue_qk(dVk, dDOk + ((stn * C::QTILE) >> 4), C::COL_DP);
-            mma_commit(dp_full);
+            mma_commit_e(dp_full);
           }
+          if (!warp_wait(p_ready, it & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          issue_dv(st, it > 0);
+          mma_commit_e(p_free);
+          mma_commit_e(qd_empty + st);  // this issuer is done with Q_i / dO_i
         }
       } else {
         auto issue_dk = [&](int buf, int st, bool acc) {
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(640, 1)
           const uint64_t b0 = dQm + ((st * C::QTILE) >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < C::BQ / 16; ++k16)
-            mma_bf16_ss(tmem + C::COL_DK,
+            mma_bf16_ss_e(tmem + C::COL_DK,
                         a0 + ((((16 * k16) >> 6) * C::DSBLK + (((16 * k16) & 63) >> 4) * 32) >> 4),
                         b0 + ((k16 * 2048) >> 4), C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
         };
@@ -451,28 +462,37 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
           for (int k16 = 0; k16 < 8; ++k16) {  // 128 keys
             if (D == 64)  // dQ[q][c] = sum_key dS[q][key] K[key][c]
-              mma_bf16_ss(tmem + C::COL_DQ, ds0 + ((k16 * 2048) >> 4), dKm + ((k16 * 2048) >> 4),
+              mma_bf16_ss_e(tmem + C::COL_DQ, ds0 + ((k16 * 2048) >> 4), dKm + ((k16 * 2048) >> 4),
                           C::IDESC_DQ, k16 > 0);
             else          // dQ^T[c][q] = sum_key K[key][c] dS^T[key][q]
-              mma_bf16_ss(tmem + C::COL_DQ, dKm + ((k16 * 2048) >> 4), ds0 + ((k16 * 2048) >> 4),
+              mma_bf16_ss_e(tmem + C::COL_DQ, dKm + ((k16 * 2048) >> 4), ds0 + ((k16 * 2048) >> 4),
                           C::IDESC_DQ, k16 > 0);
           }
         };
-        for (int it = 0; ok && it < nq; ++it) {
-          const int st = it % C::NS;
-          if (!mbar_wait(ds_ready, it & 1, wd)) { ok = false; break; }
-          if (it >= 1 && !mbar_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
-          tc_fence_after();
-          issue_dq(it & 1);
-          mma_commit(dq_full);
-          issue_dk(it & 1, st, it > 0);
-          mma_commit(ds_empty + (it & 1));
-          mma_commit(qd_empty + st);
+        if (warp == C::WARP_B) {
+          for (int it = 0; ok && it < nq; ++it) {
+            if (!warp_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+            if (it >= 1 && !warp_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_dq(it & 1);
+            mma_commit_e(dq_full);
+            mma_commit_e(ds_empty + (it & 1));
+          }
+        } else {
+          for (int it = 0; ok && it < nq; ++it) {
+            const int st = it % C::NS;
+            if (!warp_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_dk(it & 1, st, it > 0);
+            mma_commit_e(ds_empty + (it & 1));
+            mma_commit_e(qd_empty + st);  // this issuer is done with Q_i
+          }
         }
       }
-      if (ok) mma_commit(dkdv_done);
-      mma_commit(mma_done + (warp - 17));
-      mbar_wait_teardown(mma_done + (warp - 17), 0, kTeardownNs);
+      if (ok && warp != C::WARP_B) mma_commit_e(dkdv_done);  // the dV and dK issuers
+      const int who = warp == C::WARP_A ? 0 : (warp == C::WARP_B ? 1 : 2);
+      mma_commit_e(mma_done + who);
+      mbar_wait_teardown(mma_done + who, 0, kTeardownNs);
     }
   } else if (warp < 16) {
     // ------------------------------------------------------------------ P / dS warpgroups
@@ -498,30 +518,25 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_before();
       mbar_arrive(dq_empty);
       const int qs = qtile_start(it);
-      if (C::DQ_TMA) {  // lane = query row, columns = channels 16*wg ..: stage, bulk-reduce
-        uint8_t *slice = sDQS + wg * C::DQS_SLICE;
-        uint64_t *bar_free = dqs_bar + 2 * wg, *bar_written = bar_free + 1;
-        if (it >= 1) {  // the previous bulk reduction of this slice has finished reading
-          if (r == 0) bulk_wait_read_all();
-          mbar_arrive(bar_free);
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_free, (it - 1) & 1, wd))) return false;
+      if (C::DQ_TMA) {
+        // lane = query row, columns = channels 16*wg ..: each warp stages its 32 x 16 block and
+        // lane 0 adds it with one bulk tensor reduction (no synchronisation beyond the warp).
+        uint8_t *slice = sDQS + warp * C::DQS_SLICE;
+        if (it >= 1) {  // the previous reduction of this slice has finished reading it
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(slice + r * 64);
+        uint4 *dst = reinterpret_cast<uint4 *>(slice + lane * 64);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         fence_proxy_async_smem();
-        mbar_arrive(bar_written);
+        __syncwarp();
         // rows past the document end carry zeros (their dS is masked), rows past T are clipped
-        bool issued = true;
-        if (r == 0) {
-          issued = mbar_wait(bar_written, it & 1, wd);
-          if (issued) {
-            tma_reduce_add_3d(&tm_dq, slice, 16 * wg, h, seq_start + qs);
-            bulk_commit_group();
-          }
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, slice, 16 * wg, h, seq_start + qs + 32 * (warp & 3));
+          bulk_commit_group();
         }
-        return __all_sync(0xffffffffu, issued);  // same answer for the whole warp
       } else {  // lane = channel, columns = query rows 16*wg ..
         float *dst = p.dq_acc + ((size_t)(seq_start + qs + 16 * wg) * H + h) * D + r;
         const size_t step = (size_t)H * D;
@@ -537,7 +552,10 @@ __global__ void __launch_bounds__(640, 1)
       const int st = it % C::NS;
       const int qs = qtile_start(it);
       ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
-           __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd));
+           __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd)) &&
+           __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
+           (it < 2 ||
+            __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
       if (!ok) break;
       tc_fence_after();
       const int d0 = ks - qs;  // delta of (key row 0, query column 0)
@@ -564,15 +582,30 @@ __global__ void __launch_bounds__(640, 1)
       const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
       const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
       const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
-      // ---- P^T = 2^(x - lse2) for this warpgroup's query columns, 16 at a time
+      // ---- one pass per 16 query columns: P^T = 2^(x - lse2) (bf16 to TMEM for the dV
+      // product), dS^T = P^T (dP^T - D) in fp32 from the same registers (bf16, swizzled, to
+      // shared memory for the dK / dQ products). Table gradient: far tiles add into one register
+      // per side; near tiles sum each 32-row block along its diagonals with warp shuffles (lane
+      // m collects deltas base + m and base + m - 32) and add two values per lane into the
+      // per-delta array.
       {
         const float *lut_row = lut + lut_base;
         const float sl = p.scale_log2;
         const int mode = (side == 0 ? 0 : (linear ? 2 : 1)) * 2 + (need_mask ? 1 : 0);
+        uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
+        const bool near_db = do_dbias && side == 0;
+        float acc_a = 0.f, acc_b = 0.f, part = 0.f;
 #pragma unroll
         for (int sub = 0; sub < QW / 16; ++sub) {
-          uint32_t raw[16], pk[8];
-          tmem_ld16(tS + 16 * sub, raw);
+          uint32_t raw[16], dp[16], pk[8];
+          tmem_ld16_issue(tS + 16 * sub, raw);
+          tmem_ld16_issue(tDP + 16 * sub, dp);
+          tmem_ld16_fence(raw);
+          tmem_ld16_fence(dp);
+          if (sub == QW / 16 - 1) {  // S^T, dP^T fully read: the next tile's may be computed
+            tc_fence_before();
+            mbar_arrive(s_consumed);
+          }
           const float4 *l4 = lse4 + 4 * sub;
           const int jc = c0 + 16 * sub;
           switch (mode) {
@@ -583,40 +616,19 @@ __global__ void __launch_bounds__(640, 1)
             case 4: bwd_p_chunk<16, 2, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
             default: bwd_p_chunk<16, 2, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
           }
-          tmem_st8(tP + 8 * sub, pk);     // bf16 P^T: A operand of the dV product
-          tmem_st16(tS + 16 * sub, raw);  // fp32 P^T over S^T: read back by the dS pass
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_ready);
-      // ---- dS^T = P^T (dP^T - D), to shared memory (bf16, swizzled) for the dK / dQ MMAs.
-      // P^T is read back in fp32 from where S^T was (the next S^T is issued only after this
-      // pass). Table gradient: far tiles add into one register per side; near tiles sum each
-      // 32-row block along its diagonals with warp shuffles (lane m collects deltas base + m
-      // and base + m - 32) and add two values per lane into the per-delta array.
-      ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
-           (it < 2 ||
-            __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
-        const bool near_db = do_dbias && side == 0;
-        float acc_a = 0.f, acc_b = 0.f, part = 0.f;
-        // 16 columns at a time (keeps the P and dP chunks in registers)
-#pragma unroll
-        for (int sub = 0; sub < QW / 16; ++sub) {
-          uint32_t pf[16], dp[16], pk[8];
-          tmem_ld16(tS + 16 * sub, pf);
-          tmem_ld16(tDP + 16 * sub, dp);
+          if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
+            ok = __all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
           const float4 *d4 = dvs4 + 4 * sub;
           if (sub == 0)
-            part += near_db ? bwd_ds_chunk<16, true, 0>(pf, dp, d4, pk, lane, acc_a, acc_b)
-                            : bwd_ds_chunk<16, false, 0>(pf, dp, d4, pk, lane, acc_a, acc_b);
+            part += near_db ? bwd_ds_chunk<16, true, 0>(raw, dp, d4, pk, lane, acc_a, acc_b)
+                            : bwd_ds_chunk<16, false, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
           else
-            part += near_db ? bwd_ds_chunk<16, true, 16>(pf, dp, d4, pk, lane, acc_a, acc_b)
-                            : bwd_ds_chunk<16, false, 16>(pf, dp, d4, pk, lane, acc_a, acc_b);
+            part += near_db ? bwd_ds_chunk<16, true, 16>(raw, dp, d4, pk, lane, acc_a, acc_b)
+                            : bwd_ds_chunk<16, false, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
             const int j0 = c0 + 16 * sub + 8 * g;
@@ -626,6 +638,10 @@ __global__ void __launch_bounds__(640, 1)
                 make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
           }
         }
+        if (!ok) break;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready);
         if (near_db) {
           // delta of (row of lane m, column t) = base + m - t
           const int base = d0 + 32 * (warp & 3) - c0 - p.bias.lut_lo;
@@ -646,7 +662,7 @@ __global__ void __launch_bounds__(640, 1)
       }
     }
     if (ok && nq >= 1) ok = drain_dq(nq - 1);
-    if (C::DQ_TMA && r == 0) bulk_wait_all();  // reductions complete before shared memory is released
+    if (C::DQ_TMA && lane == 0) bulk_wait_all();  // reductions complete before shared memory is released
     // ---- dK, dV: this warpgroup's quarter of the channels
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
     if (ok) {
@@ -732,7 +748,7 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   const int bq = head_dim == 64 ? BwdCfg<64, 2>::BQ : BwdCfg<128, 2>::BQ;
   if (make_tmap_thd(&mq, q, T, H, head_dim, bq) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
       make_tmap_thd(&mv, v, T, H, head_dim, 128) || make_tmap_thd(&mdo, dout, T, H, head_dim, bq) ||
-      make_tmap_thd_f32(&mdq, p.dq_acc, T, H, head_dim, 16, 128))
+      make_tmap_thd_f32(&mdq, p.dq_acc, T, H, head_dim, 16, 32))
     return (int)cudaErrorInvalidValue;
   const size_t smem = bwd_smem_bytes(head_dim, p.bias.lut_len);
   const int ns = bwd_stages(head_dim, p.bias.lut_len);
