@@ -28,6 +28,7 @@
 // Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, P, dK and dV
 // fit the 512 TMEM columns together.
 #include <cstdio>
+#include <type_traits>
 
 #include "fat_attn_internal.cuh"
 
@@ -591,52 +592,63 @@ __global__ void __launch_bounds__(640, 1)
       {
         const float *lut_row = lut + lut_base;
         const float sl = p.scale_log2;
-        const int mode = (side == 0 ? 0 : (linear ? 2 : 1)) * 2 + (need_mask ? 1 : 0);
         uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
         const bool near_db = do_dbias && side == 0;
         float acc_a = 0.f, acc_b = 0.f, part = 0.f;
+        // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
+        // once per tile, so no chunk carries the other forms' instructions.
+        auto pass = [&](auto bias_c, auto mask_c, auto near_c) -> bool {
+          constexpr int BIAS = decltype(bias_c)::value;
+          constexpr bool MASK = decltype(mask_c)::value;
+          constexpr bool NEAR = decltype(near_c)::value;
 #pragma unroll
-        for (int sub = 0; sub < QW / 16; ++sub) {
-          uint32_t raw[16], dp[16], pk[8];
-          tmem_ld16_issue(tS + 16 * sub, raw);
-          tmem_ld16_issue(tDP + 16 * sub, dp);
-          tmem_ld16_fence(raw);
-          tmem_ld16_fence(dp);
-          if (sub == QW / 16 - 1) {  // S^T, dP^T fully read: the next tile's may be computed
-            tc_fence_before();
-            mbar_arrive(s_consumed);
+          for (int sub = 0; sub < QW / 16; ++sub) {
+            uint32_t raw[16], dp[16], pk[8];
+            tmem_ld16_issue(tS + 16 * sub, raw);
+            tmem_ld16_issue(tDP + 16 * sub, dp);
+            tmem_ld16_fence(raw);
+            tmem_ld16_fence(dp);
+            if (sub == QW / 16 - 1) {  // S^T, dP^T fully read: the next tile's may be computed
+              tc_fence_before();
+              mbar_arrive(s_consumed);
+            }
+            bwd_p_chunk<16, BIAS, MASK>(raw, pk, lse4 + 4 * sub, lut_row, c0 + 16 * sub, rowc, kq,
+                                        sl, lo_j, hi_j);
+            if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
+              if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
+              tc_fence_after();
+            }
+            tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
+            const float4 *d4 = dvs4 + 4 * sub;
+            if (sub == 0)
+              part += bwd_ds_chunk<16, NEAR, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
+            else
+              part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
+              const int j0 = c0 + 16 * sub + 8 * g;
+              const int chunk = (j0 & 63) >> 3;
+              uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4 *>(dst) =
+                  make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
           }
-          const float4 *l4 = lse4 + 4 * sub;
-          const int jc = c0 + 16 * sub;
-          switch (mode) {
-            case 0: bwd_p_chunk<16, 0, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-            case 1: bwd_p_chunk<16, 0, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-            case 2: bwd_p_chunk<16, 1, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-            case 3: bwd_p_chunk<16, 1, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-            case 4: bwd_p_chunk<16, 2, false>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-            default: bwd_p_chunk<16, 2, true>(raw, pk, l4, lut_row, jc, rowc, kq, sl, lo_j, hi_j); break;
-          }
-          if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
-            ok = __all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
-          const float4 *d4 = dvs4 + 4 * sub;
-          if (sub == 0)
-            part += near_db ? bwd_ds_chunk<16, true, 0>(raw, dp, d4, pk, lane, acc_a, acc_b)
-                            : bwd_ds_chunk<16, false, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
+          return true;
+        };
+        using B0 = std::integral_constant<int, 0>;
+        using B1 = std::integral_constant<int, 1>;
+        using B2 = std::integral_constant<int, 2>;
+        using Y = std::true_type;
+        using N = std::false_type;
+        if (side == 0) {  // lookup table
+          if (near_db)
+            ok = need_mask ? pass(B0{}, Y{}, Y{}) : pass(B0{}, N{}, Y{});
           else
-            part += near_db ? bwd_ds_chunk<16, true, 16>(raw, dp, d4, pk, lane, acc_a, acc_b)
-                            : bwd_ds_chunk<16, false, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
-            const int j0 = c0 + 16 * sub + 8 * g;
-            const int chunk = (j0 & 63) >> 3;
-            uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4 *>(dst) =
-                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-          }
+            ok = need_mask ? pass(B0{}, Y{}, N{}) : pass(B0{}, N{}, N{});
+        } else if (!linear) {  // constant over the tile
+          ok = need_mask ? pass(B1{}, Y{}, N{}) : pass(B1{}, N{}, N{});
+        } else {  // linear in the query index
+          ok = need_mask ? pass(B2{}, Y{}, N{}) : pass(B2{}, N{}, N{});
         }
         if (!ok) break;
         tmem_st_wait();
