@@ -202,8 +202,9 @@ __global__ void __launch_bounds__(640, 1)
   using C = BwdCfg<D, NSTAGES>;
   constexpr int QW = C::QW;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base (the 128-byte swizzle atoms need it), reached by indexing the
+  // shared array itself so every derived pointer stays a shared-memory pointer
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb = blockIdx.x, h = blockIdx.y, doc = blockIdx.z;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;

@@ -101,8 +101,9 @@ __global__ void __launch_bounds__(384, 1)
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base (the 128-byte swizzle atoms need it), reached by indexing the
+  // shared array itself so every derived pointer stays a shared-memory pointer
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int doc = blockIdx.z, h = blockIdx.y;
   const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first when causal
