@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
                                                            float4 *__restrict__ dq_acc,
                                                            float *__restrict__ dbias, int nbias,
                                                            int T, int H) {
+  grid_dep_launch();  // the main backward grid may be scheduled (it waits for this one's writes)
   constexpr int LPR = D / 8;         // lanes per row, 8 bf16 each
   constexpr int RPW = 32 / LPR;      // rows per warp step
   const int lane = threadIdx.x & 31;
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
 __global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const float4 *__restrict__ acc,
                                                              uint4 *__restrict__ dq, float scale,
                                                              long long n8) {
+  grid_dep_wait();  // the accumulator is complete (a no-op when launched without overlap)
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   auto cvt = [scale](float4 a, float4 b) {
@@ -451,12 +453,13 @@ int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *
   return launch_rc("backward preprocess launch");
 }
 
-int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const void *v,
-                      const float *bias_table, int num_buckets, int max_distance,
-                      int bidirectional, const float *alibi_slopes, const int32_t *cu_seqlens,
-                      int causal, float softmax_scale, const float *lse, const void *dout,
-                      void *workspace, size_t workspace_bytes, void *dk, void *dv,
-                      float *dbias_table) {
+namespace {
+int bwd_main_impl(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                  float softmax_scale, const float *lse, const void *dout, void *workspace,
+                  size_t workspace_bytes, void *dk, void *dv, float *dbias_table,
+                  bool overlap_previous) {
   int rc = check_shape(sh);
   if (rc) return rc;
   if (!q || !k || !v || !cu_seqlens || !lse || !dout || !dk || !dv) return FAT_EINVAL_NULL;
@@ -491,11 +494,11 @@ int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const
     p.debug_flags = g_debug_flags;
   }
   return cuda_rc(launch_bwd(p, sh->head_dim, sh->max_seqlen, q, k, v, nullptr, dout,
-                           static_cast<cudaStream_t>(sh->stream)));
+                           static_cast<cudaStream_t>(sh->stream), overlap_previous));
 }
 
-int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
-                          float softmax_scale, void *dq) {
+int bwd_finalize_impl(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
+                      float softmax_scale, void *dq, bool overlap_previous) {
   int rc = check_shape(sh);
   if (rc) return rc;
   if (!dq) return FAT_EINVAL_NULL;
@@ -506,9 +509,42 @@ int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t w
   const long long n8 = (long long)sh->total_tokens * sh->num_heads * sh->head_dim / 8;
   if (n8 == 0) return FAT_OK;
   const int blocks = (int)std::min<long long>((n8 + 255) / 256, 152LL * 8);
-  fat_bwd_finish_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(sh->stream)>>>(
-      reinterpret_cast<const float4 *>(ws.dq_acc), static_cast<uint4 *>(dq), softmax_scale, n8);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(sh->stream);
+  if (overlap_previous) {  // programmatic dependent launch on the main backward grid
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fat_bwd_finish_kernel,
+                                           reinterpret_cast<const float4 *>(ws.dq_acc),
+                                           static_cast<uint4 *>(dq), softmax_scale, n8);
+  if (e != cudaSuccess) {
+    set_last_error("backward finalize launch", (int)e, cudaGetErrorString(e));
+    return FAT_ECUDA;
+  }
   return launch_rc("backward finalize launch");
+}
+}  // namespace
+
+int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                      const float *bias_table, int num_buckets, int max_distance,
+                      int bidirectional, const float *alibi_slopes, const int32_t *cu_seqlens,
+                      int causal, float softmax_scale, const float *lse, const void *dout,
+                      void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                      float *dbias_table) {
+  return bwd_main_impl(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                       alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
+                       workspace_bytes, dk, dv, dbias_table, false);
+}
+
+int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
+                          float softmax_scale, void *dq) {
+  return bwd_finalize_impl(sh, workspace, workspace_bytes, softmax_scale, dq, false);
 }
 
 int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
@@ -536,11 +572,13 @@ int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void
   rc = fat_attn_bwd_preprocess(sh, out, dout, workspace, workspace_bytes, dbias_table,
                                num_buckets);
   if (rc) return rc;
-  rc = fat_attn_bwd_main(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
-                         alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
-                         workspace_bytes, dk, dv, dbias_table);
+  // The main and finishing grids are launched as programmatic dependents of the grid before
+  // them: each starts its set-up while that grid drains and waits for its writes in-kernel.
+  rc = bwd_main_impl(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                     alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
+                     workspace_bytes, dk, dv, dbias_table, true);
   if (rc) return rc;
-  return fat_attn_bwd_finalize(sh, workspace, workspace_bytes, softmax_scale, dq);
+  return bwd_finalize_impl(sh, workspace, workspace_bytes, softmax_scale, dq, true);
 }
 
 int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(640, 1)
   // and the loads of its row statistics) before the rest of the block builds its tables, so the
   // load latency overlaps them. The statistics are stored and announced after the block sync.
   const bool early_q = !(p.debug_flags & 2);
-  float lv0[C::BQ / 32], dv0[C::BQ / 32];
+  float lv0[C::BQ / 32];
   if (warp == 16) {
     if (lane == 0) {
       mbar_init(kv_full, 1);
@@ -300,7 +300,6 @@ __global__ void __launch_bounds__(640, 1)
         const int q = qs0 + lane + 32 * k;
         const size_t idx = (size_t)h * T + seq_start + q;
         lv0[k] = q < L ? __ldg(p.lse + idx) : 0.f;
-        dv0[k] = q < L ? __ldg(p.dvec + idx) : 0.f;
       }
       if (lane == 0) {
         mbar_expect_tx(qd_full, 2 * C::QTILE);  // the warp's 32 arrivals follow the block sync
@@ -325,6 +324,9 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above reads only inputs of the backward. D, the zeroed dQ accumulator and the
+  // zeroed table gradient come from the preprocessing grid, which this launch may overlap.
+  grid_dep_wait();
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_BWD, p.timeout_ns};
   float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (P/dS warps)
@@ -337,10 +339,12 @@ __global__ void __launch_bounds__(640, 1)
     const bool kv_issued = early_q && lane == 0;
     if (early_q) {
       // step 0: copies started with the block set-up; store its statistics and arrive
+      const int qs0 = qtile_start(0);
 #pragma unroll
       for (int k = 0; k < C::BQ / 32; ++k) {
+        const int q = qs0 + lane + 32 * k;
         s_lse2[lane + 32 * k] = lv0[k] * kLog2e;
-        s_dvec[lane + 32 * k] = dv0[k];
+        s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + (size_t)h * T + seq_start + q) : 0.f;
       }
       mbar_arrive(qd_full);
       if (lane == 0) last_q[0] = 0;
@@ -676,6 +680,7 @@ __global__ void __launch_bounds__(640, 1)
     }
     if (ok && nq >= 1) ok = drain_dq(nq - 1);
     if (C::DQ_TMA && lane == 0) bulk_wait_all();  // reductions complete before shared memory is released
+    grid_dep_launch();  // the finishing grid may be scheduled
     // ---- dK, dV: this warpgroup's quarter of the channels
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
     if (ok) {
@@ -754,7 +759,8 @@ __global__ void __launch_bounds__(640, 1)
 }
 
 int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, const void *out, const void *dout, cudaStream_t stream) {
+               const void *v, const void *out, const void *dout, cudaStream_t stream,
+               bool overlap_previous) {
   (void)out;
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
@@ -767,21 +773,37 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   const int ns = bwd_stages(head_dim, p.bias.lut_len);
   dim3 grid((max_seqlen + 127) / 128, H, p.seq.num_seqs);
   cudaError_t e;
+  bool attr_failed = false;
   auto go = [&](auto kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      kernel<<<grid, BwdCfg<64, 2>::NTHREADS, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
+    if (e != cudaSuccess) {
+      attr_failed = true;
+      return;
+    }
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(BwdCfg<64, 2>::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (overlap_previous) {  // programmatic dependent launch on the preprocessing grid
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, mdq, p);
   };
   if (head_dim == 64) {
     if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
   } else {
     if (ns == 3) go(fat_bwd_kernel<128, 3>); else go(fat_bwd_kernel<128, 2>);
   }
-  if (e != cudaSuccess) {
+  if (attr_failed) {
     set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
     return (int)e;
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
     if (head_dim == 64)

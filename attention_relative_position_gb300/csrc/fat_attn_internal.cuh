@@ -118,8 +118,11 @@ struct BwdParams {
 int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
                const void *v, cudaStream_t stream);
 size_t fwd_smem_bytes(int head_dim, int lut_len);
+// overlap_previous: launch as a programmatic dependent of the previous grid in the stream (only
+// when that grid is this library's preprocessing grid, which itself waited for its inputs).
 int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, const void *out, const void *dout, cudaStream_t stream);
+               const void *v, const void *out, const void *dout, cudaStream_t stream,
+               bool overlap_previous);
 size_t bwd_smem_bytes(int head_dim, int lut_len);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);

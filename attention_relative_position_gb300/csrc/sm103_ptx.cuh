@@ -390,6 +390,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Programmatic dependent launch. grid_dep_wait: block until the grids this one was launched
+// to depend on have completed and their writes are visible (returns at once when there are
+// none). grid_dep_launch: let the dependent grid be scheduled once every CTA of this grid has
+// signalled or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Re-balance the register file between warpgroups (whole warpgroup executes it). The sum over
 // warpgroups must stay within what the block was launched with.
 template <int N>

@@ -171,10 +171,21 @@ class Runner:
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.stream = torch.cuda.current_stream(device)
 
-    def step(self, events=None):
+    def step(self):
+        """One pass of the hot path through the public calls (forward, then the fused backward,
+        whose main and finishing grids overlap the set-up of the grid before them)."""
         fa, x, w = self.fa, self.x, self.w
-        if events is not None:
-            events[0].record(self.stream)
+        fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, out=self.out,
+                        lse=self.lse, stream=self.stream, **self.kw)
+        fa.fat_attn_bwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, self.out,
+                        self.lse, x["dout"], workspace=self.ws, dq=self.dq, dk=self.dk,
+                        dv=self.dv, dbias_table=self.dtab, stream=self.stream, **self.kw)
+
+    def step_staged(self, events):
+        """The same work as step(), backward as its three stage calls with CUDA events between
+        the kernels (per-kernel times; no overlap between the grids)."""
+        fa, x, w = self.fa, self.x, self.w
+        events[0].record(self.stream)
         fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, out=self.out,
                         lse=self.lse, stream=self.stream, **self.kw)
         between = None
@@ -196,14 +207,25 @@ class Runner:
 
 
 def time_steps(r, steps, flush=True):
-    """Per-kernel device times (ms) of `steps` steps; L2 flushed between steps (not timed)."""
+    """Device times (ms) of `steps` steps, L2 flushed between steps (not timed): "step" from
+    steps through the public calls, each bracketed by CUDA events on the launching stream;
+    the per-kernel times from as many steps run stage by stage with events between kernels."""
     torch = r.torch
-    per = {"fwd": [], "bwd_pre": [], "bwd_main": [], "bwd_fin": [], "step": []}
+    per = {"fwd": [], "bwd_pre": [], "bwd_main": [], "bwd_fin": [], "step": [], "step_staged": []}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            r.flush_l2()
+        evs[i][0].record(r.stream)
+        r.step()
+        evs[i][1].record(r.stream)
+    torch.cuda.synchronize()
+    per["step"] = [e[0].elapsed_time(e[1]) for e in evs]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     for i in range(steps):
         if flush:
             r.flush_l2()
-        r.step(evs[i])
+        r.step_staged(evs[i])
     torch.cuda.synchronize()
     for e in evs:
         t = [e[j].elapsed_time(e[j + 1]) for j in range(4)]
@@ -211,7 +233,7 @@ def time_steps(r, steps, flush=True):
         per["bwd_pre"].append(t[1])
         per["bwd_main"].append(t[2])
         per["bwd_fin"].append(t[3])
-        per["step"].append(sum(t))
+        per["step_staged"].append(sum(t))
     return per
 
 
