@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
                                                            float4 *__restrict__ dq_acc,
                                                            float *__restrict__ dbias, int nbias,
                                                            int T, int H) {
+  grid_dep_wait();    // the forward's outputs are complete (a no-op when launched without overlap)
   grid_dep_launch();  // the main backward grid may be scheduled (it waits for this one's writes)
   constexpr int LPR = D / 8;         // lanes per row, 8 bf16 each
   constexpr int RPW = 32 / LPR;      // rows per warp step
@@ -418,9 +419,10 @@ int launch_rc(const char *what) {
 }
 }  // namespace
 
-int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *dout,
-                            void *workspace, size_t workspace_bytes, float *dbias_table,
-                            int num_buckets) {
+namespace {
+int bwd_preprocess_impl(const fat_shape_t *sh, const void *out, const void *dout, void *workspace,
+                        size_t workspace_bytes, float *dbias_table, int num_buckets,
+                        bool overlap_previous) {
   int rc = check_shape(sh);
   if (rc) return rc;
   if (!out || !dout) return FAT_EINVAL_NULL;
@@ -444,13 +446,35 @@ int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *
   const auto *o = static_cast<const uint4 *>(out);
   const auto *g = static_cast<const uint4 *>(dout);
   float4 *acc4 = reinterpret_cast<float4 *>(ws.dq_acc);
-  if (d == 64)
-    fat_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, acc4, dbias_table, nbias,
-                                                         T, H);
-  else
-    fat_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, ws.dvec, acc4, dbias_table, nbias,
-                                                          T, H);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  if (overlap_previous) {  // it waits for the previous grid before touching memory
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e =
+      d == 64 ? cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<64>, o, g, ws.dvec, acc4, dbias_table,
+                                   nbias, T, H)
+              : cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<128>, o, g, ws.dvec, acc4,
+                                   dbias_table, nbias, T, H);
+  if (e != cudaSuccess) {
+    set_last_error("backward preprocess launch", (int)e, cudaGetErrorString(e));
+    return FAT_ECUDA;
+  }
   return launch_rc("backward preprocess launch");
+}
+}  // namespace
+
+int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *dout,
+                            void *workspace, size_t workspace_bytes, float *dbias_table,
+                            int num_buckets) {
+  return bwd_preprocess_impl(sh, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
+                             false);
 }
 
 namespace {
@@ -569,11 +593,12 @@ int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void
     rc = check_workspace(sh, workspace, workspace_bytes, &ws);
     if (rc) return rc;
   }
-  rc = fat_attn_bwd_preprocess(sh, out, dout, workspace, workspace_bytes, dbias_table,
-                               num_buckets);
+  rc = bwd_preprocess_impl(sh, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
+                           true);
   if (rc) return rc;
-  // The main and finishing grids are launched as programmatic dependents of the grid before
-  // them: each starts its set-up while that grid drains and waits for its writes in-kernel.
+  // All three grids are launched as programmatic dependents of the grid before them: each is
+  // scheduled while that grid drains and waits for its writes in-kernel (the preprocessing grid
+  // before it touches memory; the main grid before it reads D or touches the accumulators).
   rc = bwd_main_impl(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
                      alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
                      workspace_bytes, dk, dv, dbias_table, true);

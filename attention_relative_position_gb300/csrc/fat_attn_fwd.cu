@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(p_ready + t);
       }
+      grid_dep_launch();  // a dependent grid (the backward preprocessing) may be scheduled
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (nk - 1) & 1, wd));
       if (ok) {
         tc_fence_after();
