@@ -9,22 +9,22 @@
 // document (only those at or after the key tile when causal). Everything is computed in the
 // key-major frame (TMEM lane = key row). Five warpgroups, one warp of each per SM
 // sub-partition:
-//   warps 0-15   four P/dS warpgroups, each owning a quarter of the query columns of a tile:
-//                P^T = 2^(x - lse) written to TMEM as bf16 (own columns, the A operand of dV)
-//                and fp32 (over S^T, read back by the dS pass); dS^T = P^T (dP^T - D) written
-//                to shared memory in the 128-byte-swizzled layout the MMAs read; table-gradient
-//                partial sums; a quarter of each dQ tile drained from TMEM into the fp32 dQ
-//                accumulator with vector reductions; a quarter of dK, dV at the end.
+//   warps 0-15   four P/dS warpgroups, each owning a quarter of the query columns of a tile.
+//                One pass per 16 columns reads S^T and dP^T from TMEM (the next tile's
+//                products may then be issued), forms P^T = 2^(x - lse) (bf16 to TMEM: the A
+//                operand of dV) and dS^T = P^T (dP^T - D) in fp32 from the same registers
+//                (bf16, 128-byte swizzled, to shared memory for the dK / dQ products), and
+//                keeps table-gradient partial sums; then a quarter of each dQ tile goes from
+//                TMEM into the fp32 dQ accumulator, and at the end a quarter of dK, dV.
 //   warp 16      TMA producer: K, V once; Q_i, dO_i (and lse_i, D_i) through a 2-3 stage ring.
-//   warp 17      MMA issuer for S^T = K Q_i^T, dP^T = V dO_i^T and dV += P^T dO_i (P^T from
-//                TMEM), tcgen05 with fp32 accumulators in TMEM.
-//   warp 18      MMA issuer for dK += dS^T Q_i and dQ_i = dS K (d = 64) or dQ_i^T = K^T dS^T
-//                (d = 128); dK and dV stay in TMEM for the whole walk.
-//   warp 19      idle (it completes the fifth warpgroup).
+//   warps 17-19  MMA issuers (whole warps, one elected lane issues): C = dK += dS^T Q_i,
+//                B = dQ_i = dS K (d = 64) or dQ_i^T = K^T dS^T (d = 128), A = S^T = K Q_i^T,
+//                dP^T = V dO_i^T and dV += P^T dO_i (P^T from TMEM); fp32 accumulators in
+//                TMEM, dK and dV for the whole walk.
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
 // the other tiles reduce each 32-row block along its diagonals with warp shuffles and add the
-// sums into a shared-memory array indexed by delta; at the end the CTA maps deltas to buckets
-// and issues one global atomic per (bucket, head).
+// sums into a shared-memory array indexed by delta; at the end the CTA folds deltas into
+// buckets (segmented warp scan) and adds each run once into the global table gradient.
 // Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, P, dK and dV
 // fit the 512 TMEM columns together.
 #include <cstdio>
