@@ -148,6 +148,20 @@ int cuda_rc(int e) { return e == 0 ? FAT_OK : FAT_ECUDA; }
 
 }  // namespace
 
+int sm_count() {
+  static std::mutex mu;
+  static int cached[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 void set_last_error(const char *what, int code, const char *text) {
   snprintf(g_last_error, sizeof g_last_error, "%s: error %d (%s)", what, code, text ? text : "");
 }

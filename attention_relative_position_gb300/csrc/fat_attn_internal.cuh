@@ -57,12 +57,17 @@ __device__ __forceinline__ int t5_bucket_dev(int delta, const BiasParams &b) {
   return off + b.me + t;
 }
 
-// Bias of relative position `delta` for head h, in log2 units (natural bias * log2(e)).
-__device__ __forceinline__ float bias_log2_dev(int delta, int h, int H, const BiasParams &b) {
+// Bias of relative position `delta` (whose T5 bucket is `bucket`) for head h, in log2 units
+// (natural bias * log2(e)).
+__device__ __forceinline__ float bias_log2_bucket_dev(int bucket, int delta, int h, int H,
+                                                      const BiasParams &b) {
   float v = 0.f;
-  if (b.table) v += __ldg(b.table + (size_t)t5_bucket_dev(delta, b) * H + h);
+  if (b.table) v += __ldg(b.table + (size_t)bucket * H + h);
   if (b.slopes) v -= __ldg(b.slopes + h) * (float)(delta < 0 ? -delta : delta);
   return v * kLog2e;
+}
+__device__ __forceinline__ float bias_log2_dev(int delta, int h, int H, const BiasParams &b) {
+  return bias_log2_bucket_dev(b.table ? t5_bucket_dev(delta, b) : 0, delta, h, H, b);
 }
 
 // Closed-form bias on the far sides, in log2 units: bias(delta) = c + k * delta.
@@ -110,6 +115,7 @@ struct BwdParams {
   __nv_bfloat16 *dk, *dv;
   float *dbias;       // [nb, H] or nullptr
   int *err;
+  int nkb;            // key tiles of the longest document (filled by the launcher)
   long long timeout_ns;
   int debug_flags;
 };
@@ -126,6 +132,9 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
 size_t bwd_smem_bytes(int head_dim, int lut_len);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device; 0 if the query fails).
+int sm_count();
 
 // Record a description of the last failing CUDA call of this thread (read by the C ABI).
 void set_last_error(const char *what, int code, const char *text);
