@@ -77,9 +77,28 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 64, 1, 1);
 };
 
+// One unit of work of the persistent backward: a 128-key tile of one (document, head).
+struct WorkItem {
+  int kb, h, seq_start, L;
+  int ks;    // first key of the tile (document-local)
+  int i0;    // first query tile walked (causal: the key tile's own)
+  int nq;    // number of query tiles walked
+  int qrot;  // walk offset
+};
+// Item ring in shared memory: the producer publishes, with the first Q/dO tile of item i,
+// which item follows it, so the P/dS warpgroups need no global loads between items.
+struct ItemSlot {
+  WorkItem next;
+  int more;
+  int pad[7];
+};
+constexpr int kItemSlots = 8;
+
 template <int D, int NS>
 size_t bwd_smem_bytes_t(int lut_len) {
-  return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 9 + 16;
+  // lut, diag (fp32), bucket ids (bytes), one table column (256 fp32), the item ring
+  return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 9 + 16 + 1024 +
+         kItemSlots * sizeof(ItemSlot);
 }
 // Three Q/dO stages when they fit next to the bias table, else two.
 int bwd_stages(int head_dim, int lut_len) {
@@ -195,14 +214,6 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
   return p0 + p1;
 }
 
-// One unit of work of the persistent backward: a 128-key tile of one (document, head).
-struct WorkItem {
-  int kb, h, seq_start, L;
-  int ks;    // first key of the tile (document-local)
-  int i0;    // first query tile walked (causal: the key tile's own)
-  int nq;    // number of query tiles walked
-  int qrot;  // walk offset
-};
 
 template <int D, int NSTAGES>
 __global__ void __launch_bounds__(640, 1)
@@ -218,15 +229,26 @@ __global__ void __launch_bounds__(640, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
 
-  // Work items: (document, head, 128-key tile), key tile fastest; CTA c takes items c,
-  // c + gridDim.x, ... (every role walks the same sequence). Items past a document's end are
-  // skipped; a corrupt cu_seqlens entry is reported and its items skipped.
-  const long long n_virtual = (long long)p.nkb * H * p.seq.num_seqs;
+  // Work items: (document, head, 128-key tile). Ranks run over groups of p.group (document,
+  // head) pairs, and within a group with the key tile slowest (when causal the first key tiles
+  // walk the most query tiles: longest first); the group size keeps the query-side tensors of
+  // the items in flight within L2. Round k of CTA c takes rank k G + c on even rounds and
+  // k G + G - 1 - c on odd ones (G CTAs), which evens out the work per CTA; every role walks
+  // the same sequence. Items past a document's end are skipped; a corrupt cu_seqlens entry is
+  // reported and its items skipped.
+  const long long n_dh = (long long)H * p.seq.num_seqs;
+  const long long n_virtual = (long long)p.nkb * n_dh;
+  const long long per_group = (long long)p.group * p.nkb;
   auto next_item = [&](long long &v, WorkItem &w) -> bool {
-    for (; v < n_virtual; v += gridDim.x) {
-      const int kb = (int)(v % p.nkb);
-      const long long rest = v / p.nkb;
-      const int h = (int)(rest % H), doc = (int)(rest / H);
+    for (;; ++v) {
+      const long long rank =
+          v * gridDim.x + ((v & 1) ? (long long)gridDim.x - 1 - blockIdx.x : (long long)blockIdx.x);
+      if (rank >= n_virtual) return false;
+      const long long grp = rank / per_group, within = rank % per_group;
+      const long long in_grp = min((long long)p.group, n_dh - grp * p.group);
+      const int kb = (int)(within / in_grp);
+      const long long dh = grp * p.group + within % in_grp;
+      const int h = (int)(dh % H), doc = (int)(dh / H);
       const int s0 = __ldg(p.seq.cu_seqlens + doc), s1 = __ldg(p.seq.cu_seqlens + doc + 1);
       if (s0 < 0 || s1 > T || s1 < s0) {
         if (tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
@@ -245,13 +267,12 @@ __global__ void __launch_bounds__(640, 1)
       w.qrot = w.nq > 0 ? kb % w.nq : 0;
       return true;
     }
-    return false;
   };
   auto qtile_start = [](const WorkItem &w, int it) {
     const int k = it + w.qrot;
     return (w.i0 + (k >= w.nq ? k - w.nq : k)) * C::BQ;
   };
-  long long v_first = blockIdx.x;
+  long long v_first = 0;  // round index
   WorkItem first;
   if (!next_item(v_first, first)) return;  // nothing to do: before any barrier or allocation
   const bool do_dbias = p.dbias != nullptr && p.bias.table != nullptr;
@@ -284,6 +305,8 @@ __global__ void __launch_bounds__(640, 1)
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
   float *diag = lut + p.bias.lut_len;
   uint8_t *lbk = reinterpret_cast<uint8_t *>(diag + p.bias.lut_len);
+  float *tcol_s = reinterpret_cast<float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15));
+  ItemSlot *slots = reinterpret_cast<ItemSlot *>(tcol_s + 256);
 
   // The producer warp sets up the barriers and starts the first item's first step (K, V, the
   // first Q/dO tile and the loads of its lse) before the rest of the block builds its tables, so
@@ -380,9 +403,20 @@ __global__ void __launch_bounds__(640, 1)
       int ii = 0, gs = 0;
       WorkItem w = first;
       do {
+        long long vnext = v + 1;
+        WorkItem wnext;
+        const bool more = next_item(vnext, wnext);
+        auto publish = [&]() {  // before the arrival on this item's first Q/dO stage
+          if (lane == 0) {
+            ItemSlot &sl = slots[ii % kItemSlots];
+            if (more) sl.next = wnext;
+            sl.more = more ? 1 : 0;
+          }
+        };
         for (int it = 0; it < w.nq; ++it) {
           const int g = gs + it, st = g % C::NS, u = g / C::NS;
           const int qs = qtile_start(w, it);
+          if (it == 0) publish();
           if (g == 0) {  // copies started with the block set-up; store its statistics, arrive
 #pragma unroll
             for (int k = 0; k < C::BQ / 32; ++k) {
@@ -447,8 +481,10 @@ __global__ void __launch_bounds__(640, 1)
         if (ii == 0) last_kv = 0;
         gs += w.nq;
         ++ii;
-        v += gridDim.x;
-      } while (ok && next_item(v, w));
+        v = vnext;
+        w = wnext;
+        if (!more) break;
+      } while (ok);
     }
     if (lane == 0) {  // teardown: every copy this thread issued has landed
       if (last_kv >= 0) mbar_wait_teardown(kv_full, last_kv & 1, kTeardownNs);
@@ -538,7 +574,7 @@ __global__ void __launch_bounds__(640, 1)
           mma_commit_e(dkdv_done);
           gs += w.nq;
           ++ii;
-          v += gridDim.x;
+          ++v;
         } while (next_item(v, w));
       } else if (warp == C::WARP_B) {
         const uint64_t dDSm = sw128_desc(smem_u32(sDS), C::DSBLK, 1024);  // dS^T, MN-major
@@ -572,7 +608,7 @@ __global__ void __launch_bounds__(640, 1)
           mma_commit_e(kv_empty);  // K is free once this item's dQ products complete
           gs += w.nq;
           ++ii;
-          v += gridDim.x;
+          ++v;
         } while (next_item(v, w));
       } else {
         const uint64_t dDSk = sw128_desc(smem_u32(sDS), 16, 1024);     // dS^T, K-major
@@ -604,7 +640,7 @@ __global__ void __launch_bounds__(640, 1)
           mma_commit_e(dkdv_done);
           gs += w.nq;
           ++ii;
-          v += gridDim.x;
+          ++v;
         } while (next_item(v, w));
       }
       const int who = warp == C::WARP_A ? 0 : (warp == C::WARP_B ? 1 : 2);
@@ -663,14 +699,15 @@ __global__ void __launch_bounds__(640, 1)
     };
 
     bool ok = true;
-    long long v = v_first;
     int ii = 0, gs = 0;
     WorkItem w = first;
+    FarBias fb = far_bias_dev(w.h, H, p.bias);
     do {
       const int krow = w.ks + r;
       const bool row_valid = krow < w.L;
-      const FarBias fb = far_bias_dev(w.h, H, p.bias);
       float acc_pos = 0.f, acc_neg = 0.f;  // table-gradient sums of far tiles, this item
+      bool new_head = false;
+      float tcol_next = 0.f, slope_next = 0.f;
       for (int it = 0; it < w.nq; ++it) {
         const int g = gs + it, st = g % C::NS;
         const int qs = qtile_start(w, it);
@@ -681,6 +718,19 @@ __global__ void __launch_bounds__(640, 1)
               __all_sync(0xffffffffu, mbar_wait(ds_empty + (g & 1), ((g >> 1) - 1) & 1, wd)));
         if (!ok) break;
         tc_fence_after();
+        if (it == 0) {
+          // The next item (published by the producer with this item's first Q/dO tile) and,
+          // when its head differs, its head's table column and slope, fetched now so that the
+          // switch between items reads shared memory only.
+          const ItemSlot &sl = slots[ii % kItemSlots];
+          const int hn = sl.next.h;
+          new_head = sl.more != 0 && hn != w.h && p.bias.has_bias;
+          if (new_head) {
+            if (has_table && tid < p.bias.nb)
+              tcol_next = __ldg(p.bias.table + (size_t)tid * H + hn);
+            if (has_slopes) slope_next = __ldg(p.bias.slopes + hn);
+          }
+        }
         const int d0 = w.ks - qs;  // delta of (key row 0, query column 0)
         const bool need_mask =
             (w.ks + 128 > w.L) || (qs + C::BQ > w.L) || (p.causal && d0 + 127 > 0);
@@ -835,10 +885,7 @@ __global__ void __launch_bounds__(640, 1)
       }
       // ---- table gradient of the item, then the next item's bias table (between two syncs
       // of the P/dS warpgroups)
-      long long vn = v + gridDim.x;
-      WorkItem wn;
-      const bool more = next_item(vn, wn);
-      const bool new_head = more && wn.h != w.h;
+      const bool more = slots[ii % kItemSlots].more != 0;
       if (do_dbias || new_head) {
         if (do_dbias) {  // far sides: one bucket each, added at the saturation deltas
           float a = acc_pos, b = acc_neg;
@@ -852,6 +899,7 @@ __global__ void __launch_bounds__(640, 1)
             if (b != 0.f) red_add_shared(diag - p.bias.sat_neg - p.bias.lut_lo, b);
           }
         }
+        if (new_head && tid < p.bias.nb) tcol_s[tid] = tcol_next;
         mbar_arrive(comp_sync);
         if (!__all_sync(0xffffffffu, mbar_wait(comp_sync, 0, wd))) { ok = false; break; }
         if (do_dbias) {
@@ -877,17 +925,26 @@ __global__ void __launch_bounds__(640, 1)
               red_add(p.dbias + (size_t)b * H + w.h, x);
           }
         }
-        if (new_head)
-          for (int i = tid; i < p.bias.lut_len; i += C::NCOMP)
-            lut[i] = bias_log2_bucket_dev(lbk[i], p.bias.lut_lo + i, wn.h, H, p.bias);
+        if (new_head) {  // same arithmetic as the set-up's table (bias_log2_bucket_dev)
+          for (int i = tid; i < p.bias.lut_len; i += C::NCOMP) {
+            const int delta = p.bias.lut_lo + i;
+            float x = 0.f;
+            if (has_table) x += tcol_s[lbk[i]];
+            if (has_slopes) x -= slope_next * (float)(delta < 0 ? -delta : delta);
+            lut[i] = x * kLog2e;
+          }
+          fb.c_pos = has_table ? tcol_s[lbk[p.bias.sat_pos - p.bias.lut_lo]] * kLog2e : 0.f;
+          fb.c_neg = has_table ? tcol_s[lbk[-p.bias.sat_neg - p.bias.lut_lo]] * kLog2e : 0.f;
+          fb.k_pos = has_slopes ? -(slope_next * kLog2e) : 0.f;
+          fb.k_neg = has_slopes ? slope_next * kLog2e : 0.f;
+        }
         mbar_arrive(comp_sync);
         if (!__all_sync(0xffffffffu, mbar_wait(comp_sync, 1, wd))) { ok = false; break; }
       }
-      gs += w.nq;
-      ++ii;
-      v = vn;
-      w = wn;
       if (!more) break;
+      gs += w.nq;
+      w = slots[ii % kItemSlots].next;
+      ++ii;
     } while (true);
     (void)ok;
     grid_dep_launch();  // the finishing grid may be scheduled
@@ -918,6 +975,9 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   // persistent grid: one CTA per SM (or per work item when there are fewer)
   BwdParams pp = p;
   pp.nkb = (max_seqlen + 127) / 128;
+  // one scheduling group: the key tile is the slowest index over all (document, head) pairs
+  // (measured faster than smaller groups, which keep fewer heads in flight)
+  pp.group = (int)std::min<long long>((long long)H * p.seq.num_seqs, 1LL << 30);
   const long long items = (long long)pp.nkb * H * p.seq.num_seqs;
   const int sms = sm_count();
   dim3 grid((unsigned)std::min<long long>(items, sms > 0 ? sms : 1));
