@@ -229,26 +229,21 @@ __global__ void __launch_bounds__(640, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
 
-  // Work items: (document, head, 128-key tile). Ranks run over groups of p.group (document,
-  // head) pairs, and within a group with the key tile slowest (when causal the first key tiles
-  // walk the most query tiles: longest first); the group size keeps the query-side tensors of
-  // the items in flight within L2. Round k of CTA c takes rank k G + c on even rounds and
-  // k G + G - 1 - c on odd ones (G CTAs), which evens out the work per CTA; every role walks
-  // the same sequence. Items past a document's end are skipped; a corrupt cu_seqlens entry is
-  // reported and its items skipped.
+  // Work items: (document, head, 128-key tile), ranked with the key tile slowest (when causal,
+  // the first key tiles walk the most query tiles: longest first). Round k of CTA c takes rank
+  // k G + c on even rounds and k G + G - 1 - c on odd ones (G CTAs), which evens out the work
+  // per CTA; every role walks the same sequence. Items past a document's end are skipped; a
+  // corrupt cu_seqlens entry is reported and its items skipped.
+  const long long n_virtual = (long long)p.nkb * H * p.seq.num_seqs;
   const long long n_dh = (long long)H * p.seq.num_seqs;
-  const long long n_virtual = (long long)p.nkb * n_dh;
-  const long long per_group = (long long)p.group * p.nkb;
   auto next_item = [&](long long &v, WorkItem &w) -> bool {
     for (;; ++v) {
       const long long rank =
           v * gridDim.x + ((v & 1) ? (long long)gridDim.x - 1 - blockIdx.x : (long long)blockIdx.x);
       if (rank >= n_virtual) return false;
-      const long long grp = rank / per_group, within = rank % per_group;
-      const long long in_grp = min((long long)p.group, n_dh - grp * p.group);
-      const int kb = (int)(within / in_grp);
-      const long long dh = grp * p.group + within % in_grp;
-      const int h = (int)(dh % H), doc = (int)(dh / H);
+      const int kb = (int)(rank / n_dh);
+      const long long rest = rank % n_dh;
+      const int h = (int)(rest % H), doc = (int)(rest / H);
       const int s0 = __ldg(p.seq.cu_seqlens + doc), s1 = __ldg(p.seq.cu_seqlens + doc + 1);
       if (s0 < 0 || s1 > T || s1 < s0) {
         if (tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
@@ -959,6 +954,573 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
+// The same backward as a plain grid of one CTA per (key tile, head, document), used for long
+// documents: each CTA walks many query tiles, so there is no set-up to hide, and the hardware
+// hands out CTAs in key-tile order (the CTAs in flight share few heads) and balances them.
+template <int D, int NSTAGES>
+__global__ void __launch_bounds__(640, 1)
+    fat_bwd_tiles_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = BwdCfg<D, NSTAGES>;
+  constexpr int QW = C::QW;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base (the 128-byte swizzle atoms need it), reached by indexing the
+  // shared array itself so every derived pointer stays a shared-memory pointer
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kb = blockIdx.x, h = blockIdx.y, doc = blockIdx.z;
+  const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  const int seq_start = __ldg(p.seq.cu_seqlens + doc);
+  const int seq_end = __ldg(p.seq.cu_seqlens + doc + 1);
+  if (seq_start < 0 || seq_end > T || seq_end < seq_start) {
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    return;
+  }
+  const int L = seq_end - seq_start;
+  const int ks = kb * 128;
+  if (ks >= L) return;
+  const int i0 = p.causal ? ks / C::BQ : 0;
+  const int nq = (L + C::BQ - 1) / C::BQ - i0;
+  // Query tiles are walked starting at a per-CTA offset, so the key-tile CTAs of one head do not
+  // all add into the same dQ rows at the same time (same-address reductions serialise in L2).
+  const int qrot = nq > 0 ? kb % nq : 0;
+  auto qtile_start = [&](int it) {
+    const int k = it + qrot;
+    return (i0 + (k >= nq ? k - nq : k)) * C::BQ;
+  };
+  const bool do_dbias = p.dbias != nullptr && p.bias.table != nullptr;
+
+  uint8_t *sK = sm + C::OFF_K, *sV = sm + C::OFF_V, *sQ = sm + C::OFF_Q, *sDO = sm + C::OFF_DO;
+  uint8_t *sDS = sm + C::OFF_DS;
+  uint8_t *sDQS = sm + C::OFF_DQS;
+  float *s_lse2 = reinterpret_cast<float *>(sm + C::OFF_STAT);
+  float *s_dvec = s_lse2 + C::NS * C::BQ;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+  uint64_t *kv_full = bars;
+  uint64_t *qd_full = kv_full + 1;       // [NS]
+  uint64_t *qd_empty = qd_full + C::NS;  // [NS]
+  uint64_t *s_full = qd_empty + C::NS;
+  uint64_t *dp_full = s_full + 1;
+  uint64_t *p_ready = dp_full + 1;
+  uint64_t *ds_ready = p_ready + 1;
+  uint64_t *ds_empty = ds_ready + 1;     // [2]
+  uint64_t *dq_full = ds_empty + 2;
+  uint64_t *dq_empty = dq_full + 1;
+  uint64_t *dkdv_done = dq_empty + 1;
+  uint64_t *mma_done = dkdv_done + 1;  // [3], one per issuer
+  uint64_t *s_consumed = mma_done + 3;  // S^T and dP^T of the tile are in registers
+  uint64_t *p_free = s_consumed + 1;    // the dV product has read P^T
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(p_free + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
+  float *diag = lut + p.bias.lut_len;
+  uint8_t *lbk = reinterpret_cast<uint8_t *>(diag + p.bias.lut_len);
+
+  // The producer warp sets up the barriers and starts its first step (K, V, the first Q/dO tile
+  // and the loads of its row statistics) before the rest of the block builds its tables, so the
+  // load latency overlaps them. The statistics are stored and announced after the block sync.
+  const bool early_q = !(p.debug_flags & 2);
+  float lv0[C::BQ / 32];
+  if (warp == 16) {
+    if (lane == 0) {
+      mbar_init(kv_full, 1);
+      for (int s = 0; s < C::NS; ++s) {
+        mbar_init(qd_full + s, 32);
+        mbar_init(qd_empty + s, 2);  // both MMA issuers release a stage
+      }
+      mbar_init(s_full, 1);
+      mbar_init(dp_full, 1);
+      mbar_init(p_ready, C::NCOMP);
+      mbar_init(ds_ready, C::NCOMP);
+      mbar_init(ds_empty, 2);  // the dQ and dK products both read dS
+      mbar_init(ds_empty + 1, 2);
+      mbar_init(dq_full, 1);
+      mbar_init(dq_empty, C::NCOMP);
+      mbar_init(dkdv_done, 2);
+      for (int i = 0; i < 3; ++i) mbar_init(mma_done + i, 1);
+      mbar_init(s_consumed, C::NCOMP);
+      mbar_init(p_free, 1);
+      *abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+    }
+    __syncwarp();
+    if (early_q) {
+      const int qs0 = qtile_start(0);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
+        for (int b = 0; b < C::DB; ++b) {
+          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, h, seq_start + ks);
+          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, h, seq_start + ks);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < C::BQ / 32; ++k) {
+        const int q = qs0 + lane + 32 * k;
+        const size_t idx = (size_t)h * T + seq_start + q;
+        lv0[k] = q < L ? __ldg(p.lse + idx) : 0.f;
+      }
+      if (lane == 0) {
+        mbar_expect_tx(qd_full, 2 * C::QTILE);  // the warp's 32 arrivals follow the block sync
+        for (int b = 0; b < C::DB; ++b) {
+          tma_load_3d(&tm_q, qd_full, sQ + b * C::QBLK, 64 * b, h, seq_start + qs0);
+          tma_load_3d(&tm_do, qd_full, sDO + b * C::QBLK, 64 * b, h, seq_start + qs0);
+        }
+      }
+    }
+  }
+  if (warp == 17) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
+    lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
+    if (do_dbias) {
+      diag[i] = 0.f;
+      lbk[i] = static_cast<uint8_t>(t5_bucket_dev(p.bias.lut_lo + i, p.bias));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // Everything above reads only inputs of the backward. D, the zeroed dQ accumulator and the
+  // zeroed table gradient come from the preprocessing grid, which this launch may overlap.
+  grid_dep_wait();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_BWD, p.timeout_ns};
+  float acc_pos = 0.f, acc_neg = 0.f;  // bias-gradient sums of far tiles (P/dS warps)
+
+  if (warp == 16) {
+    // ------------------------------------------------------------------ producer
+    int last_q[C::NS];
+#pragma unroll
+    for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
+    const bool kv_issued = early_q && lane == 0;
+    if (early_q) {
+      // step 0: copies started with the block set-up; store its statistics and arrive
+      const int qs0 = qtile_start(0);
+#pragma unroll
+      for (int k = 0; k < C::BQ / 32; ++k) {
+        const int q = qs0 + lane + 32 * k;
+        s_lse2[lane + 32 * k] = lv0[k] * kLog2e;
+        s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + (size_t)h * T + seq_start + q) : 0.f;
+      }
+      mbar_arrive(qd_full);
+      if (lane == 0) last_q[0] = 0;
+      for (int it = 1; it < nq; ++it) {
+        const int st = it % C::NS, u = it / C::NS;
+        const int qs = qtile_start(it);
+        // fetch this tile's row statistics before waiting for the stage to be free
+        float lv[C::BQ / 32], dv[C::BQ / 32];
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          const int q = qs + lane + 32 * k;
+          const size_t idx = (size_t)h * T + seq_start + q;
+          lv[k] = q < L ? __ldg(p.lse + idx) * kLog2e : 0.f;
+          dv[k] = q < L ? __ldg(p.dvec + idx) : 0.f;
+        }
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(qd_empty + st, (u - 1) & 1, wd))) break;
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          s_lse2[st * C::BQ + lane + 32 * k] = lv[k];
+          s_dvec[st * C::BQ + lane + 32 * k] = dv[k];
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qd_full + st, 2 * C::QTILE);
+          for (int b = 0; b < C::DB; ++b) {
+            tma_load_3d(&tm_q, qd_full + st, sQ + st * C::QTILE + b * C::QBLK, 64 * b, h,
+                        seq_start + qs);
+            tma_load_3d(&tm_do, qd_full + st, sDO + st * C::QTILE + b * C::QBLK, 64 * b, h,
+                        seq_start + qs);
+          }
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == st) last_q[x] = u;
+        } else {
+          mbar_arrive(qd_full + st);
+        }
+      }
+    }
+    if (lane == 0) {
+      if (kv_issued) mbar_wait_teardown(kv_full, 0, kTeardownNs);
+#pragma unroll
+      for (int x = 0; x < C::NS; ++x)
+        if (last_q[x] >= 0) mbar_wait_teardown(qd_full + x, last_q[x] & 1, kTeardownNs);
+    }
+  } else if (warp == C::WARP_A || warp == C::WARP_B || warp == C::WARP_C) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Three warps on three schedulers: A issues the products that feed and consume P (S^T,
+    // dP^T, dV), B the dQ product and C the dK product, so that no chain of hand-offs waits
+    // behind another and the issue cost is spread; each Q/dO stage is released by A and C, each
+    // dS buffer by B and C.
+    {  // the whole warp runs the loop; one elected lane issues each instruction
+      // descriptors built once; moving the start address by b bytes adds b >> 4
+      const uint64_t dKk = sw128_desc(smem_u32(sK), 16, 1024);         // K, K-major
+      const uint64_t dVk = sw128_desc(smem_u32(sV), 16, 1024);         // V, K-major
+      const uint64_t dQk = sw128_desc(smem_u32(sQ), 16, 1024);         // Q_i, K-major
+      const uint64_t dDOk = sw128_desc(smem_u32(sDO), 16, 1024);       // dO_i, K-major
+      const uint64_t dQm = sw128_desc(smem_u32(sQ), C::QBLK, 1024);    // Q_i, MN-major
+      const uint64_t dDOm = sw128_desc(smem_u32(sDO), C::QBLK, 1024);  // dO_i, MN-major
+      const uint64_t dDSk = sw128_desc(smem_u32(sDS), 16, 1024);       // dS^T, K-major
+      const uint64_t dDSm = sw128_desc(smem_u32(sDS), C::DSBLK, 1024); // dS^T, MN-major
+      const uint64_t dKm = sw128_desc(smem_u32(sK), C::KBLK, 1024);    // K, MN-major
+      auto issue_qk = [&](uint64_t a0, uint64_t b0, uint32_t dcol) {
+        // D[key][q] = sum_c A[key][c] * B[q][c]; A, B K-major
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss_e(tmem + dcol, a0 + (((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4),
+                      b0 + (((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4), C::IDESC_S, kk > 0);
+      };
+      bool ok = true;
+      if (warp == C::WARP_A) {
+        auto issue_dv = [&](int st, bool acc) {
+          // dV[key][c] += sum_q P^T[key][q] dO[q][c]; A = P^T in TMEM, B = dO MN-major
+          const uint64_t b0 = dDOm + ((st * C::QTILE) >> 4);
+#pragma unroll
+          for (int k16 = 0; k16 < C::BQ / 16; ++k16)
+            mma_bf16_ts_e(tmem + C::COL_DV, tmem + C::COL_P + 8 * k16, b0 + ((k16 * 2048) >> 4),
+                        C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
+        };
+        ok = warp_wait(kv_full, 0, wd) && warp_wait(qd_full, 0, wd);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(dKk, dQk, C::COL_S);
+          mma_commit_e(s_full);
+          issue_qk(dVk, dDOk, C::COL_DP);
+          mma_commit_e(dp_full);
+        }
+        // The next tile's S^T and dP^T as soon as this tile's have been read into registers
+        // (they run while the P/dS pass computes); dV once P^T is in TMEM.
+        for (int it = 0; ok && it < nq; ++it) {
+          const int st = it % C::NS;
+          const int stn = (it + 1) % C::NS, un = (it + 1) / C::NS;
+          if (it + 1 < nq) {
+            if (!warp_wait(s_consumed, it & 1, wd) || !warp_wait(qd_full + stn, un & 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(dKk, dQk + ((stn * C::QTILE) >> 4), C::COL_S);
+            mma_commit_e(s_full);
+            issue_qk(dVk, dDOk + ((stn * C::QTILE) >> 4), C::COL_DP);
+            mma_commit_e(dp_full);
+          }
+          if (!warp_wait(p_ready, it & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          issue_dv(st, it > 0);
+          mma_commit_e(p_free);
+          mma_commit_e(qd_empty + st);  // this issuer is done with Q_i / dO_i
+        }
+      } else {
+        auto issue_dk = [&](int buf, int st, bool acc) {
+          // dK[key][c] += sum_q dS^T[key][q] Q[q][c]; A = dS^T K-major, B = Q MN-major
+          const uint64_t a0 = dDSk + ((buf * C::DSTILE) >> 4);
+          const uint64_t b0 = dQm + ((st * C::QTILE) >> 4);
+#pragma unroll
+          for (int k16 = 0; k16 < C::BQ / 16; ++k16)
+            mma_bf16_ss_e(tmem + C::COL_DK,
+                        a0 + ((((16 * k16) >> 6) * C::DSBLK + (((16 * k16) & 63) >> 4) * 32) >> 4),
+                        b0 + ((k16 * 2048) >> 4), C::IDESC_DKV, (acc || k16 > 0) ? 1u : 0u);
+        };
+        auto issue_dq = [&](int buf) {
+          const uint64_t ds0 = dDSm + ((buf * C::DSTILE) >> 4);
+#pragma unroll
+          for (int k16 = 0; k16 < 8; ++k16) {  // 128 keys
+            if (D == 64)  // dQ[q][c] = sum_key dS[q][key] K[key][c]
+              mma_bf16_ss_e(tmem + C::COL_DQ, ds0 + ((k16 * 2048) >> 4), dKm + ((k16 * 2048) >> 4),
+                          C::IDESC_DQ, k16 > 0);
+            else          // dQ^T[c][q] = sum_key K[key][c] dS^T[key][q]
+              mma_bf16_ss_e(tmem + C::COL_DQ, dKm + ((k16 * 2048) >> 4), ds0 + ((k16 * 2048) >> 4),
+                          C::IDESC_DQ, k16 > 0);
+          }
+        };
+        if (warp == C::WARP_B) {
+          for (int it = 0; ok && it < nq; ++it) {
+            if (!warp_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+            if (it >= 1 && !warp_wait(dq_empty, (it - 1) & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_dq(it & 1);
+            mma_commit_e(dq_full);
+            mma_commit_e(ds_empty + (it & 1));
+          }
+        } else {
+          for (int it = 0; ok && it < nq; ++it) {
+            const int st = it % C::NS;
+            if (!warp_wait(ds_ready, it & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_dk(it & 1, st, it > 0);
+            mma_commit_e(ds_empty + (it & 1));
+            mma_commit_e(qd_empty + st);  // this issuer is done with Q_i
+          }
+        }
+      }
+      if (ok && warp != C::WARP_B) mma_commit_e(dkdv_done);  // the dV and dK issuers
+      const int who = warp == C::WARP_A ? 0 : (warp == C::WARP_B ? 1 : 2);
+      mma_commit_e(mma_done + who);
+      mbar_wait_teardown(mma_done + who, 0, kTeardownNs);
+    }
+  } else if (warp < 16) {
+    // ------------------------------------------------------------------ P / dS warpgroups
+    const int wg = warp >> 2;
+    const int r = tid & 127;
+    const int c0 = wg * QW;  // this warpgroup's first query column
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::COL_S + c0;
+    const uint32_t tP = tmem + lane_off + C::COL_P + c0 / 2;
+    const uint32_t tDP = tmem + lane_off + C::COL_DP + c0;
+    const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
+    const int krow = ks + r;
+    const bool row_valid = krow < L;
+    const FarBias fb = far_bias_dev(h, H, p.bias);
+    const bool has_slopes = p.bias.slopes != nullptr;
+
+    // dQ tile `it` (quarter of its 64 columns) into the fp32 accumulator
+    auto drain_dq = [&](int it) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wd))) return false;
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tDQ, v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int qs = qtile_start(it);
+      if (C::DQ_TMA) {
+        // lane = query row, columns = channels 16*wg ..: each warp stages its 32 x 16 block and
+        // lane 0 adds it with one bulk tensor reduction (no synchronisation beyond the warp).
+        uint8_t *slice = sDQS + warp * C::DQS_SLICE;
+        if (it >= 1) {  // the previous reduction of this slice has finished reading it
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(slice + lane * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dst[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        // rows past the document end carry zeros (their dS is masked), rows past T are clipped
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, slice, 16 * wg, h, seq_start + qs + 32 * (warp & 3));
+          bulk_commit_group();
+        }
+      } else {  // lane = channel, columns = query rows 16*wg ..
+        float *dst = p.dq_acc + ((size_t)(seq_start + qs + 16 * wg) * H + h) * D + r;
+        const size_t step = (size_t)H * D;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (qs + 16 * wg + j < L) red_add(dst + j * step, __uint_as_float(v[j]));
+      }
+      return true;
+    };
+
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int st = it % C::NS;
+      const int qs = qtile_start(it);
+      ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
+           __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd)) &&
+           __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
+           (it < 2 ||
+            __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
+      if (!ok) break;
+      tc_fence_after();
+      const int d0 = ks - qs;  // delta of (key row 0, query column 0)
+      const bool need_mask = (ks + 128 > L) || (qs + C::BQ > L) || (p.causal && d0 + 127 > 0);
+      const int lo_j = p.causal ? krow - qs : -1;
+      const int hi_j = row_valid ? L - qs : 0;
+      // side: 0 = lookup table, 1 = positive far side, 2 = negative far side, 3 = no bias
+      int side;
+      float rowc = 0.f, kq = 0.f;  // bias = rowc + kq * j
+      if (!p.bias.has_bias) {
+        side = 3;
+      } else if (d0 - (C::BQ - 1) >= p.bias.sat_pos) {
+        side = 1;
+        rowc = fmaf(fb.k_pos, (float)(d0 + r), fb.c_pos);
+        kq = -fb.k_pos;
+      } else if (d0 + 127 <= -p.bias.sat_neg) {
+        side = 2;
+        rowc = fmaf(fb.k_neg, (float)(d0 + r), fb.c_neg);
+        kq = -fb.k_neg;
+      } else {
+        side = 0;
+      }
+      const bool linear = has_slopes && (side == 1 || side == 2);
+      const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
+      const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
+      const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
+      // ---- one pass per 16 query columns: P^T = 2^(x - lse2) (bf16 to TMEM for the dV
+      // product), dS^T = P^T (dP^T - D) in fp32 from the same registers (bf16, swizzled, to
+      // shared memory for the dK / dQ products). Table gradient: far tiles add into one register
+      // per side; near tiles sum each 32-row block along its diagonals with warp shuffles (lane
+      // m collects deltas base + m and base + m - 32) and add two values per lane into the
+      // per-delta array.
+      {
+        const float *lut_row = lut + lut_base;
+        const float sl = p.scale_log2;
+        uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
+        const bool near_db = do_dbias && side == 0;
+        float acc_a = 0.f, acc_b = 0.f, part = 0.f;
+        // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
+        // once per tile, so no chunk carries the other forms' instructions.
+        auto pass = [&](auto bias_c, auto mask_c, auto near_c) -> bool {
+          constexpr int BIAS = decltype(bias_c)::value;
+          constexpr bool MASK = decltype(mask_c)::value;
+          constexpr bool NEAR = decltype(near_c)::value;
+#pragma unroll
+          for (int sub = 0; sub < QW / 16; ++sub) {
+            uint32_t raw[16], dp[16], pk[8];
+            tmem_ld16_issue(tS + 16 * sub, raw);
+            tmem_ld16_issue(tDP + 16 * sub, dp);
+            tmem_ld16_fence(raw);
+            tmem_ld16_fence(dp);
+            if (sub == QW / 16 - 1) {  // S^T, dP^T fully read: the next tile's may be computed
+              tc_fence_before();
+              mbar_arrive(s_consumed);
+            }
+            bwd_p_chunk<16, BIAS, MASK>(raw, pk, lse4 + 4 * sub, lut_row, c0 + 16 * sub, rowc, kq,
+                                        sl, lo_j, hi_j);
+            if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
+              if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
+              tc_fence_after();
+            }
+            tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
+            const float4 *d4 = dvs4 + 4 * sub;
+            if (sub == 0)
+              part += bwd_ds_chunk<16, NEAR, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
+            else
+              part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
+              const int j0 = c0 + 16 * sub + 8 * g;
+              const int chunk = (j0 & 63) >> 3;
+              uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4 *>(dst) =
+                  make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+          }
+          return true;
+        };
+        using B0 = std::integral_constant<int, 0>;
+        using B1 = std::integral_constant<int, 1>;
+        using B2 = std::integral_constant<int, 2>;
+        using Y = std::true_type;
+        using N = std::false_type;
+        if (side == 0) {  // lookup table
+          if (near_db)
+            ok = need_mask ? pass(B0{}, Y{}, Y{}) : pass(B0{}, N{}, Y{});
+          else
+            ok = need_mask ? pass(B0{}, Y{}, N{}) : pass(B0{}, N{}, N{});
+        } else if (!linear) {  // constant over the tile
+          ok = need_mask ? pass(B1{}, Y{}, N{}) : pass(B1{}, N{}, N{});
+        } else {  // linear in the query index
+          ok = need_mask ? pass(B2{}, Y{}, N{}) : pass(B2{}, N{}, N{});
+        }
+        if (!ok) break;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+        if (near_db) {
+          // delta of (row of lane m, column t) = base + m - t
+          const int base = d0 + 32 * (warp & 3) - c0 - p.bias.lut_lo;
+          red_add_shared(diag + base + lane, acc_a);
+          if (lane > 0) red_add_shared(diag + base + lane - 32, acc_b);
+        } else if (side == 1) {
+          acc_pos += part;
+        } else if (side == 2) {
+          acc_neg += part;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(ds_ready);
+      // ---- the previous tile's dQ (its product was issued after this tile's S^T and dP^T)
+      if (it >= 1 && !drain_dq(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && nq >= 1) ok = drain_dq(nq - 1);
+    if (C::DQ_TMA && lane == 0) bulk_wait_all();  // reductions complete before shared memory is released
+    grid_dep_launch();  // the finishing grid may be scheduled
+    // ---- dK, dV: this warpgroup's quarter of the channels
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
+    if (ok) {
+      tc_fence_after();
+      const bool valid = krow < L;
+      const int cb = wg * (D / 4);
+      __nv_bfloat16 *dkrow = p.dk + ((size_t)(seq_start + krow) * H + h) * D + cb;
+      __nv_bfloat16 *dvrow = p.dv + ((size_t)(seq_start + krow) * H + h) * D + cb;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t a[16];
+        tmem_ld16(tmem + lane_off + C::COL_DK + cb + 16 * c, a);
+        uint32_t pa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
+                              __uint_as_float(a[2 * i + 1]) * p.scale);
+        if (valid) {
+          uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 16 * c);
+          dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+        }
+        tmem_ld16(tmem + lane_off + C::COL_DV + cb + 16 * c, a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+        if (valid) {
+          uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 16 * c);
+          dv4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          dv4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 17) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (do_dbias && !*abort_flag) {
+    // Per-delta sums to per-bucket sums: each warp takes 32 consecutive deltas, runs of equal
+    // buckets are summed with a segmented scan, and each run adds once to the global gradient.
+    for (int base = warp * 32; base < p.bias.lut_len; base += C::NTHREADS) {
+      const int i = base + lane;
+      const bool in = i < p.bias.lut_len;
+      float v = in ? diag[i] : 0.f;
+      const int b = in ? static_cast<int>(lbk[i]) : -1;
+      const int b_prev = __shfl_up_sync(0xffffffffu, b, 1);
+      const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || b_prev != b);
+      const int seg = __popc(heads & (0xffffffffu >> (31 - lane)));  // run index of this lane
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float vo = __shfl_up_sync(0xffffffffu, v, off);
+        const int so = __shfl_up_sync(0xffffffffu, seg, off);
+        if (lane >= off && so == seg) v += vo;
+      }
+      const int seg_next = __shfl_down_sync(0xffffffffu, seg, 1);
+      if (in && (lane == 31 || seg_next != seg) && v != 0.f)
+        red_add(p.dbias + (size_t)b * H + h, v);
+    }
+    if (warp < 16) {  // far tiles: one bucket per side
+      float a = acc_pos, b = acc_neg;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+        b += __shfl_xor_sync(0xffffffffu, b, off);
+      }
+      if (lane == 0) {
+        if (a != 0.f) red_add(p.dbias + (size_t)t5_bucket_dev(p.bias.sat_pos, p.bias) * H + h, a);
+        if (b != 0.f) red_add(p.dbias + (size_t)t5_bucket_dev(-p.bias.sat_neg, p.bias) * H + h, b);
+      }
+    }
+  }
+}
+
 int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
                const void *v, const void *out, const void *dout, cudaStream_t stream,
                bool overlap_previous) {
@@ -972,15 +1534,15 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
     return (int)cudaErrorInvalidValue;
   const size_t smem = bwd_smem_bytes(head_dim, p.bias.lut_len);
   const int ns = bwd_stages(head_dim, p.bias.lut_len);
-  // persistent grid: one CTA per SM (or per work item when there are fewer)
+  // Short documents with d = 64: the persistent kernel (one CTA per SM walking the items, so
+  // the set-up and tail of one item overlap the next). Otherwise one CTA per key tile.
   BwdParams pp = p;
   pp.nkb = (max_seqlen + 127) / 128;
-  // one scheduling group: the key tile is the slowest index over all (document, head) pairs
-  // (measured faster than smaller groups, which keep fewer heads in flight)
-  pp.group = (int)std::min<long long>((long long)H * p.seq.num_seqs, 1LL << 30);
+  const bool persistent = head_dim == 64 && pp.nkb <= 64;
   const long long items = (long long)pp.nkb * H * p.seq.num_seqs;
   const int sms = sm_count();
-  dim3 grid((unsigned)std::min<long long>(items, sms > 0 ? sms : 1));
+  const dim3 grid = persistent ? dim3((unsigned)std::min<long long>(items, sms > 0 ? sms : 1))
+                               : dim3((unsigned)pp.nkb, H, p.seq.num_seqs);
   cudaError_t e;
   bool attr_failed = false;
   auto go = [&](auto kernel) {
@@ -1004,9 +1566,13 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
     e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, mdq, pp);
   };
   if (head_dim == 64) {
-    if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
+    if (persistent) {
+      if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
+    } else {
+      if (ns == 3) go(fat_bwd_tiles_kernel<64, 3>); else go(fat_bwd_tiles_kernel<64, 2>);
+    }
   } else {
-    if (ns == 3) go(fat_bwd_kernel<128, 3>); else go(fat_bwd_kernel<128, 2>);
+    if (ns == 3) go(fat_bwd_tiles_kernel<128, 3>); else go(fat_bwd_tiles_kernel<128, 2>);
   }
   if (attr_failed) {
     set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));

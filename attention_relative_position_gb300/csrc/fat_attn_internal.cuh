@@ -116,7 +116,6 @@ struct BwdParams {
   float *dbias;       // [nb, H] or nullptr
   int *err;
   int nkb;            // key tiles of the longest document (filled by the launcher)
-  int group;          // (document, head) pairs per scheduling group (filled by the launcher)
   long long timeout_ns;
   int debug_flags;
 };
