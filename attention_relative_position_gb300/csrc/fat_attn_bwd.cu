@@ -5,10 +5,12 @@
 //   P = exp(S' - lse), dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D = rowsum(dO * O),
 //   dK = scale * dS^T Q, dQ = scale * dS K, dTable[b, h] = sum of dS over pairs in bucket b.
 //
-// GB300 design: one CTA per (document, head, 128-key tile); it walks the query tiles of the
-// document (only those at or after the key tile when causal). Everything is computed in the
-// key-major frame (TMEM lane = key row). Five warpgroups, one warp of each per SM
-// sub-partition:
+// GB300 design: the unit of work is a (document, head, 128-key tile) item; its CTA walks the
+// query tiles of the document (only those at or after the key tile when causal). Two launch
+// shapes: fat_bwd_kernel is persistent (one CTA per SM walks several items; used for d = 64 and
+// short documents, where one item's set-up and tail overlap the next item), fat_bwd_tiles_kernel
+// has one CTA per item. Everything is computed in the key-major frame (TMEM lane = key row).
+// Five warpgroups, one warp of each per SM sub-partition:
 //   warps 0-15   four P/dS warpgroups, each owning a quarter of the query columns of a tile.
 //                One pass per 16 columns reads S^T and dP^T from TMEM (the next tile's
 //                products may then be issued), forms P^T = 2^(x - lse) (bf16 to TMEM: the A

@@ -31,6 +31,12 @@ SMALL = [
     W("alibi_bidir_d64", (260,), 4, 64, 1.0, None, True, False, 0.125, seed=19),
     W("t5dec_alibi_causal_d64", (700, 45), 2, 64, 1.0, (32, 128, False), True, True, 0.25,
       seed=20),
+    # many short documents: the persistent backward gives CTAs several items, switching heads,
+    # skipping key tiles past short documents and an empty one
+    W("t5enc_many_docs_d64", (300,) * 12 + (64,) * 6 + (0, 129), 4, 64, 1.0, (32, 128, True),
+      False, False, 0.5, seed=22),
+    W("t5dec_many_docs_causal_d64", (200,) * 16 + (1,) * 4 + (383,), 3, 64, 1.0,
+      (32, 128, False), False, True, 0.5, seed=23),
 ]
 
 
