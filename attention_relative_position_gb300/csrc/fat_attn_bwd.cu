@@ -653,6 +653,11 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tS = tmem + lane_off + C::COL_S + c0;
     const uint32_t tP = tmem + lane_off + C::COL_P + c0 / 2;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + c0;
+    // dS^T store addresses: row r of the 128-byte swizzled tile; the 16-byte group 2 sub + gg of
+    // this warpgroup's columns sits at chunk ((c0 & 63) / 8 + 2 sub + gg) ^ (r & 7) (the two
+    // terms of the sum have no bit in common)
+    const uint32_t ds_row = smem_u32(sDS) + (c0 >> 6) * C::DSBLK + r * 128;
+    const uint32_t ds_x = static_cast<uint32_t>((((c0 & 63) >> 3) ^ (r & 7)) << 4);
     const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
     const bool has_slopes = p.bias.slopes != nullptr;
     bool dq_staged = false;  // this warp has a bulk reduction in flight from its staging slice
@@ -762,7 +767,7 @@ __global__ void __launch_bounds__(640, 1)
         {
           const float *lut_row = lut + lut_base;
           const float sl = p.scale_log2;
-          uint8_t *dsb = sDS + (g & 1) * C::DSTILE;
+          const uint32_t dsb = ds_row + (g & 1) * C::DSTILE;
           const bool near_db = do_dbias && side == 0;
           float acc_a = 0.f, acc_b = 0.f, part = 0.f;
           // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
@@ -795,13 +800,9 @@ __global__ void __launch_bounds__(640, 1)
               else
                 part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
 #pragma unroll
-              for (int gg = 0; gg < 2; ++gg) {  // groups of 8 queries = 16 bytes each
-                const int j0 = c0 + 16 * sub + 8 * gg;
-                const int chunk = (j0 & 63) >> 3;
-                uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) =
-                    make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
-              }
+              for (int gg = 0; gg < 2; ++gg)  // groups of 8 queries = 16 bytes each
+                st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), pk[4 * gg], pk[4 * gg + 1],
+                             pk[4 * gg + 2], pk[4 * gg + 3]);
             }
             return true;
           };
@@ -1274,6 +1275,11 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tS = tmem + lane_off + C::COL_S + c0;
     const uint32_t tP = tmem + lane_off + C::COL_P + c0 / 2;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + c0;
+    // dS^T store addresses: row r of the 128-byte swizzled tile; the 16-byte group 2 sub + gg of
+    // this warpgroup's columns sits at chunk ((c0 & 63) / 8 + 2 sub + gg) ^ (r & 7) (the two
+    // terms of the sum have no bit in common)
+    const uint32_t ds_row = smem_u32(sDS) + (c0 >> 6) * C::DSBLK + r * 128;
+    const uint32_t ds_x = static_cast<uint32_t>((((c0 & 63) >> 3) ^ (r & 7)) << 4);
     const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
     const int krow = ks + r;
     const bool row_valid = krow < L;
@@ -1362,7 +1368,7 @@ __global__ void __launch_bounds__(640, 1)
       {
         const float *lut_row = lut + lut_base;
         const float sl = p.scale_log2;
-        uint8_t *dsb = sDS + (it & 1) * C::DSTILE;
+        const uint32_t dsb = ds_row + (it & 1) * C::DSTILE;
         const bool near_db = do_dbias && side == 0;
         float acc_a = 0.f, acc_b = 0.f, part = 0.f;
         // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
@@ -1395,13 +1401,9 @@ __global__ void __launch_bounds__(640, 1)
             else
               part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {  // groups of 8 queries = 16 bytes each
-              const int j0 = c0 + 16 * sub + 8 * g;
-              const int chunk = (j0 & 63) >> 3;
-              uint8_t *dst = dsb + (j0 >> 6) * C::DSBLK + r * 128 + ((chunk ^ (r & 7)) << 4);
-              *reinterpret_cast<uint4 *>(dst) =
-                  make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-            }
+            for (int gg = 0; gg < 2; ++gg)  // groups of 8 queries = 16 bytes each
+              st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), pk[4 * gg], pk[4 * gg + 1],
+                           pk[4 * gg + 2], pk[4 * gg + 3]);
           }
           return true;
         };
