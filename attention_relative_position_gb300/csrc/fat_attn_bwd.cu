@@ -203,10 +203,12 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
       if (NEAR) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float y = __shfl_sync(0xffffffffu, ds[e], (lane + T0 + t + e) & 31);
-          const bool lo = lane + T0 + t + e < 32;
-          acc_a += lo ? y : 0.f;
-          acc_b += lo ? 0.f : y;
+          // the source lane index is taken modulo 32 by the shuffle
+          const float y = __shfl_sync(0xffffffffu, ds[e], lane + T0 + t + e);
+          if (lane + T0 + t + e < 32)  // one predicated add per element
+            acc_a += y;
+          else
+            acc_b += y;
         }
       }
     }
