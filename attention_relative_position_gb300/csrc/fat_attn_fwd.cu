@@ -67,7 +67,7 @@ __device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], f
   for (int c = 0; c < 4; ++c) tmem_ld32_fence(x[c]);
   const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
   const uint64_t rc2 = f2_pack(rowc, rowc);
-  float mx[2] = {-INFINITY, -INFINITY};
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short dependency chains
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -89,10 +89,10 @@ __device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], f
       }
       x[c][i] = __float_as_uint(v0);
       x[c][i + 1] = __float_as_uint(v1);
-      mx[(i >> 1) & 1] = fmax3(mx[(i >> 1) & 1], v0, v1);
+      mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], v0, v1);
     }
   }
-  return fmaxf(mx[0], mx[1]);
+  return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
 }
 
 template <int D>
@@ -465,7 +465,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
         const uint64_t m2 = f2_pack(m_use, m_use);
-        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        uint64_t sum2[4];  // four short dependency chains
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sum2[k] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -478,14 +480,14 @@ __global__ void __launch_bounds__(384, 1)
             a = ex2(a);
             b = ex2(b);
             pk[i] = pack_bf16x2(a, b);
-            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a, b));
+            sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(a, b));
           }
           tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
         }
         {
           float s0, s1, s2, s3;
-          f2_unpack(sum2[0], s0, s1);
-          f2_unpack(sum2[1], s2, s3);
+          f2_unpack(f2_add(sum2[0], sum2[2]), s0, s1);
+          f2_unpack(f2_add(sum2[1], sum2[3]), s2, s3);
           l += (s0 + s1) + (s2 + s3);
         }
         tmem_st_wait();
