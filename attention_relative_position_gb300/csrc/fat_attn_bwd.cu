@@ -185,7 +185,8 @@ template <int W, bool NEAR, int T0>
 __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uint32_t (&dp)[W],
                                               const float4 *dvs4, uint32_t (&pk)[W / 2],
                                               int lane, float &acc_a, float &acc_b) {
-  uint64_t part2 = f2_pack(0.f, 0.f);
+  uint64_t part2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+  float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f};  // two short dependency chains each
 #pragma unroll
   for (int g = 0; g < W / 4; ++g) {
     const float4 d4 = dvs4[g];
@@ -196,7 +197,7 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
       const uint64_t p2 = f2_pack(__uint_as_float(pf[t]), __uint_as_float(pf[t + 1]));
       const uint64_t dp2 = f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1]));
       const uint64_t ds2 = f2_mul(p2, f2_sub(dp2, dv2[h]));
-      part2 = f2_add(part2, ds2);
+      part2[h] = f2_add(part2[h], ds2);
       float ds[2];
       f2_unpack(ds2, ds[0], ds[1]);
       pk[t / 2] = pack_bf16x2(ds[0], ds[1]);
@@ -206,15 +207,19 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
           // the source lane index is taken modulo 32 by the shuffle
           const float y = __shfl_sync(0xffffffffu, ds[e], lane + T0 + t + e);
           if (lane + T0 + t + e < 32)  // one predicated add per element
-            acc_a += y;
+            a[e] += y;
           else
-            acc_b += y;
+            b[e] += y;
         }
       }
     }
   }
+  if (NEAR) {
+    acc_a += a[0] + a[1];
+    acc_b += b[0] + b[1];
+  }
   float p0, p1;
-  f2_unpack(part2, p0, p1);
+  f2_unpack(f2_add(part2[0], part2[1]), p0, p1);
   return p0 + p1;
 }
 
