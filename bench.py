@@ -32,6 +32,23 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def max_over_ranks(x, device):
+    """The largest value of x over the ranks of the default process group (the slowest replica
+    sets the job's time); x itself without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops, world, ms):
+    """Whole-job throughput: every replica does step_flops per step of ms milliseconds."""
+    return step_flops * world / ms / 1e9
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,13 +402,9 @@ def run_ours(args, rank, world, local_rank):
     if bits:
         raise RuntimeError(f"device error word {bits}")
     mean = {k: statistics.mean(v) for k, v in per.items()}
-    step_ms = mean["step"]
-    if world > 1:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(mean["step"], device)
     f = w.fwd_flops()
-    value = 3.5 * f * world / step_ms / 1e9  # TFLOP/s
+    value = job_tflops(3.5 * f, world, step_ms)  # TFLOP/s
     kernels = {"fwd": ("fat_fwd_kernel", f, mean["fwd"], "fat_attn_fwd.cu"),
                "bwd_main": ("fat_bwd_kernel", 2.5 * f, mean["bwd_main"], "fat_attn_bwd.cu")}
     dom = max(kernels, key=lambda k: kernels[k][2])
@@ -423,11 +436,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         e_steps = max(3, min(steps, 20))
         ems, h2d, d2h = e2e_steps(w, r, e_steps)
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        line["e2e"] = {"value": round(3.5 * f * world / ems / 1e9, 3), "unit": "TFLOP/s",
+        ems = max_over_ranks(ems, device)
+        line["e2e"] = {"value": round(job_tflops(3.5 * f, world, ems), 3), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ems, 4)}
         if rank == 0 and world == 1:
