@@ -98,6 +98,9 @@ size_t fat_attn_bwd_workspace_size(const fat_shape_t *shape);
  * (zeroed by the library, then accumulated with fp32 atomics: bit-exact bucket assignment,
  * order-dependent rounding). ALiBi slopes receive no gradient. workspace must hold
  * fat_attn_bwd_workspace_size(shape) bytes; its contents need not be initialised.
+ * It enqueues the three stages below; the second and third are launched as programmatic
+ * dependents of the grid before them (each is scheduled while that grid drains and waits for
+ * its outputs inside the kernel), which the stage-by-stage calls do not do.
  */
 int fat_attn_bwd(const fat_shape_t *shape, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
