@@ -254,28 +254,50 @@ def time_steps(r, steps, flush=True):
     return per
 
 
+def _packed(tensors, device, pin=False):
+    """One flat byte buffer holding the given tensors (256-byte aligned) and views into it with
+    the tensors' shapes and dtypes, so that a whole set moves with one copy."""
+    import torch
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    flat = torch.empty(max(total, 1), dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [flat[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for o, t in zip(offs, tensors)]
+    return flat, views
+
+
 def e2e_steps(w, r, steps, nbuf=2):
     """Same metric through the public API from pinned host buffers: every step copies its
     inputs host->device, runs forward + backward, and copies out, dq, dk, dv (and the table
     gradient) back to host. Steps are pipelined as a training loop would run them: `nbuf` sets
     of device buffers and three streams, so the inputs of step i+1 are copied in and the results
-    of step i-1 copied out while step i computes. The timed region runs from the first step's
-    first input copy to the last step's last result copy."""
+    of step i-1 copied out while step i computes; each direction moves one packed buffer per
+    step. The timed region runs from the first step's input copy to the last step's result
+    copy."""
     torch, fa = r.torch, r.fa
     x = r.x
     names_in = [n for n in ("q", "k", "v", "dout", "cu_seqlens", "table", "slopes")
                 if x[n] is not None]
-    host_in = {n: x[n].cpu().pin_memory() for n in names_in}
-    dev_in = [{n: torch.empty_like(x[n]) for n in names_in} for _ in range(nbuf)]
+    host_in_flat, host_in_views = _packed([x[n] for n in names_in], "cpu", pin=True)
+    for v_, n in zip(host_in_views, names_in):
+        v_.copy_(x[n].cpu())
+    dev_in = []
+    for _ in range(nbuf):
+        flat, views = _packed([x[n] for n in names_in], x["q"].device)
+        dev_in.append((flat, dict(zip(names_in, views))))
     out_names = ["out", "dq", "dk", "dv"] + (["dtab"] if r.dtab is not None else [])
     like = {"out": r.out, "dq": r.dq, "dk": r.dk, "dv": r.dv, "dtab": r.dtab}
-    dev_out = [{n: torch.empty_like(like[n]) for n in out_names} for _ in range(nbuf)]
+    dev_out = []
+    for _ in range(nbuf):
+        flat, views = _packed([like[n] for n in out_names], x["q"].device)
+        dev_out.append((flat, dict(zip(out_names, views))))
+    host_out = [_packed([like[n] for n in out_names], "cpu", pin=True)[0] for _ in range(nbuf)]
     lse = [torch.empty_like(r.lse) for _ in range(nbuf)]
     ws = [torch.empty_like(r.ws) for _ in range(nbuf)]
-    host_out = [{n: torch.empty(like[n].shape, dtype=like[n].dtype, pin_memory=True)
-                 for n in out_names} for _ in range(nbuf)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    h2d = sum(x[n].numel() * x[n].element_size() for n in names_in)
+    d2h = sum(like[n].numel() * like[n].element_size() for n in out_names)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     s_cmp = r.stream
     ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # inputs of the buffer set copied in
@@ -285,12 +307,11 @@ def e2e_steps(w, r, steps, nbuf=2):
 
     def one(i):
         b = i % nbuf
-        din, dout_ = dev_in[b], dev_out[b]
+        (in_flat, din), (out_flat, dout_) = dev_in[b], dev_out[b]
         with torch.cuda.stream(s_in):
             if i >= nbuf:
                 s_in.wait_event(ev_cmp[b])
-            for n in names_in:
-                din[n].copy_(host_in[n], non_blocking=True)
+            in_flat.copy_(host_in_flat, non_blocking=True)
             ev_in[b].record(s_in)
         s_cmp.wait_event(ev_in[b])
         if i >= nbuf:
@@ -306,8 +327,7 @@ def e2e_steps(w, r, steps, nbuf=2):
         ev_cmp[b].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_cmp[b])
-            for n in out_names:
-                host_out[b][n].copy_(dout_[n], non_blocking=True)
+            host_out[b].copy_(out_flat, non_blocking=True)
             ev_out[b].record(s_out)
 
     for i in range(2 * nbuf):
@@ -466,7 +486,8 @@ def run_ours(args, rank, world, local_rank):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ems, 4),
                        "pipelining": "2 buffer sets: step i+1 copied in and step i-1 copied "
-                                     "out while step i computes"}
+                                     "out while step i computes; one packed copy per "
+                                     "direction per step"}
         if rank == 0 and world == 1:
             from attention_relative_position_gb300 import workloads as wl
             others = {}
