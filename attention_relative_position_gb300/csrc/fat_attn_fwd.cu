@@ -16,8 +16,11 @@
 //               lane i), so row max/sum need no shuffles. Bias: closed form on tiles that lie
 //               beyond the T5 saturation distance, a per-CTA lookup table over delta on the rest.
 //               The running max is only raised (and O rescaled in TMEM) when it grows by more
-//               than 2^8, which keeps P <= 256 and leaves the final result exact.
-// While one warpgroup computes its softmax, the tensor cores run the other tile's MMAs.
+//               than 2^32, which keeps P <= 2^32 and leaves the final result exact.
+// While one warpgroup computes its softmax, the tensor cores run the other tile's MMAs. With
+// d = 64 the two warpgroups take their exponential phases in turns (tile 0 of key tile j, then
+// tile 1 of key tile j, then tile 0 of key tile j + 1, ...): each finds the special-function
+// units to itself, and the other's logits and waits overlap it.
 #include <cstdio>
 
 #include "fat_attn_internal.cuh"
@@ -35,6 +38,7 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
   static constexpr int OFF_LUT = OFF_BAR + 256;
+  static_assert((1 + 4 * NS + 12) * 8 + 8 <= 256, "barrier block");
   static constexpr int NTHREADS = 384;
   // TMEM columns: S_t at 128 t, O_t at 256 + O_STRIDE t. With d = 64 the O_t take 64 columns
   // each and P_t (bf16 pairs) gets its own 64 columns at 384 + 64 t, so S_t of the next key tile
@@ -136,7 +140,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t *o_ready = p_ready + 2;
   uint64_t *s_free = o_ready + 2;  // S_t has been read into registers (separate-P layout)
   uint64_t *mma_done = s_free + 2;  // [2], one per issuer
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
+  uint64_t *turn = mma_done + 2;  // [2]: the exponential phase of warpgroup t may start
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(turn + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
 
@@ -159,6 +164,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(mma_done, 1);
     mbar_init(mma_done + 1, 1);
+    mbar_init(turn, 4);  // one arrival per warp of the other warpgroup
+    mbar_init(turn + 1, 4);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -381,6 +388,7 @@ __global__ void __launch_bounds__(384, 1)
     const int t = warp >> 2;
     if (t < ntile) {
       const int nk = t == 0 ? nkv0 : nkv1;
+      const int nk_other = t == 0 ? nkv1 : nkv0;
       const int r = tid & 127;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tS = tmem + lane_off + C::COL_S0 + 128 * t;
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(384, 1)
         if (j == 0) {
           m = mx;
         } else {
-          const bool need = mx > m + 8.0f;
+          const bool need = mx > m + 32.0f;
           if (C::SEP_P) {  // P_t and O_t are still read by PV_{j-1}
             ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (j - 1) & 1, wd));
             if (!ok) break;
@@ -463,6 +471,14 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
+        // turn order (d = 64, two tiles): tile 0 waits for tile 1's exponentials of the previous
+        // key tile, tile 1 for tile 0's of this one. Only the order of work depends on it, so the
+        // wait gives up quietly after a bounded time.
+        const bool turns = C::SEP_P && ntile == 2;
+        if (turns && (t == 0 ? (j >= 1 && j - 1 < nk_other) : (j < nk_other))) {
+          (void)mbar_wait_hint(turn + t, static_cast<uint32_t>((t == 0 ? j - 1 : j) & 1), kTurnNs);
+          __syncwarp();
+        }
         const float m_use = (m == -INFINITY) ? 0.f : m;
         const uint64_t m2 = f2_pack(m_use, m_use);
         uint64_t sum2[4];  // four short dependency chains
@@ -484,6 +500,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
         }
+        if (turns && lane == 0) mbar_arrive(turn + (1 - t));
         {
           float s0, s1, s2, s3;
           f2_unpack(f2_add(sum2[0], sum2[2]), s0, s1);

@@ -17,6 +17,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSmemLimit = 232448;           // 227 KB of dynamic shared memory per block
 constexpr long long kDefaultTimeoutNs = 4000000000LL;
 constexpr long long kTeardownNs = 200000000LL;
+constexpr long long kTurnNs = 20000LL;  // bound of a wait that only orders work
 
 // How the additive bias of relative position delta = k - q is formed.
 //   T5 part: table[bucket(delta), h]; the bucket is a pure integer function of delta: exact

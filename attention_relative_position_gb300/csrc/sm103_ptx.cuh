@@ -115,6 +115,17 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parit
   return true;
 }
 
+// Wait on a barrier that only orders work (no data depends on it): gives up silently after
+// limit_ns, and the caller goes on either way.
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity, long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA (tensor copies global -> shared, completion counted on an mbarrier)
 // ---------------------------------------------------------------------------------------------
