@@ -127,6 +127,12 @@ __global__ void __launch_bounds__(384, 1)
   const int nkv0 = p.causal ? min((q0 >> 7) + 1, nkv_all) : nkv_all;
   const int nkv1 = ntile == 2 ? (p.causal ? min((q0 >> 7) + 2, nkv_all) : nkv_all) : 0;
   const int nkv_max = max(nkv0, nkv1);
+  // Causal rows take their key tiles from the diagonal backwards: the first tile holds each
+  // row's largest ALiBi bias, so the running max rarely grows afterwards. Stream position j
+  // (the order of the K/V ring) holds key tile kt0 + kdir * j; Q tile t uses positions
+  // [jbeg_t, jbeg_t + nkv_t).
+  const int kt0 = p.causal ? nkv_max - 1 : 0, kdir = p.causal ? -1 : 1;
+  const int jbeg0 = p.causal ? nkv_max - nkv0 : 0, jbeg1 = p.causal ? nkv_max - nkv1 : 0;
 
   uint8_t *sQ = sm + C::OFF_Q, *sK = sm + C::OFF_K, *sV = sm + C::OFF_V;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
@@ -179,10 +185,10 @@ __global__ void __launch_bounds__(384, 1)
                       seq_start + q0 + 128 * t);
       mbar_arrive_expect_tx(k_full, C::TILE);
       for (int b = 0; b < C::DB; ++b)
-        tma_load_3d(&tm_k, k_full, sK + b * C::BLK, 64 * b, h, seq_start);
+        tma_load_3d(&tm_k, k_full, sK + b * C::BLK, 64 * b, h, seq_start + 128 * kt0);
       mbar_arrive_expect_tx(v_full, C::TILE);
       for (int b = 0; b < C::DB; ++b)
-        tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, h, seq_start);
+        tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, h, seq_start + 128 * kt0);
     }
   }
   if (warp == 9) {
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(k_full + s, C::TILE);
           for (int b = 0; b < C::DB; ++b)
             tma_load_3d(&tm_k, k_full + s, sK + s * C::TILE + b * C::BLK, 64 * b, h,
-                        seq_start + 128 * j);
+                        seq_start + 128 * (kt0 + kdir * j));
 #pragma unroll
           for (int x = 0; x < C::NS; ++x)
             if (x == s) last_k[x] = u;
@@ -222,7 +228,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(v_full + s, C::TILE);
           for (int b = 0; b < C::DB; ++b)
             tma_load_3d(&tm_v, v_full + s, sV + s * C::TILE + b * C::BLK, 64 * b, h,
-                        seq_start + 128 * j);
+                        seq_start + 128 * (kt0 + kdir * j));
 #pragma unroll
           for (int x = 0; x < C::NS; ++x)
             if (x == s) last_v[x] = u;
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(384, 1)
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < ntile; ++t) {
+          if ((t == 0 ? jbeg0 : jbeg1) > 0) continue;  // this tile starts further down the stream
           issue_S(t, 0);
           mma_commit(s_full + t);
         }
@@ -276,16 +283,18 @@ __global__ void __launch_bounds__(384, 1)
         }
         bool k_next = false;
         for (int t = 0; t < ntile && ok; ++t) {
-          const int nk = t == 0 ? nkv0 : nkv1;
-          if (j >= nk) continue;
-          if (!mbar_wait(p_ready + t, j & 1, wd)) {
-            ok = false;
-            break;
+          const int jb = t == 0 ? jbeg0 : jbeg1, je = jb + (t == 0 ? nkv0 : nkv1);
+          if (j >= jb && j < je) {
+            const int jl = j - jb;  // this tile's own step count
+            if (!mbar_wait(p_ready + t, jl & 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_PV(t, s, jl > 0);
+            mma_commit(o_ready + t);
           }
-          tc_fence_after();
-          issue_PV(t, s, j > 0);
-          mma_commit(o_ready + t);
-          if (jn < nk) {
+          if (jn >= jb && jn < je) {
             if (!k_next) {
               if (!mbar_wait(k_full + sn, un & 1, wd)) {
                 ok = false;
@@ -334,19 +343,31 @@ __global__ void __launch_bounds__(384, 1)
           mma_bf16_ts(dO_t, aP_t + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_PV,
                       (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(q_full, 0, wd) && mbar_wait(k_full, 0, wd);
+      const int jb = t == 0 ? jbeg0 : jbeg1, je = jb + nk;
+      bool ok = true;
+      // stream positions before this tile's first one: release them once loaded, in order
+      for (int j = 0; ok && j < jb; ++j) {
+        const int s = j % C::NS, u = j / C::NS;
+        if (!mbar_wait(k_full + s, u & 1, wd)) { ok = false; break; }
+        mbar_arrive(k_empty + s);
+        if (!mbar_wait(v_full + s, u & 1, wd)) { ok = false; break; }
+        mbar_arrive(v_empty + s);
+      }
+      ok = ok && mbar_wait(q_full, 0, wd) &&
+           mbar_wait(k_full + jb % C::NS, static_cast<uint32_t>((jb / C::NS) & 1), wd);
       if (ok) {
         tc_fence_after();
-        issue_S(0);
+        issue_S(jb % C::NS);
         mma_commit(s_full + t);
-        mma_commit(k_empty);
+        mma_commit(k_empty + jb % C::NS);
       }
-      for (int j = 0; ok && j < nk; ++j) {
+      for (int j = jb; ok && j < je; ++j) {
+        const int jl = j - jb;  // this tile's own step count
         const int s = j % C::NS, u = j / C::NS;
         const int jn = j + 1, sn = jn % C::NS, un = jn / C::NS;
         if (C::SEP_P) {  // next key tile's S_t as soon as the softmax has read S_t
-          if (!mbar_wait(s_free + t, j & 1, wd)) { ok = false; break; }
-          if (jn < nk) {
+          if (!mbar_wait(s_free + t, jl & 1, wd)) { ok = false; break; }
+          if (jn < je) {
             if (!mbar_wait(k_full + sn, un & 1, wd)) { ok = false; break; }
             tc_fence_after();
             issue_S(sn);
@@ -354,15 +375,15 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(k_empty + sn);
           }
         }
-        if (!mbar_wait(v_full + s, u & 1, wd) || !mbar_wait(p_ready + t, j & 1, wd)) {
+        if (!mbar_wait(v_full + s, u & 1, wd) || !mbar_wait(p_ready + t, jl & 1, wd)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_PV(s, j > 0);
+        issue_PV(s, jl > 0);
         mma_commit(o_ready + t);
         mma_commit(v_empty + s);
-        if (!C::SEP_P && jn < nk) {  // S_t is overwritten only after P_t V is issued
+        if (!C::SEP_P && jn < je) {  // S_t is overwritten only after P_t V is issued
           if (!mbar_wait(k_full + sn, un & 1, wd)) { ok = false; break; }
           tc_fence_after();
           issue_S(sn);
@@ -372,7 +393,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       // key tiles this Q tile does not need (causal): release them once they have been loaded,
       // in order, so each release lands in the phase of its stage
-      for (int j = nk; ok && j < nkv_max; ++j) {
+      for (int j = je; ok && j < nkv_max; ++j) {
         const int s = j % C::NS, u = j / C::NS;
         if (!mbar_wait(k_full + s, u & 1, wd)) { ok = false; break; }
         mbar_arrive(k_empty + s);
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(s_full + t, j & 1, wd));
         if (!ok) break;
         tc_fence_after();
-        const int ks = 128 * j;
+        const int ks = 128 * (kt0 + kdir * ((t == 0 ? jbeg0 : jbeg1) + j));
         const int d0 = ks - qs;  // delta of (row 0, key 0) of the tile
         const bool need_mask = (ks + 128 > L) || (p.causal && d0 + 127 > 0);
         const int lim = min(L - ks, p.causal ? (qrow - ks + 1) : 128);
