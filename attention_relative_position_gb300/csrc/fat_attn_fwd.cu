@@ -57,14 +57,15 @@ size_t fwd_smem_bytes(int head_dim, int lut_len) {
 }
 
 // Load the S row from TMEM (all four 32-column loads in flight), form
-// x = S * scale_log2 + bias (log2 units) two columns per packed fp32x2 instruction, apply the
-// mask, and return the row maximum.
-//   MODE 0: bias = rowc (constant over the tile)
-//   MODE 1: bias = rowc + kk * j (linear in the key index)
-//   MODE 2: bias = lut_row[j]
-template <int MODE, bool MASK>
+// x = S * scale_log2 + bias - m_ref (log2 units, m_ref the row's current reference max) two
+// columns per packed fp32x2 instruction, apply the mask, and return the row maximum of x.
+//   MODE 0: bias - m_ref = rowc (constant over the tile; the caller folds m_ref in)
+//   MODE 1: bias - m_ref = rowc + kk * j (linear in the key index; likewise)
+//   MODE 2: bias = lut_row[j], and nm2 holds -m_ref twice (FOLD; else m_ref is 0)
+template <int MODE, bool MASK, bool FOLD>
 __device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], float scale_log2,
-                                            float rowc, float kk, const float *lut_row, int lim) {
+                                            float rowc, float kk, const float *lut_row, int lim,
+                                            uint64_t nm2) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) tmem_ld32_issue(tS + c * 32, x[c]);
 #pragma unroll
@@ -83,7 +84,8 @@ __device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], f
       else if (MODE == 1)
         b2 = f2_pack(fmaf(kk, (float)j, rowc), fmaf(kk, (float)(j + 1), rowc));
       else
-        b2 = f2_pack(lut_row[j], lut_row[j + 1]);
+        b2 = FOLD ? f2_add(f2_pack(lut_row[j], lut_row[j + 1]), nm2)
+                  : f2_pack(lut_row[j], lut_row[j + 1]);
       float v0, v1;
       f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c][i]), __uint_as_float(x[c][i + 1])), sl2, b2),
                 v0, v1);
@@ -97,6 +99,28 @@ __device__ __forceinline__ float fwd_logits(uint32_t tS, uint32_t (&x)[4][32], f
     }
   }
   return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+}
+
+// P = 2^(x - sub) for one row of 128 columns (x already relative to the row's reference max;
+// sub is nonzero only when that reference has just moved), packed to bf16 pairs into TMEM,
+// with the fp32 sum of the row accumulated in four short dependency chains.
+template <bool SUB>
+__device__ __forceinline__ void fwd_exp_pass(const uint32_t (&x)[4][32], uint64_t sub2,
+                                             uint32_t tP, uint64_t (&sum2)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float a = __uint_as_float(x[c][2 * i]), b = __uint_as_float(x[c][2 * i + 1]);
+      if (SUB) f2_unpack(f2_sub(f2_pack(a, b), sub2), a, b);
+      a = ex2(a);
+      b = ex2(b);
+      pk[i] = pack_bf16x2(a, b);
+      sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(a, b));
+    }
+    tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
+  }
 }
 
 template <int D>
@@ -445,26 +469,36 @@ __global__ void __launch_bounds__(384, 1)
           mode = 2;
         }
         const float *lut_row = lut + (d0 - r - p.bias.lut_lo);
+        // d = 128: logits relative to the row's current max, so that the exponentials need no
+        // subtraction unless the max moves (with d = 64 the extra registers cost more than the
+        // subtraction saves)
+        constexpr bool FOLD = !C::SEP_P;
+        const float m_ref = (FOLD && m != -INFINITY) ? m : 0.f;
+        rowc -= m_ref;
+        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
         uint32_t x[4][32];
-        float mx;
+        float mx;  // row max of x (relative to m_ref)
+#define FAT_LOGITS(MODE, MASK) \
+  fwd_logits<MODE, MASK, FOLD>(tS, x, p.scale_log2, rowc, kk, lut_row, lim, nm2)
         if (mode == 0)
-          mx = need_mask ? fwd_logits<0, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
-                         : fwd_logits<0, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+          mx = need_mask ? FAT_LOGITS(0, true) : FAT_LOGITS(0, false);
         else if (mode == 1)
-          mx = need_mask ? fwd_logits<1, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
-                         : fwd_logits<1, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+          mx = need_mask ? FAT_LOGITS(1, true) : FAT_LOGITS(1, false);
         else
-          mx = need_mask ? fwd_logits<2, true>(tS, x, p.scale_log2, rowc, kk, lut_row, lim)
-                         : fwd_logits<2, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim);
+          mx = need_mask ? FAT_LOGITS(2, true) : FAT_LOGITS(2, false);
+#undef FAT_LOGITS
 
         if (C::SEP_P) {  // S_t is in registers: the next S_t may be computed
           tc_fence_before();
           mbar_arrive(s_free + t);
         }
-        if (j == 0) {
+        float sub = 0.f;  // what the exponentials still subtract from x (FOLD)
+        if (j == 0) {      // m_ref was 0
           m = mx;
+          sub = (mx == -INFINITY) ? 0.f : mx;
         } else {
-          const bool need = mx > m + 32.0f;
+          const bool fresh = m == -INFINITY;  // no key of this row so far
+          const bool need = fresh ? (mx != -INFINITY) : (mx > (FOLD ? 0.f : m) + 32.0f);
           if (C::SEP_P) {  // P_t and O_t are still read by PV_{j-1}
             ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (j - 1) & 1, wd));
             if (!ok) break;
@@ -477,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            const float f = need ? ex2(m - mx) : 1.0f;
+            const float f = need ? (fresh ? 0.f : ex2(FOLD ? -mx : m - mx)) : 1.0f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -488,7 +522,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (need) {
               l *= f;
-              m = mx;
+              m = (fresh || !FOLD) ? mx : m + mx;
+              sub = mx;
             }
           }
         }
@@ -500,26 +535,16 @@ __global__ void __launch_bounds__(384, 1)
           (void)mbar_wait_hint(turn + t, static_cast<uint32_t>((t == 0 ? j - 1 : j) & 1), kTurnNs);
           __syncwarp();
         }
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        const uint64_t m2 = f2_pack(m_use, m_use);
         uint64_t sum2[4];  // four short dependency chains
 #pragma unroll
         for (int k = 0; k < 4; ++k) sum2[k] = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float a, b;
-            f2_unpack(f2_sub(f2_pack(__uint_as_float(x[c][2 * i]), __uint_as_float(x[c][2 * i + 1])),
-                             m2),
-                      a, b);
-            a = ex2(a);
-            b = ex2(b);
-            pk[i] = pack_bf16x2(a, b);
-            sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(a, b));
-          }
-          tmem_st16(tP + c * 16, pk);  // P (bf16 pairs): own columns (d 64) or over S (d 128)
+        if (!FOLD) {  // x is absolute: subtract the row max
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          fwd_exp_pass<true>(x, f2_pack(m_use, m_use), tP, sum2);
+        } else if (__any_sync(0xffffffffu, sub != 0.f)) {
+          fwd_exp_pass<true>(x, f2_pack(sub, sub), tP, sum2);
+        } else {
+          fwd_exp_pass<false>(x, 0, tP, sum2);
         }
         if (turns && lane == 0) mbar_arrive(turn + (1 - t));
         {
