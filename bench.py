@@ -394,6 +394,35 @@ def cpu_baseline(w, seconds=10.0):
             "seconds": dt}
 
 
+def hbm_bytes(w):
+    """Algorithmic HBM bytes of one launch of each kernel: the forward reads Q, K, V (and the
+    table) and writes O and lse; the backward preprocess reads O and dO, writes D and zeroes the
+    fp32 dQ accumulator (and the table gradient); the finish reads that accumulator and writes
+    dq in bf16."""
+    T, H, d = w.total_tokens, w.num_heads, w.head_dim
+    x = T * H * d
+    tab = w.t5[0] * H * 4 if w.t5 else 0
+    return {"fwd": 3 * x * 2 + tab + x * 2 + T * H * 4,
+            "bwd_pre": 2 * x * 2 + T * H * 4 + x * 4 + tab,
+            "bwd_fin": x * 4 + x * 2}
+
+
+def hbm_figures(w, per, peak_gbs):
+    """GB/s of the memory-bound kernels (algorithmic bytes / mean CUDA-event time) and their
+    fraction of the measured copy bandwidth; the forward's figure matters for short sequences,
+    where it is latency-bound rather than tensor-bound."""
+    b = hbm_bytes(w)
+    res = {}
+    for k in ("fwd", "bwd_pre", "bwd_fin"):
+        ms = statistics.mean(per[k])
+        gbs = b[k] / ms / 1e6
+        res[k + "_us"] = round(ms * 1e3, 2)
+        res[k + "_gbs"] = round(gbs, 1)
+        res[k + "_gbs_frac"] = round(gbs / peak_gbs, 4)
+    res["peak_gbs"] = peak_gbs
+    return res
+
+
 def quick_other(w, device, peaks, steps=10):
     r = Runner(w, device)
     for _ in range(3):
@@ -408,6 +437,7 @@ def quick_other(w, device, peaks, steps=10):
     res.update({k + "_frac": v / peaks["bf16_tflops"] for k, v in list(res.items())})
     res = {k: round(v, 4) for k, v in res.items()}
     res["ms_per_step"] = round(step_ms, 4)
+    res["hbm"] = hbm_figures(w, per, peaks["hbm_gbs"])
     del r
     return res
 
@@ -473,6 +503,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} bf16 dense (burst; kernel timed alone)",
                      "traffic": traffic_for(f"{kname}<{w.head_dim}>@{w.name}"),
                      "algorithmic_flops_per_launch": kflops},
+        "hbm": hbm_figures(w, per, peaks["hbm_gbs"]),
         "gpu_launches": steps * Runner.LAUNCHES_PER_STEP,
         "timed_wall_s": round(wall, 4),
     }
@@ -491,10 +522,13 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0 and world == 1:
             from attention_relative_position_gb300 import workloads as wl
             others = {}
-            for idx in (2, 3, 4):
+            for idx in (0, 2, 3, 4):
                 ow = wl.WORKLOADS[idx]
                 if ow.name != w.name:
-                    others[ow.name] = quick_other(ow, device, peaks)
+                    try:
+                        others[ow.name] = quick_other(ow, device, peaks)
+                    except Exception as e:  # one side measurement must not cost the line
+                        others[ow.name] = {"error": f"{type(e).__name__}: {e}"[:200]}
             line["other_workloads"] = others
             line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
