@@ -20,19 +20,20 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "oracle_xattn.c")]
+_HDRS = [os.path.join(_HERE, "oracle.h"), os.path.join(_HERE, "oracle_xattn.h")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
+    """Compile oracle.c and oracle_xattn.c into liboracle.so next to them (gcc, -O2, OpenMP)."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
-                                                   os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS + _HDRS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall",
-           _SRC, "-o", tmp, "-lm"]
+           *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -59,6 +60,29 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _XProblem(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int),
+        ("total_q", ctypes.c_int),
+        ("total_k", ctypes.c_int),
+        ("num_heads_q", ctypes.c_int),
+        ("num_heads_kv", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("bias_table", ctypes.c_void_p),
+        ("num_buckets", ctypes.c_int),
+        ("max_distance", ctypes.c_int),
+        ("bidirectional", ctypes.c_int),
+        ("alibi_slopes", ctypes.c_void_p),
+        ("causal", ctypes.c_int),
+        ("softmax_scale", ctypes.c_double),
+    ]
+
+
 def _load():
     global _lib
     if _lib is None:
@@ -74,8 +98,12 @@ def _load():
         lib.oracle_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp]
         lib.oracle_attn_fwd_rows.argtypes = [P, i, i, vp, i, vp, vp]
         lib.oracle_attn_bwd_rows.argtypes = [P, vp, i, i, vp, i, vp, i, vp, vp, vp, vp]
+        XP = ctypes.POINTER(_XProblem)
+        lib.oracle_xattn_fwd.argtypes = [XP, vp, vp]
+        lib.oracle_xattn_bwd.argtypes = [XP, vp, vp, vp, vp, vp]
         for f in ("oracle_attn_fwd", "oracle_attn_bwd", "oracle_attn_fwd_rows",
-                  "oracle_attn_bwd_rows", "oracle_num_threads"):
+                  "oracle_attn_bwd_rows", "oracle_num_threads", "oracle_xattn_fwd",
+                  "oracle_xattn_bwd"):
             getattr(lib, f).restype = i
         _lib = lib
     return _lib
@@ -210,3 +238,83 @@ def attn_bwd_rows(pb: Problem, dout: np.ndarray, doc: int, head: int, qrows: Seq
         krows.ctypes.data, len(krows), dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
         dcol.ctypes.data if dcol is not None else None), "bwd_rows")
     return dq, dk, dv, dcol
+
+
+# ---- generalised problem: own query and key lengths, grouped-query heads, bottom-right causal ----
+@dataclass
+class XProblem:
+    """Per document a query sequence and a key/value sequence of their own lengths.
+
+    q: [total_q, Hq, d]; k, v: [total_k, Hkv, d] (Hq a multiple of Hkv; query head h reads
+    key/value head h // (Hq // Hkv)); cu_seqlens_q / cu_seqlens_k: int32 [n + 1]. Causal masking
+    is aligned at the bottom right (query p of a document sees keys r <= p + Lk - Lq), and the
+    relative position of the bias is r - (p + Lk - Lq). Stored widened to fp64.
+    """
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_k: np.ndarray
+    table: Optional[np.ndarray] = None
+    num_buckets: int = 0
+    max_distance: int = 0
+    bidirectional: bool = True
+    slopes: Optional[np.ndarray] = None
+    causal: bool = False
+    scale: float = 1.0
+
+    def __post_init__(self):
+        self.q, self.k, self.v = widen(self.q), widen(self.k), widen(self.v)
+        self.cu_seqlens_q = np.ascontiguousarray(self.cu_seqlens_q, dtype=np.int32)
+        self.cu_seqlens_k = np.ascontiguousarray(self.cu_seqlens_k, dtype=np.int32)
+        if self.table is not None:
+            self.table = widen(self.table)
+        if self.slopes is not None:
+            self.slopes = widen(self.slopes)
+
+    def _c(self) -> _XProblem:
+        p = _XProblem()
+        p.num_seqs = len(self.cu_seqlens_q) - 1
+        p.total_q, p.num_heads_q, p.head_dim = self.q.shape
+        p.total_k, p.num_heads_kv = self.k.shape[0], self.k.shape[1]
+        p.cu_seqlens_q = self.cu_seqlens_q.ctypes.data
+        p.cu_seqlens_k = self.cu_seqlens_k.ctypes.data
+        p.q, p.k, p.v = self.q.ctypes.data, self.k.ctypes.data, self.v.ctypes.data
+        p.bias_table = self.table.ctypes.data if self.table is not None else None
+        p.num_buckets, p.max_distance = int(self.num_buckets), int(self.max_distance)
+        p.bidirectional = int(bool(self.bidirectional))
+        p.alibi_slopes = self.slopes.ctypes.data if self.slopes is not None else None
+        p.causal = int(bool(self.causal))
+        p.softmax_scale = float(self.scale)
+        return p
+
+
+def xattn_fwd(pb: XProblem):
+    """Returns (out fp64 [total_q, Hq, d], lse fp64 [Hq, total_q])."""
+    if len(pb.cu_seqlens_k) != len(pb.cu_seqlens_q) or pb.k.shape != pb.v.shape:
+        raise ValueError("oracle xattn_fwd: mismatched problem")
+    Tq, Hq, d = pb.q.shape
+    out = np.zeros((Tq, Hq, d))
+    lse = np.zeros((Hq, Tq))
+    c = pb._c()
+    _check(_load().oracle_xattn_fwd(ctypes.byref(c), out.ctypes.data, lse.ctypes.data),
+           "xattn_fwd")
+    return out, lse
+
+
+def xattn_bwd(pb: XProblem, dout: np.ndarray):
+    """Gradients of sum(out * dout): (dq, dk, dv, dtable or None)."""
+    if len(pb.cu_seqlens_k) != len(pb.cu_seqlens_q) or pb.k.shape != pb.v.shape:
+        raise ValueError("oracle xattn_bwd: mismatched problem")
+    dout = widen(dout)
+    if dout.shape != pb.q.shape:
+        raise ValueError("oracle xattn_bwd: dout shape")
+    dq = np.zeros(pb.q.shape)
+    dk = np.zeros(pb.k.shape)
+    dv = np.zeros(pb.v.shape)
+    dt = np.zeros((pb.num_buckets, pb.q.shape[1])) if pb.table is not None else None
+    c = pb._c()
+    _check(_load().oracle_xattn_bwd(ctypes.byref(c), dout.ctypes.data, dq.ctypes.data,
+                                    dk.ctypes.data, dv.ctypes.data,
+                                    dt.ctypes.data if dt is not None else None), "xattn_bwd")
+    return dq, dk, dv, dt
