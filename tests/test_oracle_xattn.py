@@ -210,3 +210,20 @@ def test_argument_errors():
     xp.cu_seqlens_k = np.array([0, 3], dtype=np.int32)  # does not end at total_k
     with pytest.raises(ValueError):
         oracle.xattn_fwd(xp)
+
+
+@pytest.mark.parametrize("t5,alibi", [((32, 128, False), False), (None, True)])
+def test_decode_row_equals_last_row_of_self_attention(t5, alibi):
+    # decode step: one new query over the whole key cache of its document (causal decoder with
+    # T5 or ALiBi bias) equals the last row of causal self-attention over the full sequence
+    L = [40, 17]
+    full = _xproblem(L, L, 2, 2, 8, seed=63, t5=t5, alibi=alibi, causal=True)
+    o_full, l_full = oracle.xattn_fwd(full)
+    last = np.cumsum(L) - 1
+    dec = oracle.XProblem(full.q[last], full.k, full.v, np.array([0, 1, 2]), full.cu_seqlens_k,
+                          table=full.table, num_buckets=full.num_buckets,
+                          max_distance=full.max_distance, bidirectional=full.bidirectional,
+                          slopes=full.slopes, causal=True, scale=full.scale)
+    o_dec, l_dec = oracle.xattn_fwd(dec)
+    np.testing.assert_allclose(o_dec, o_full[last], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l_dec, l_full[:, last], rtol=0, atol=1e-14)
