@@ -318,3 +318,62 @@ def xattn_bwd(pb: XProblem, dout: np.ndarray):
                                     dk.ctypes.data, dv.ctypes.data,
                                     dt.ctypes.data if dt is not None else None), "xattn_bwd")
     return dq, dk, dv, dt
+
+
+# ---- rotary position embedding (RoPE), applied to Q and K before plain attention ----
+def rope_rotate_at(x, positions, base: float = 10000.0, inverse: bool = False) -> np.ndarray:
+    """Rotary position embedding of RoFormer, the RoPE the FAT5 report lists among the
+    positional encodings its kernels accept (positional-encoding note of the "Noyau CUDA"
+    section). Channel pair (2i, 2i+1) of a row at position m is turned by the angle
+    m * base^(-2i/d); inverse=True turns it back (the transpose, used for gradients).
+    x: [T, H, d] (d even); positions: [T]. fp64 throughout."""
+    x = widen(x)
+    T, H, d = x.shape
+    if d % 2:
+        raise ValueError("rotary embedding needs an even head_dim")
+    pos = np.asarray(positions, dtype=np.float64).reshape(T)
+    theta = base ** (-np.arange(0, d, 2, dtype=np.float64) / d)  # [d/2]
+    ang = pos[:, None] * theta[None, :]  # [T, d/2]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    if inverse:
+        s = -s
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+def doc_positions(cu_seqlens) -> np.ndarray:
+    """Position of every packed token within its document (restarting at 0 per document)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    pos = np.zeros(int(cu[-1]), dtype=np.int64)
+    for i in range(len(cu) - 1):
+        pos[cu[i]:cu[i + 1]] = np.arange(cu[i + 1] - cu[i])
+    return pos
+
+
+def rope_attn_fwd(pb: Problem, base: float = 10000.0):
+    """Attention with RoPE on Q and K (positions local to each document) and the problem's own
+    bias/mask settings: the plain oracle on the rotated inputs. Returns (out, lse)."""
+    pos = doc_positions(pb.cu_seqlens)
+    rot = _replace_qk(pb, rope_rotate_at(pb.q, pos, base), rope_rotate_at(pb.k, pos, base))
+    return attn_fwd(rot)
+
+
+def rope_attn_bwd(pb: Problem, dout: np.ndarray, base: float = 10000.0):
+    """Gradients of sum(out * dout) with respect to the unrotated q, k, v (and the table): the
+    rotation is orthogonal, so dq and dk are the rotated-space gradients turned back."""
+    pos = doc_positions(pb.cu_seqlens)
+    rot = _replace_qk(pb, rope_rotate_at(pb.q, pos, base), rope_rotate_at(pb.k, pos, base))
+    dq_r, dk_r, dv, dt = attn_bwd(rot, dout)
+    return (rope_rotate_at(dq_r, pos, base, inverse=True),
+            rope_rotate_at(dk_r, pos, base, inverse=True), dv, dt)
+
+
+def _replace_qk(pb: Problem, q, k) -> Problem:
+    return Problem(q, k, pb.v, pb.cu_seqlens, table=pb.table, num_buckets=pb.num_buckets,
+                   max_distance=pb.max_distance, bidirectional=pb.bidirectional,
+                   slopes=pb.slopes, causal=pb.causal, scale=pb.scale,
+                   d_from_bf16_out=pb.d_from_bf16_out)
