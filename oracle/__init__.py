@@ -4,9 +4,12 @@ TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the CPU-bas
 ``bench.py`` are the only callers. The product library never imports this package, and this
 package never imports the product library.
 
-The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP); this module compiles it with gcc and
-marshals numpy arrays through ctypes. Inputs may be the exact bf16 bit patterns the GPU path
-receives (numpy ``uint16``), fp32 or fp64 arrays; all are widened exactly to fp64 here.
+The arithmetic lives in ``oracle.c`` (self-attention with the relative-position bias) and
+``oracle_xattn.c`` (own query and key lengths per document, grouped-query heads, bottom-right
+causal alignment), plain C, fp64, OpenMP; this module compiles them with gcc and marshals numpy
+arrays through ctypes. The rotary embedding (``rope_*``) is numpy fp64 around the plain oracle.
+Inputs may be the exact bf16 bit patterns the GPU path receives (numpy ``uint16``), fp32 or fp64
+arrays; all are widened exactly to fp64 here.
 """
 from __future__ import annotations
 
