@@ -525,10 +525,19 @@ def run_ours(args, rank, world, local_rank):
             for idx in (0, 2, 3, 4):
                 ow = wl.WORKLOADS[idx]
                 if ow.name != w.name:
-                    try:
+                    try:  # one side measurement must not cost the line
                         others[ow.name] = quick_other(ow, device, peaks)
-                    except Exception as e:  # one side measurement must not cost the line
+                    except Exception as e:
                         others[ow.name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+                        continue
+                    try:  # the oracle beside it, on a ~3 s sample
+                        cb = cpu_baseline(ow, seconds=3.0)
+                        cb["full_workload_s_extrapolated"] = round(
+                            3.5 * ow.fwd_flops() / (cb["value"] * 1e12), 1)
+                        others[ow.name]["cpu_baseline"] = cb
+                    except Exception as e:
+                        others[ow.name]["cpu_baseline"] = {
+                            "error": f"{type(e).__name__}: {e}"[:200]}
             line["other_workloads"] = others
             line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
