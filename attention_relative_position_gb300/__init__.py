@@ -15,7 +15,9 @@ from typing import Optional
 __all__ = [
     "FatAttnError", "load", "fat_attn_fwd", "fat_attn_bwd", "fat_attn_bwd_workspace_size",
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
-    "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages", "LIB_PATH",
+    "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages",
+    "fat_attn_bwd_noalloc", "FAT_DEVERR_TIMEOUT_FWD", "FAT_DEVERR_TIMEOUT_BWD",
+    "FAT_DEVERR_SEQLENS", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfatattn.so")
