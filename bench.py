@@ -394,6 +394,14 @@ def cpu_baseline(w, seconds=10.0):
             "seconds": dt}
 
 
+def _guarded(fn, *args):
+    """fn(*args), or an error record: a side figure must not cost the benchmark line."""
+    try:
+        return fn(*args)
+    except Exception as e:
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
 def hbm_bytes(w):
     """Algorithmic HBM bytes of one launch of each kernel: the forward reads Q, K, V (and the
     table) and writes O and lse; the backward preprocess reads O and dO, writes D and zeroes the
@@ -437,7 +445,7 @@ def quick_other(w, device, peaks, steps=10):
     res.update({k + "_frac": v / peaks["bf16_tflops"] for k, v in list(res.items())})
     res = {k: round(v, 4) for k, v in res.items()}
     res["ms_per_step"] = round(step_ms, 4)
-    res["hbm"] = hbm_figures(w, per, peaks["hbm_gbs"])
+    res["hbm"] = _guarded(hbm_figures, w, per, peaks["hbm_gbs"])
     del r
     return res
 
@@ -503,7 +511,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} bf16 dense (burst; kernel timed alone)",
                      "traffic": traffic_for(f"{kname}<{w.head_dim}>@{w.name}"),
                      "algorithmic_flops_per_launch": kflops},
-        "hbm": hbm_figures(w, per, peaks["hbm_gbs"]),
+        "hbm": _guarded(hbm_figures, w, per, peaks["hbm_gbs"]),
         "gpu_launches": steps * Runner.LAUNCHES_PER_STEP,
         "timed_wall_s": round(wall, 4),
     }

@@ -36,3 +36,10 @@ def test_hbm_figures_units():
     assert r["bwd_fin_us"] == 20.0
     assert abs(r["fwd_gbs_frac"] - r["fwd_gbs"] / 5000.0) < 1e-4
     assert r["peak_gbs"] == 5000.0
+
+
+def test_guarded_side_figure_records_errors():
+    import bench
+    assert bench._guarded(lambda a: a + 1, 1) == 2
+    r = bench._guarded(lambda: 1 / 0)
+    assert r["error"].startswith("ZeroDivisionError")
