@@ -103,6 +103,13 @@ def _stream_ptr(stream, device) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _on(device):
+    """Context that makes `device` the current CUDA device for the duration of a library call:
+    the library launches on, and looks up its per-GPU state for, the current device."""
+    import torch
+    return torch.cuda.device(device)
+
+
 def _shape(total_tokens, num_seqs, max_seqlen, num_heads, head_dim, stream_ptr) -> _Shape:
     return _Shape(int(total_tokens), int(num_seqs), int(max_seqlen), int(num_heads),
                   int(head_dim), stream_ptr)
@@ -141,10 +148,11 @@ def fat_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, bias_table=None, num_buck
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
-    rc = lib.fat_attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
-                          int(num_buckets), int(max_distance), int(bool(bidirectional)),
-                          _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
-                          float(softmax_scale), _ptr(out), _ptr(lse))
+    with _on(q.device):
+        rc = lib.fat_attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                              int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                              _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                              float(softmax_scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_fwd")
     return out, lse
@@ -181,12 +189,14 @@ def fat_attn_bwd(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, bias_tabl
     need = int(lib.fat_attn_bwd_workspace_size(ctypes.byref(sh)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    rc = lib.fat_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
-                          int(num_buckets), int(max_distance), int(bool(bidirectional)),
-                          _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
-                          float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
-                          _ptr(workspace), int(workspace.numel()), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(dbias_table))
+    with _on(q.device):
+        rc = lib.fat_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                              int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                              _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                              float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
+                              _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                              _ptr(dq), _ptr(dk), _ptr(dv),
+                              _ptr(dbias_table))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd")
     return dq, dk, dv, dbias_table
@@ -206,23 +216,26 @@ def fat_attn_bwd_stages(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, wo
     nbytes = int(workspace.numel() * workspace.element_size())
     if between is not None:
         between(-1)
-    rc = lib.fat_attn_bwd_preprocess(ctypes.byref(sh), _ptr(out), _ptr(dout), _ptr(workspace),
-                                     nbytes, _ptr(dbias_table), int(num_buckets))
+    with _on(q.device):
+        rc = lib.fat_attn_bwd_preprocess(ctypes.byref(sh), _ptr(out), _ptr(dout), _ptr(workspace),
+                                         nbytes, _ptr(dbias_table), int(num_buckets))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd_preprocess")
     if between is not None:
         between(0)
-    rc = lib.fat_attn_bwd_main(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
-                               int(num_buckets), int(max_distance), int(bool(bidirectional)),
-                               _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
-                               float(softmax_scale), _ptr(lse), _ptr(dout), _ptr(workspace),
-                               nbytes, _ptr(dk), _ptr(dv), _ptr(dbias_table))
+    with _on(q.device):
+        rc = lib.fat_attn_bwd_main(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                                   int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                                   _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                                   float(softmax_scale), _ptr(lse), _ptr(dout), _ptr(workspace),
+                                   nbytes, _ptr(dk), _ptr(dv), _ptr(dbias_table))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd_main")
     if between is not None:
         between(1)
-    rc = lib.fat_attn_bwd_finalize(ctypes.byref(sh), _ptr(workspace), nbytes,
-                                   float(softmax_scale), _ptr(dq))
+    with _on(q.device):
+        rc = lib.fat_attn_bwd_finalize(ctypes.byref(sh), _ptr(workspace), nbytes,
+                                       float(softmax_scale), _ptr(dq))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd_finalize")
     if between is not None:
@@ -240,11 +253,12 @@ def fat_attn_bwd_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, d
     lib = load()
     T, H, d = q.shape
     sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
-    rc = lib.fat_attn_bwd_noalloc(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
-                                  int(num_buckets), int(max_distance), int(bool(bidirectional)),
-                                  _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
-                                  float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
-                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias_table))
+    with _on(q.device):
+        rc = lib.fat_attn_bwd_noalloc(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                                      int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                                      _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
+                                      float(softmax_scale), _ptr(out), _ptr(lse), _ptr(dout),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias_table))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd_noalloc")
     return dq, dk, dv, dbias_table
@@ -284,9 +298,10 @@ def fat_attn_debug_buckets(delta_lo: int, n: int, num_buckets: int, max_distance
     lib = load()
     if out is None:
         out = torch.empty(n, dtype=torch.int32, device=device)
-    rc = lib.fat_attn_debug_buckets(int(delta_lo), int(n), int(num_buckets), int(max_distance),
-                                    int(bool(bidirectional)), _ptr(out),
-                                    _stream_ptr(stream, out.device))
+    with _on(out.device):
+        rc = lib.fat_attn_debug_buckets(int(delta_lo), int(n), int(num_buckets), int(max_distance),
+                                        int(bool(bidirectional)), _ptr(out),
+                                        _stream_ptr(stream, out.device))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_debug_buckets")
     return out

@@ -20,27 +20,18 @@ std::mutex g_mu;
 thread_local char g_last_error[256] = "";
 long long g_timeout_ns = kDefaultTimeoutNs;
 int g_debug_flags = 0;
-int *g_err_ptr[128] = {nullptr};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Address of the current device's error word, looked up on every call (a host-side query that
+// allocates nothing), so that no address outlives a context that was torn down.
 int device_error_ptr(int **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 128) {
-    set_last_error("cudaGetDevice", (int)e, cudaGetErrorString(e));
+  void *ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_fat_device_error);
+  if (e != cudaSuccess) {
+    set_last_error("cudaGetSymbolAddress(error word)", (int)e, cudaGetErrorString(e));
     return FAT_ECUDA;
   }
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
-    void *ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_fat_device_error);
-    if (e != cudaSuccess) {
-      set_last_error("cudaGetSymbolAddress(error word)", (int)e, cudaGetErrorString(e));
-      return FAT_ECUDA;
-    }
-    g_err_ptr[dev] = static_cast<int *>(ptr);
-  }
-  *out = g_err_ptr[dev];
+  *out = static_cast<int *>(ptr);
   return FAT_OK;
 }
 
@@ -384,7 +375,7 @@ int fat_attn_fwd(const fat_shape_t *sh, const void *q, const void *k, const void
   if (sh->total_tokens == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0) return FAT_OK;
   rc = device_error_ptr(&p.err);
   if (rc) return rc;
-  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens};
+  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens, sh->max_seqlen};
   p.causal = causal ? 1 : 0;
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(out);
@@ -516,7 +507,7 @@ int bwd_main_impl(const fat_shape_t *sh, const void *q, const void *k, const voi
   if (empty_problem(sh)) return FAT_OK;
   rc = device_error_ptr(&p.err);
   if (rc) return rc;
-  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens};
+  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens, sh->max_seqlen};
   p.causal = causal ? 1 : 0;
   p.scale_log2 = softmax_scale * kLog2e;
   p.scale = softmax_scale;
@@ -585,24 +576,45 @@ int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t w
   return bwd_finalize_impl(sh, workspace, workspace_bytes, softmax_scale, dq, false);
 }
 
+}  // extern "C"
+
+namespace fat {
+int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                   const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                   const float *alibi_slopes, const int32_t *cu_seqlens, const void *out,
+                   const float *lse, const void *dout, const void *dq, const void *dk,
+                   const void *dv, const float *dbias_table) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  if (!q || !k || !v || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv)
+    return FAT_EINVAL_NULL;
+  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
+      misaligned(dq) || misaligned(dk) || misaligned(dv) || misaligned(lse) ||
+      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
+      misaligned(dbias_table))
+    return FAT_EINVAL_SHAPE;
+  BiasParams b{};
+  rc = fill_bias(&b, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (bwd_smem_bytes(sh->head_dim, b.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  return FAT_OK;
+}
+}  // namespace fat
+
+extern "C" {
+
 int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
                  float softmax_scale, const void *out, const float *lse, const void *dout,
                  void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
                  float *dbias_table) {
-  int rc = check_shape(sh);
-  if (rc) return rc;
-  if (!q || !k || !v || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv)
-    return FAT_EINVAL_NULL;
-  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
   // validate everything before enqueueing anything
-  if (misaligned(out) || misaligned(dq)) return FAT_EINVAL_SHAPE;
+  int rc = check_bwd_args(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                          alibi_slopes, cu_seqlens, out, lse, dout, dq, dk, dv, dbias_table);
+  if (rc) return rc;
   {
-    BiasParams b{};
-    rc = fill_bias(&b, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
-    if (rc) return rc;
-    if (bwd_smem_bytes(sh->head_dim, b.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
     WorkspaceView ws{};
     rc = check_workspace(sh, workspace, workspace_bytes, &ws);
     if (rc) return rc;

@@ -254,10 +254,12 @@ __global__ void __launch_bounds__(640, 1)
       const long long rest = rank % n_dh;
       const int h = (int)(rest % H), doc = (int)(rest / H);
       const int s0 = __ldg(p.seq.cu_seqlens + doc), s1 = __ldg(p.seq.cu_seqlens + doc + 1);
-      if (s0 < 0 || s1 > T || s1 < s0) {
-        if (tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+      if (s0 < 0 || s1 > T || s1 < s0) {  // reported by whichever thread decodes the item
+        atomicOr(p.err, FAT_DEVERR_SEQLENS);
         continue;
       }
+      // key tiles of a document longer than max_seqlen lie beyond the item space: reported
+      if (kb == 0 && s1 - s0 > p.seq.max_seqlen) atomicOr(p.err, FAT_DEVERR_SEQLENS);
       if (kb * 128 >= s1 - s0) continue;
       w.kb = kb;
       w.h = h;
@@ -988,6 +990,7 @@ __global__ void __launch_bounds__(640, 1)
     return;
   }
   const int L = seq_end - seq_start;
+  if (L > p.seq.max_seqlen && kb == 0 && tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int ks = kb * 128;
   if (ks >= L) return;
   const int i0 = p.causal ? ks / C::BQ : 0;

@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   const int L = seq_end - seq_start;
+  // a document longer than the caller's max_seqlen has rows no block covers: reported, once
+  if (L > p.seq.max_seqlen && blockIdx.x == 0 && tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int q0 = qb * 256;
   if (q0 >= L) return;  // whole CTA, before any barrier or TMEM allocation
   const int ntile = (q0 + 128 < L) ? 2 : 1;

@@ -41,6 +41,7 @@ struct BiasParams {
 struct SeqParams {
   const int32_t *cu_seqlens;
   int num_seqs, num_heads, total_tokens;
+  int max_seqlen;  // the caller's bound on every document length (sizes the grids)
 };
 
 __device__ __forceinline__ int t5_bucket_dev(int delta, const BiasParams &b) {
@@ -133,6 +134,14 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
 size_t bwd_smem_bytes(int head_dim, int lut_len);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);
+
+// The host-side argument checks of the backward (everything but the workspace): FAT_OK or the
+// FAT_E* code fat_attn_bwd would return for these arguments.
+int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                   const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                   const float *alibi_slopes, const int32_t *cu_seqlens, const void *out,
+                   const float *lse, const void *dout, const void *dq, const void *dk,
+                   const void *dv, const float *dbias_table);
 
 // Number of SMs of the current device (cached per device; 0 if the query fails).
 int sm_count();

@@ -22,7 +22,8 @@ std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[128] = {nullptr};  // device address of the array, per device ordinal
 
 // Device address of the scratch on the current device. The first call on a device looks it up
-// (with that device current); later calls reuse it.
+// (set-up, with that device current); later calls reuse it. The address stays valid as long as
+// the device's primary context does: resetting the device after the first call is unsupported.
 int scratch_on_current_device(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -54,9 +55,12 @@ extern "C" int fat_attn_bwd_noalloc(const fat_shape_t *sh, const void *q, const 
                                     int causal, float softmax_scale, const void *out,
                                     const float *lse, const void *dout, void *dq, void *dk,
                                     void *dv, float *dbias_table) {
-  if (!sh) return FAT_EINVAL_NULL;
+  // the same argument checks as fat_attn_bwd first, so that errors come out as they would there
+  int rc = fat::check_bwd_args(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                               alibi_slopes, cu_seqlens, out, lse, dout, dq, dk, dv,
+                               dbias_table);
+  if (rc) return rc;
   const size_t need = fat_attn_bwd_workspace_size(sh);
-  if (need == 0 && (sh->head_dim != 64 && sh->head_dim != 128)) return FAT_EINVAL_SHAPE;
   if (need > (size_t)FAT_NOALLOC_SCRATCH_BYTES) {
     fat::set_last_error("fat_attn_bwd_noalloc: the problem needs more scratch than the built-in "
                         "array holds (bytes needed)",
@@ -65,7 +69,7 @@ extern "C" int fat_attn_bwd_noalloc(const fat_shape_t *sh, const void *q, const 
     return FAT_EUNSUPPORTED;
   }
   void *scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  rc = scratch_on_current_device(&scratch);
   if (rc) return rc;
   return fat_attn_bwd(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
                       alibi_slopes, cu_seqlens, causal, softmax_scale, out, lse, dout, scratch,

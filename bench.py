@@ -27,7 +27,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "bf16 attention TFLOP/s fwd & fwd+bwd (T5-bias, varlen) vs tensor-core peak"
-DEFAULT_WORKLOAD = 1  # T5 encoder, batch 8 x seq 1024, 8 heads, head_dim 64
+# the largest single-GPU workload: long-context T5 encoder, 1 x 16384 tokens, 12 heads, d 64
+DEFAULT_WORKLOAD = 4
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -224,7 +225,7 @@ class Runner:
 
 
 def time_steps(r, steps, flush=True):
-    """Device times (ms) of `steps` steps, L2 flushed between steps (not timed): "step" from
+    """Device times (ms, one entry per step; summarised by their median) of `steps` steps, L2 flushed between steps (not timed): "step" from
     steps through the public calls, each bracketed by CUDA events on the launching stream;
     the per-kernel times from as many steps run stage by stage with events between kernels."""
     torch = r.torch
@@ -416,13 +417,13 @@ def hbm_bytes(w):
 
 
 def hbm_figures(w, per, peak_gbs):
-    """GB/s of the memory-bound kernels (algorithmic bytes / mean CUDA-event time) and their
+    """GB/s of the memory-bound kernels (algorithmic bytes / median CUDA-event time) and their
     fraction of the measured copy bandwidth; the forward's figure matters for short sequences,
     where it is latency-bound rather than tensor-bound."""
     b = hbm_bytes(w)
     res = {}
     for k in ("fwd", "bwd_pre", "bwd_fin"):
-        ms = statistics.mean(per[k])
+        ms = statistics.median(per[k])
         gbs = b[k] / ms / 1e6
         res[k + "_us"] = round(ms * 1e3, 2)
         res[k + "_gbs"] = round(gbs, 1)
@@ -437,9 +438,9 @@ def quick_other(w, device, peaks, steps=10):
         r.step()
     per = time_steps(r, steps)
     f = w.fwd_flops()
-    fwd_ms = statistics.mean(per["fwd"])
-    step_ms = statistics.mean(per["step"])
-    main_ms = statistics.mean(per["bwd_main"])
+    fwd_ms = statistics.median(per["fwd"])
+    step_ms = statistics.median(per["step"])
+    main_ms = statistics.median(per["bwd_main"])
     res = {"fwd_tflops": f / fwd_ms / 1e9, "fwd_bwd_tflops": 3.5 * f / step_ms / 1e9,
            "bwd_main_tflops": 2.5 * f / main_ms / 1e9}
     res.update({k + "_frac": v / peaks["bf16_tflops"] for k, v in list(res.items())})
@@ -484,12 +485,12 @@ def run_ours(args, rank, world, local_rank):
     bits = r.fa.fat_attn_get_device_error()
     if bits:
         raise RuntimeError(f"device error word {bits}")
-    mean = {k: statistics.mean(v) for k, v in per.items()}
-    step_ms = max_over_ranks(mean["step"], device)
+    med = {k: statistics.median(v) for k, v in per.items()}
+    step_ms = max_over_ranks(med["step"], device)
     f = w.fwd_flops()
     value = job_tflops(3.5 * f, world, step_ms)  # TFLOP/s
-    kernels = {"fwd": ("fat_fwd_kernel", f, mean["fwd"], "fat_attn_fwd.cu"),
-               "bwd_main": ("fat_bwd_kernel", 2.5 * f, mean["bwd_main"], "fat_attn_bwd.cu")}
+    kernels = {"fwd": ("fat_fwd_kernel", f, med["fwd"], "fat_attn_fwd.cu"),
+               "bwd_main": ("fat_bwd_kernel", 2.5 * f, med["bwd_main"], "fat_attn_bwd.cu")}
     dom = max(kernels, key=lambda k: kernels[k][2])
     kname, kflops, kms, ksrc = kernels[dom]
     achieved = kflops / kms / 1e9
@@ -501,10 +502,11 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1)-type inputs of the workload's shapes; no dataset)",
         "config": workload_config(w, world, "flushed between timed steps (256 MiB write, "
                                             "outside the timed kernels)"),
-        "fwd_tflops": round(f / mean["fwd"] / 1e9, 3),
-        "bwd_tflops": round(2.5 * f / (mean["bwd_pre"] + mean["bwd_main"] + mean["bwd_fin"])
+        "fwd_tflops": round(f / med["fwd"] / 1e9, 3),
+        "bwd_tflops": round(2.5 * f / (med["bwd_pre"] + med["bwd_main"] + med["bwd_fin"])
                             / 1e9, 3),
-        "per_kernel_ms": {k: round(v, 5) for k, v in mean.items()},
+        "per_kernel_ms": {k: round(v, 5) for k, v in med.items()},
+        "timing": "median of the per-step CUDA-event times",
         "roofline": {"kernel": f"{kname}<{w.head_dim}>", "bound": "tensor",
                      "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
@@ -530,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0 and world == 1:
             from attention_relative_position_gb300 import workloads as wl
             others = {}
-            for idx in (0, 2, 3, 4):
+            for idx in range(len(wl.WORKLOADS)):
                 ow = wl.WORKLOADS[idx]
                 if ow.name != w.name:
                     try:  # one side measurement must not cost the line
@@ -584,10 +586,13 @@ def run_reference(args, rank, world):
         f = 3.5 * 4.0 * L * L * w.head_dim
         return f / 2 if w.causal else f
 
+    # warm-up: the oracle has no cache or compiled code to warm, so each warm-up step is one
+    # forward row (it only touches the library and the input pages)
     for k in range(warmup):
-        one(k)
+        doc, h = pairs[k % len(pairs)]
+        oracle.attn_fwd_rows(pb, doc, h, [0])
     t0 = time.perf_counter()
-    flops = sum(one(warmup + k) for k in range(steps))
+    flops = sum(one(k) for k in range(steps))
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {

@@ -29,9 +29,12 @@
  * Every pointer must be 16-byte aligned. head_dim must be 64 or 128.
  *
  * Ownership and execution. The caller allocates every buffer, including the backward
- * workspace; the library never allocates device memory. Calls are asynchronous on
- * shape->stream (a cudaStream_t; NULL = legacy default stream) and return after enqueueing.
- * The only global state is a device error word per GPU (see fat_attn_get_device_error).
+ * workspace; no call allocates device memory. Calls are asynchronous on shape->stream (a
+ * cudaStream_t; NULL = legacy default stream) and return after enqueueing. Global state: a
+ * device error word per GPU (see fat_attn_get_device_error) and the scratch array of
+ * fat_attn_bwd_noalloc (FAT_NOALLOC_SCRATCH_BYTES per GPU), both file-scope device variables
+ * that every GPU on which the library's module is loaded holds until the process exits, whether
+ * or not those calls are made.
  *
  * Errors. Every call returns 0 on success or a negative FAT_E* code; nothing throws, exits or
  * traps. Argument errors are detected on the host before anything is enqueued. Device-side
@@ -60,13 +63,16 @@ extern "C" {
 /* bits of the device error word */
 #define FAT_DEVERR_TIMEOUT_FWD 1 /* a forward pipeline wait exceeded its time limit */
 #define FAT_DEVERR_TIMEOUT_BWD 2 /* a backward pipeline wait exceeded its time limit */
-#define FAT_DEVERR_SEQLENS 4     /* cu_seqlens had an entry outside [0, total_tokens] or out of order */
+#define FAT_DEVERR_SEQLENS 4     /* cu_seqlens had an entry outside [0, total_tokens] or out of
+                                    order, or a document longer than max_seqlen (its rows beyond
+                                    the grid were not computed) */
 
 typedef struct {
   int32_t total_tokens; /* T: sum of document lengths (rows of q, k, v) */
   int32_t num_seqs;     /* n: number of documents; cu_seqlens has n + 1 entries */
   int32_t max_seqlen;   /* upper bound on every document length (sizes the grid; must not be
-                           smaller than the longest document, which the host cannot check) */
+                           smaller than the longest document: the host cannot check it, the
+                           kernels report a longer one as FAT_DEVERR_SEQLENS) */
   int32_t num_heads;    /* H (q, k and v share the head count) */
   int32_t head_dim;     /* d: 64 or 128 */
   void *stream;         /* cudaStream_t the work is enqueued on */
@@ -144,7 +150,10 @@ int fat_attn_bwd_finalize(const fat_shape_t *shape, const void *workspace,
  *     rejected with FAT_EUNSUPPORTED before any work is enqueued (fat_attn_last_error_message
  *     says why); e.g. T * H * (d + 1) * 4 bytes must fit, about 8 M elements of q at d = 64.
  *   - The first call on a device looks up the array's device address with that device current;
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture. Make the device of shape->stream current
+ *     for every call (as for any kernel launch); resetting a device after its first call is not
+ *     supported (the looked-up address is kept for the life of the process).
+ *   - Argument errors are reported exactly as fat_attn_bwd reports them, before the size test.
  *   - All calls on a device share the one array, which keeps whatever the last call left there
  *     (each call zeroes the part that must start at zero). Calls whose work overlaps on the GPU
  *     (other streams, other host threads) race on it and must be serialised by the caller.

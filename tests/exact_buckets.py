@@ -40,3 +40,21 @@ def exact_bucket(delta: int, nb: int, md: int, bidir: bool) -> int:
         _cache[key] = exact_thresholds(nbh, md)
     t = sum(1 for th in _cache[key] if n >= th)
     return off + me + t
+
+
+def exact_bucket_array(deltas, nb: int, md: int, bidir: bool):
+    """exact_bucket over a numpy array of deltas: the thresholds come from the integer roots
+    above, the count of thresholds <= n from a sorted search."""
+    import numpy as np
+    deltas = np.asarray(deltas, dtype=np.int64)
+    nbh = nb // 2 if bidir else nb
+    me = nbh // 2
+    thr = np.asarray(exact_thresholds(nbh, md), dtype=np.int64)
+    if bidir:
+        off = np.where(deltas > 0, nbh, 0)
+        n = np.abs(deltas)
+    else:
+        off = np.zeros_like(deltas)
+        n = np.maximum(-deltas, 0)
+    t = np.searchsorted(thr, n, side="right")
+    return off + np.where(n < me, n, me + t)

@@ -410,3 +410,11 @@ def test_backward_with_bf16_output_statistic_identity(causal, alibi):
                     b = exact_bucket(r - p, pb.num_buckets, pb.max_distance, pb.bidirectional)
                     want[b, h] += P[p, r] * delta[s + p, h]
     np.testing.assert_allclose(dt1 - dt0, want, atol=1e-12)
+
+
+@pytest.mark.parametrize("nb,md,bidir", BUCKET_CASES)
+def test_vectorised_exact_bucket_matches_scalar_form(nb, md, bidir):
+    from exact_buckets import exact_bucket_array
+    deltas = np.arange(-3000, 3001)
+    want = np.array([exact_bucket(int(x), nb, md, bidir) for x in deltas])
+    np.testing.assert_array_equal(exact_bucket_array(deltas, nb, md, bidir), want)

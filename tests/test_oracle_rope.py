@@ -44,6 +44,30 @@ def test_first_pair_turns_by_the_position_in_radians():
     np.testing.assert_allclose(y[:, 0, 1], np.sin(m), atol=1e-15)
 
 
+def test_frequency_ladder_hand_values():
+    """The frequency of pair i is base^(-2i/d), pinned by values worked out by hand:
+    d = 4, base = 100 gives theta_1 = 100^(-1/2) = 0.1, so pair 1 at position 10 turns by one
+    radian; d = 8, base = 10^4 gives theta_i = 10^(-i) (1, 0.1, 0.01, 0.001), so pair i at
+    position 10^i turns by one radian. A ladder over d/2 instead of d, or starting at i = 1,
+    moves every one of these."""
+    x = np.zeros((1, 1, 4))
+    x[0, 0, 2] = 1.0
+    y = oracle.rope_rotate_at(x, [10], base=100.0)
+    np.testing.assert_allclose(y[0, 0], [0.0, 0.0, np.cos(1.0), np.sin(1.0)], atol=1e-14)
+    for i in range(4):
+        x = np.zeros((1, 1, 8))
+        x[0, 0, 2 * i] = 1.0
+        y = oracle.rope_rotate_at(x, [10 ** i], base=1e4)
+        want = np.zeros(8)
+        want[2 * i], want[2 * i + 1] = np.cos(1.0), np.sin(1.0)
+        np.testing.assert_allclose(y[0, 0], want, atol=1e-12)
+    # a second pair at the same time: pair 1 of d = 8 at position 5 turns by 0.5 radian
+    x = np.zeros((1, 1, 8))
+    x[0, 0, 3] = 1.0  # the odd channel of pair 1: (0, 1) turns to (-sin, cos)
+    y = oracle.rope_rotate_at(x, [5], base=1e4)
+    np.testing.assert_allclose(y[0, 0, 2:4], [-np.sin(0.5), np.cos(0.5)], atol=1e-14)
+
+
 def test_scores_depend_only_on_relative_position():
     rng = np.random.default_rng(72)
     q = rng.standard_normal((1, 1, 32))
