@@ -16,7 +16,8 @@ __all__ = [
     "FatAttnError", "load", "fat_attn_fwd", "fat_attn_bwd", "fat_attn_bwd_workspace_size",
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
     "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages",
-    "fat_attn_bwd_noalloc", "FAT_DEVERR_TIMEOUT_FWD", "FAT_DEVERR_TIMEOUT_BWD",
+    "fat_attn_bwd_noalloc", "fat_xattn_fwd", "fat_xattn_bwd", "fat_xattn_bwd_workspace_size",
+    "fat_xattn_splitkv_num_splits", "FAT_DEVERR_TIMEOUT_FWD", "FAT_DEVERR_TIMEOUT_BWD",
     "FAT_DEVERR_SEQLENS", "LIB_PATH",
 ]
 
@@ -40,6 +41,14 @@ class _Shape(ctypes.Structure):
     _fields_ = [("total_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
                 ("max_seqlen", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("stream", ctypes.c_void_p)]
+
+
+class _XShape(ctypes.Structure):
+    _fields_ = [("total_q", ctypes.c_int32), ("total_k", ctypes.c_int32),
+                ("num_seqs", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
+                ("max_seqlen_k", ctypes.c_int32), ("num_heads_q", ctypes.c_int32),
+                ("num_heads_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("stream", ctypes.c_void_p)]
 
 
 _lib = None
@@ -75,6 +84,21 @@ def load(path: Optional[str] = None):
     lib.fat_attn_bwd_noalloc.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp,
                                          vp, vp, vp, vp, vp, vp]
     lib.fat_attn_bwd_noalloc.restype = i32
+    X = ctypes.POINTER(_XShape)
+    lib.fat_xattn_fwd.argtypes = [X, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, f32, vp, vp]
+    lib.fat_xattn_fwd.restype = i32
+    lib.fat_xattn_splitkv_num_splits.argtypes = [X]
+    lib.fat_xattn_splitkv_num_splits.restype = i32
+    lib.fat_xattn_splitkv_workspace_size.argtypes = [X, i32]
+    lib.fat_xattn_splitkv_workspace_size.restype = ctypes.c_size_t
+    lib.fat_xattn_fwd_splitkv.argtypes = [X, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, f32,
+                                          i32, vp, ctypes.c_size_t, vp, vp]
+    lib.fat_xattn_fwd_splitkv.restype = i32
+    lib.fat_xattn_bwd_workspace_size.argtypes = [X]
+    lib.fat_xattn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fat_xattn_bwd.argtypes = [X, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, f32, vp, vp,
+                                  vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.fat_xattn_bwd.restype = i32
     lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.fat_attn_get_device_error.restype = i32
     lib.fat_attn_strerror.argtypes = [i32]
@@ -261,6 +285,109 @@ def fat_attn_bwd_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, lse, dout, d
                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias_table))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_bwd_noalloc")
+    return dq, dk, dv, dbias_table
+
+
+def _xshape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, stream) -> _XShape:
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    return _XShape(int(Tq), int(Tk), int(cu_seqlens_q.numel() - 1), int(max_seqlen_q),
+                   int(max_seqlen_k), int(Hq), int(Hkv), int(d), _stream_ptr(stream, q.device))
+
+
+def fat_xattn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  bias_table=None, num_buckets: int = 0, max_distance: int = 0,
+                  bidirectional: bool = True, alibi_slopes=None, causal: bool = False,
+                  softmax_scale: float = 1.0, out=None, lse=None, num_splits: int = 1,
+                  workspace=None, stream=None):
+    """Forward with its own query and key lengths per document (cross-attention, decode over a
+    key cache) and grouped-query heads. q: bf16 [Tq, Hq, d]; k, v: bf16 [Tk, Hkv, d];
+    cu_seqlens_q / cu_seqlens_k: int32 [n + 1]. num_splits > 1 splits every document's keys
+    into that many ranges (merged by a second grid); 0 lets the library choose.
+    Returns (out bf16 [Tq, Hq, d], lse fp32 [Hq, Tq])."""
+    import torch
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_tensor(name, t, torch.bfloat16, 3)
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        _check_tensor(name, t, torch.int32, 1)
+    _check_tensor("bias_table", bias_table, torch.float32)
+    _check_tensor("alibi_slopes", alibi_slopes, torch.float32)
+    Tq, Hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    sh = _xshape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, stream)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), int(num_buckets), int(max_distance),
+            int(bool(bidirectional)), _ptr(alibi_slopes), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            int(bool(causal)), float(softmax_scale))
+    with _on(q.device):
+        if num_splits == 0:
+            num_splits = int(lib.fat_xattn_splitkv_num_splits(ctypes.byref(sh)))
+        if num_splits == 1:
+            rc = lib.fat_xattn_fwd(ctypes.byref(sh), *args, _ptr(out), _ptr(lse))
+        else:
+            need = int(lib.fat_xattn_splitkv_workspace_size(ctypes.byref(sh), int(num_splits)))
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+            rc = lib.fat_xattn_fwd_splitkv(ctypes.byref(sh), *args, int(num_splits),
+                                           _ptr(workspace),
+                                           int(workspace.numel() * workspace.element_size()),
+                                           _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_xattn_fwd")
+    return out, lse
+
+
+def fat_xattn_splitkv_num_splits(q, k, cu_seqlens_q, max_seqlen_q: int, max_seqlen_k: int) -> int:
+    """The number of key splits the library suggests for this problem."""
+    sh = _xshape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, None)
+    return int(load().fat_xattn_splitkv_num_splits(ctypes.byref(sh)))
+
+
+def fat_xattn_bwd_workspace_size(total_q: int, total_k: int, num_heads_q: int,
+                                 num_heads_kv: int, head_dim: int) -> int:
+    sh = _XShape(int(total_q), int(total_k), 1, 1, 1, int(num_heads_q), int(num_heads_kv),
+                 int(head_dim), None)
+    return int(load().fat_xattn_bwd_workspace_size(ctypes.byref(sh)))
+
+
+def fat_xattn_bwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  out, lse, dout, bias_table=None, num_buckets: int = 0, max_distance: int = 0,
+                  bidirectional: bool = True, alibi_slopes=None, causal: bool = False,
+                  softmax_scale: float = 1.0, want_dbias: bool = True, workspace=None, dq=None,
+                  dk=None, dv=None, dbias_table=None, stream=None):
+    """Backward of sum(out * dout) for fat_xattn_fwd. Returns (dq, dk, dv, dbias or None)."""
+    import torch
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check_tensor(name, t, torch.bfloat16, 3)
+    _check_tensor("lse", lse, torch.float32, 2)
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        _check_tensor(name, t, torch.int32, 1)
+    _check_tensor("bias_table", bias_table, torch.float32)
+    _check_tensor("alibi_slopes", alibi_slopes, torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dbias_table is None and want_dbias and bias_table is not None:
+        dbias_table = torch.empty_like(bias_table)
+    sh = _xshape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, stream)
+    need = int(lib.fat_xattn_bwd_workspace_size(ctypes.byref(sh)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with _on(q.device):
+        rc = lib.fat_xattn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
+                               int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                               _ptr(alibi_slopes), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                               int(bool(causal)), float(softmax_scale), _ptr(out), _ptr(lse),
+                               _ptr(dout), _ptr(workspace),
+                               int(workspace.numel() * workspace.element_size()), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(dbias_table))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_xattn_bwd")
     return dq, dk, dv, dbias_table
 
 

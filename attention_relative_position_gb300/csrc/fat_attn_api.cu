@@ -203,7 +203,8 @@ int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, in
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        box_c * 4 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_last_error("cuTensorMapEncodeTiled(fp32)", (int)r, "");
@@ -217,15 +218,17 @@ int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, in
 using namespace fat;
 
 // ---- preprocessing and finishing kernels of the backward -----------------------------------
-// D[h, t] = sum_c dout[t, h, c] * out[t, h, c] (fp32), the dQ accumulator zeroed, and the
-// table gradient zeroed. Memory bound: each lane loads 16 bytes of out and of dout (D/8 lanes per
-// (token, head) row, two row groups in flight per thread), and the zeroing is a separate flat
-// sweep of 16-byte stores over the accumulator.
+// D[h, t] = sum_c dout[t, h, c] * out[t, h, c] (fp32), the fp32 accumulators zeroed (dQ, and
+// dK, dV when query heads share key/value heads: one contiguous region of n4_zero float4), and
+// the table gradient zeroed. Memory bound: each lane loads 16 bytes of out and of dout (D/8
+// lanes per (token, head) row, two row groups in flight per thread), and the zeroing is a
+// separate flat sweep of 16-byte stores.
 template <int D>
 __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restrict__ out,
                                                            const uint4 *__restrict__ dout,
                                                            float *__restrict__ dvec,
-                                                           float4 *__restrict__ dq_acc,
+                                                           float4 *__restrict__ acc,
+                                                           long long n4_zero,
                                                            float *__restrict__ dbias, int nbias,
                                                            int T, int H) {
   grid_dep_wait();    // the forward's outputs are complete (a no-op when launched without overlap)
@@ -243,14 +246,14 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
   auto dot8 = [](uint4 a, uint4 b) {
     const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
     const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
-    float acc = 0.f;
+    float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(b2[i]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+      s = fmaf(x.x, y.x, s);
+      s = fmaf(x.y, y.y, s);
     }
-    return acc;
+    return s;
   };
   // Row groups of RPW rows; each warp takes two groups per step so that four 16-byte loads per
   // lane are in flight.
@@ -272,42 +275,438 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
       if (v1) dvec[(r1 % H) * (long long)T + r1 / H] = s1;
     }
   }
-  const long long n4 = nrows * (D / 4);
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   long long i = gtid;
-  for (; i + 3 * nthreads < n4; i += 4 * nthreads) {
-    dq_acc[i] = z;
-    dq_acc[i + nthreads] = z;
-    dq_acc[i + 2 * nthreads] = z;
-    dq_acc[i + 3 * nthreads] = z;
+  for (; i + 3 * nthreads < n4_zero; i += 4 * nthreads) {
+    acc[i] = z;
+    acc[i + nthreads] = z;
+    acc[i + 2 * nthreads] = z;
+    acc[i + 3 * nthreads] = z;
   }
-  for (; i < n4; i += nthreads) dq_acc[i] = z;
+  for (; i < n4_zero; i += nthreads) acc[i] = z;
 }
 
-// dq = bf16(dq_acc * softmax_scale): eight accumulator values in, one 16-byte store out per
-// thread step; n8 = element count / 8 (the element count is a multiple of 64).
-__global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const float4 *__restrict__ acc,
-                                                             uint4 *__restrict__ dq, float scale,
-                                                             long long n8) {
-  grid_dep_wait();  // the accumulator is complete (a no-op when launched without overlap)
+// out = bf16(acc * scale) over up to three segments (dQ; dK and dV when query heads share
+// key/value heads): eight accumulator values in, one 16-byte store out per thread step; each
+// segment's n8 = element count / 8 (element counts are multiples of 64).
+struct FinishSegs {
+  const float4 *acc[3];
+  uint4 *out[3];
+  float scale[3];
+  long long n8[3];
+  int nseg;
+};
+__global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const FinishSegs f) {
+  grid_dep_wait();  // the accumulators are complete (a no-op when launched without overlap)
   const long long nthreads = (long long)gridDim.x * blockDim.x;
-  long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  auto cvt = [scale](float4 a, float4 b) {
-    uint4 o;
-    o.x = pack_bf16x2(a.x * scale, a.y * scale);
-    o.y = pack_bf16x2(a.z * scale, a.w * scale);
-    o.z = pack_bf16x2(b.x * scale, b.y * scale);
-    o.w = pack_bf16x2(b.z * scale, b.w * scale);
-    return o;
-  };
-  for (; i + nthreads < n8; i += 2 * nthreads) {
-    const float4 a0 = acc[2 * i], b0 = acc[2 * i + 1];
-    const float4 a1 = acc[2 * (i + nthreads)], b1 = acc[2 * (i + nthreads) + 1];
-    dq[i] = cvt(a0, b0);
-    dq[i + nthreads] = cvt(a1, b1);
+  for (int sg = 0; sg < f.nseg; ++sg) {
+    const float4 *acc = f.acc[sg];
+    uint4 *dq = f.out[sg];
+    const float scale = f.scale[sg];
+    const long long n8 = f.n8[sg];
+    long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    auto cvt = [scale](float4 a, float4 b) {
+      uint4 o;
+      o.x = pack_bf16x2(a.x * scale, a.y * scale);
+      o.y = pack_bf16x2(a.z * scale, a.w * scale);
+      o.z = pack_bf16x2(b.x * scale, b.y * scale);
+      o.w = pack_bf16x2(b.z * scale, b.w * scale);
+      return o;
+    };
+    for (; i + nthreads < n8; i += 2 * nthreads) {
+      const float4 a0 = acc[2 * i], b0 = acc[2 * i + 1];
+      const float4 a1 = acc[2 * (i + nthreads)], b1 = acc[2 * (i + nthreads) + 1];
+      dq[i] = cvt(a0, b0);
+      dq[i + nthreads] = cvt(a1, b1);
+    }
+    if (i < n8) dq[i] = cvt(acc[2 * i], acc[2 * i + 1]);
   }
-  if (i < n8) dq[i] = cvt(acc[2 * i], acc[2 * i + 1]);
 }
+
+// dK = dV = 0 for the keys of documents without queries (cross-attention): no backward item
+// covers them. One block per document; the others exit at once.
+__global__ void __launch_bounds__(256) fat_zero_unseen_keys_kernel(const int32_t *cu_q,
+                                                                   const int32_t *cu_k, int Tk,
+                                                                   int row_elems, uint4 *dk,
+                                                                   uint4 *dv) {
+  const int doc = blockIdx.x;
+  const int q0 = __ldg(cu_q + doc), q1 = __ldg(cu_q + doc + 1);
+  const int k0 = __ldg(cu_k + doc), k1 = __ldg(cu_k + doc + 1);
+  if (q1 != q0 || k0 < 0 || k1 > Tk || k1 <= k0) return;
+  const long long n16 = (long long)(k1 - k0) * row_elems / 8;  // 16-byte units
+  const long long base = (long long)k0 * row_elems / 8;
+  for (long long i = threadIdx.x; i < n16; i += blockDim.x) {
+    dk[base + i] = make_uint4(0u, 0u, 0u, 0u);
+    dv[base + i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// ---- the generalised problem every entry point is lowered to ------------------------------
+namespace fat {
+namespace {
+
+struct XShape {
+  int Tq, Tk, n, maxq, maxk, Hq, Hkv, d;
+  cudaStream_t stream;
+};
+
+int to_xshape(const fat_shape_t *sh, XShape *x) {
+  int rc = check_shape(sh);
+  if (rc) return rc;
+  *x = XShape{sh->total_tokens, sh->total_tokens, sh->num_seqs, sh->max_seqlen, sh->max_seqlen,
+              sh->num_heads, sh->num_heads, sh->head_dim, static_cast<cudaStream_t>(sh->stream)};
+  return FAT_OK;
+}
+
+int to_xshape(const fat_xshape_t *xs, XShape *x) {
+  if (!xs) return FAT_EINVAL_NULL;
+  if (xs->total_q < 0 || xs->total_k < 0 || xs->num_seqs < 0 || xs->max_seqlen_q < 0 ||
+      xs->max_seqlen_k < 0 || xs->num_heads_q <= 0 || xs->num_heads_kv <= 0 ||
+      xs->num_heads_q % xs->num_heads_kv != 0)
+    return FAT_EINVAL_SHAPE;
+  if (xs->head_dim != 64 && xs->head_dim != 128) return FAT_EINVAL_SHAPE;
+  if ((long long)xs->total_q * xs->num_heads_q * xs->head_dim > (1LL << 40) ||
+      (long long)xs->total_k * xs->num_heads_kv * xs->head_dim > (1LL << 40))
+    return FAT_EINVAL_SHAPE;
+  if (xs->num_heads_q > 65535 || xs->num_seqs > 65535) return FAT_EUNSUPPORTED;
+  *x = XShape{xs->total_q, xs->total_k, xs->num_seqs, xs->max_seqlen_q, xs->max_seqlen_k,
+              xs->num_heads_q, xs->num_heads_kv, xs->head_dim,
+              static_cast<cudaStream_t>(xs->stream)};
+  return FAT_OK;
+}
+
+SeqParams seq_params(const XShape &x, const int32_t *cu_q, const int32_t *cu_k) {
+  SeqParams s{};
+  s.cu_seqlens = cu_q;
+  s.cu_seqlens_k = cu_k;
+  s.num_seqs = x.n;
+  s.num_heads = x.Hq;
+  s.total_tokens = x.Tq;
+  s.max_seqlen = x.maxq;
+  s.num_heads_kv = x.Hkv;
+  s.total_k = x.Tk;
+  s.max_seqlen_k = x.maxk;
+  s.group = x.Hq / x.Hkv;
+  return s;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Backward workspace: fp32 dQ accumulator [Tq, Hq, d]; when query heads share key/value heads,
+// fp32 dK and dV accumulators [Tk, Hkv, d]; then D [Hq, Tq]. Each 256-byte aligned; the
+// accumulators form one contiguous region (zeroed by the preprocess).
+struct WsLayout {
+  size_t dk, dv, dvec, zero_bytes, total;
+};
+WsLayout ws_layout(const XShape &x) {
+  WsLayout l{};
+  const size_t a = align256((size_t)x.Tq * x.Hq * x.d * 4);
+  const size_t b = x.Hq != x.Hkv ? align256((size_t)x.Tk * x.Hkv * x.d * 4) : 0;
+  l.dk = a;
+  l.dv = a + b;
+  l.dvec = a + 2 * b;
+  l.zero_bytes = a + 2 * b;
+  l.total = l.dvec + align256((size_t)x.Tq * x.Hq * 4);
+  return l;
+}
+
+struct WorkspaceView {
+  float *dq_acc, *dk_acc, *dv_acc, *dvec;
+  size_t zero_bytes;
+};
+int check_workspace(const XShape &x, const void *ws, size_t bytes, WorkspaceView *view) {
+  const WsLayout l = ws_layout(x);
+  if (!ws && l.total) return FAT_EINVAL_NULL;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return FAT_EINVAL_SHAPE;
+  if (bytes < l.total) return FAT_EINVAL_SHAPE;
+  char *base = static_cast<char *>(const_cast<void *>(ws));
+  view->dq_acc = reinterpret_cast<float *>(base);
+  view->dk_acc = x.Hq != x.Hkv ? reinterpret_cast<float *>(base + l.dk) : nullptr;
+  view->dv_acc = x.Hq != x.Hkv ? reinterpret_cast<float *>(base + l.dv) : nullptr;
+  view->dvec = reinterpret_cast<float *>(base + l.dvec);
+  view->zero_bytes = l.zero_bytes;
+  return FAT_OK;
+}
+
+int launch_rc(const char *what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return FAT_OK;
+  set_last_error(what, (int)e, cudaGetErrorString(e));
+  return FAT_ECUDA;
+}
+
+void fill_runtime_knobs(long long *timeout_ns, int *debug_flags) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *timeout_ns = g_timeout_ns;
+  *debug_flags = g_debug_flags;
+}
+
+// Split-key forward workspace: normalised partial outputs fp32 [splits, Tq, Hq, d], then
+// partial lse fp32 [splits, Hq, Tq], each 256-byte aligned.
+size_t splitkv_bytes(const XShape &x, int splits) {
+  return align256((size_t)splits * x.Tq * x.Hq * x.d * 4) + align256((size_t)splits * x.Hq * x.Tq * 4);
+}
+
+// Number of key splits: enough blocks for about two per SM when the rows alone give fewer, each
+// split keeping at least two key tiles, at most 64.
+int auto_splits(const XShape &x) {
+  const long long base = (long long)((x.maxq + 255) / 256) * x.Hq * x.n;
+  const int sms = sm_count() > 0 ? sm_count() : 152;
+  const int nkt = (x.maxk + 127) / 128;
+  if (base <= 0 || base >= sms || nkt < 4) return 1;
+  long long want = (2LL * sms + base - 1) / base;
+  want = std::min<long long>(want, nkt / 2);
+  want = std::min<long long>(want, 64);
+  return (int)std::max<long long>(want, 1);
+}
+
+int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
+             const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+             const float *alibi_slopes, const int32_t *cu_q, const int32_t *cu_k, int causal,
+             float softmax_scale, void *out, float *lse, int splits, void *workspace,
+             size_t workspace_bytes) {
+  if (!q || !k || !v || !cu_q || !cu_k || !out) return FAT_EINVAL_NULL;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(cu_q) ||
+      misaligned(cu_k) || misaligned(bias_table) || misaligned(alibi_slopes) || misaligned(lse))
+    return FAT_EINVAL_SHAPE;
+  FwdParams p{};
+  int rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (fwd_smem_bytes(x.d, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  if (splits < 1 || splits > 64 || (long long)x.n * splits > 65535) return FAT_EUNSUPPORTED;
+  if (splits > 1) {
+    if (!workspace) return FAT_EINVAL_NULL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        workspace_bytes < splitkv_bytes(x, splits))
+      return FAT_EINVAL_SHAPE;
+  }
+  if (x.Tq == 0 || x.n == 0 || x.maxq == 0) return FAT_OK;
+  rc = device_error_ptr(&p.err);
+  if (rc) return rc;
+  p.seq = seq_params(x, cu_q, cu_k);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  fill_runtime_knobs(&p.timeout_ns, &p.debug_flags);
+  p.kv_splits = splits;
+  const int nkt = (x.maxk + 127) / 128;
+  p.split_tiles = splits == 1 ? (1 << 30) : (nkt + splits - 1) / splits;
+  if (splits > 1) {
+    char *base = static_cast<char *>(workspace);
+    p.o_part = reinterpret_cast<float *>(base);
+    p.lse_part = reinterpret_cast<float *>(
+        base + align256((size_t)splits * x.Tq * x.Hq * x.d * 4));
+  }
+  rc = cuda_rc(launch_fwd(p, x.d, q, k, v, x.stream));
+  if (rc || splits == 1) return rc;
+  return cuda_rc(launch_fwd_combine(p, x.d, x.stream));
+}
+
+int check_bwd_args_x(const XShape &x, const void *q, const void *k, const void *v,
+                     const float *bias_table, int num_buckets, int max_distance,
+                     int bidirectional, const float *alibi_slopes, const int32_t *cu_q,
+                     const int32_t *cu_k, const void *out, const float *lse, const void *dout,
+                     const void *dq, const void *dk, const void *dv,
+                     const float *dbias_table) {
+  if (!q || !k || !v || !cu_q || !cu_k || !out || !lse || !dout || !dq || !dk || !dv)
+    return FAT_EINVAL_NULL;
+  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
+      misaligned(dq) || misaligned(dk) || misaligned(dv) || misaligned(lse) ||
+      misaligned(cu_q) || misaligned(cu_k) || misaligned(bias_table) ||
+      misaligned(alibi_slopes) || misaligned(dbias_table))
+    return FAT_EINVAL_SHAPE;
+  BiasParams b{};
+  int rc = fill_bias(&b, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (bwd_smem_bytes(x.d, b.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  return FAT_OK;
+}
+
+int bwd_preprocess_impl(const XShape &x, const void *out, const void *dout, void *workspace,
+                        size_t workspace_bytes, float *dbias_table, int num_buckets,
+                        bool overlap_previous) {
+  if (!out || !dout) return FAT_EINVAL_NULL;
+  if (misaligned(out) || misaligned(dout) || misaligned(dbias_table)) return FAT_EINVAL_SHAPE;
+  if (dbias_table && (num_buckets < 2 || num_buckets > 256)) return FAT_EINVAL_BUCKETS;
+  WorkspaceView ws{};
+  int rc = check_workspace(x, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  const int T = x.Tq, H = x.Hq, d = x.d;
+  const int nbias = dbias_table ? num_buckets * H : 0;
+  const long long n4 = (long long)(ws.zero_bytes / 16);
+  if (T == 0 && n4 == 0) {
+    if (!nbias) return FAT_OK;
+    const cudaError_t e = cudaMemsetAsync(dbias_table, 0, sizeof(float) * nbias, x.stream);
+    if (e != cudaSuccess) set_last_error("cudaMemsetAsync(dbias_table)", (int)e, cudaGetErrorString(e));
+    return cuda_rc((int)e);
+  }
+  const long long rows = (long long)T * H;
+  // Enough warps for every (token, head) row group and the zeroing, at most eight 256-thread
+  // blocks per SM.
+  const long long want = std::max<long long>((rows + 63) / 64, (n4 + 1023) / 1024);
+  const int blocks = (int)std::max<long long>(1, std::min<long long>(want, 152LL * 8));
+  const auto *o = static_cast<const uint4 *>(out);
+  const auto *g = static_cast<const uint4 *>(dout);
+  float4 *acc4 = reinterpret_cast<float4 *>(ws.dq_acc);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = x.stream;
+  if (overlap_previous) {  // it waits for the previous grid before touching memory
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e =
+      d == 64 ? cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<64>, o, g, ws.dvec, acc4, n4,
+                                   dbias_table, nbias, T, H)
+              : cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<128>, o, g, ws.dvec, acc4, n4,
+                                   dbias_table, nbias, T, H);
+  if (e != cudaSuccess) {
+    set_last_error("backward preprocess launch", (int)e, cudaGetErrorString(e));
+    return FAT_ECUDA;
+  }
+  return launch_rc("backward preprocess launch");
+}
+
+int bwd_main_impl(const XShape &x, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_q, const int32_t *cu_k,
+                  int causal, float softmax_scale, const float *lse, const void *dout,
+                  void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                  float *dbias_table, bool overlap_previous) {
+  if (!q || !k || !v || !cu_q || !cu_k || !lse || !dout || !dk || !dv) return FAT_EINVAL_NULL;
+  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dout) || misaligned(dk) ||
+      misaligned(dv) || misaligned(lse) || misaligned(cu_q) || misaligned(cu_k) ||
+      misaligned(bias_table) || misaligned(alibi_slopes) || misaligned(dbias_table))
+    return FAT_EINVAL_SHAPE;
+  BwdParams p{};
+  int rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  if (rc) return rc;
+  if (bwd_smem_bytes(x.d, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  WorkspaceView ws{};
+  rc = check_workspace(x, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  if (x.Tq == 0 || x.Tk == 0 || x.n == 0 || x.maxq == 0 || x.maxk == 0) return FAT_OK;
+  rc = device_error_ptr(&p.err);
+  if (rc) return rc;
+  p.seq = seq_params(x, cu_q, cu_k);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.scale = softmax_scale;
+  p.lse = lse;
+  p.dvec = ws.dvec;
+  p.dq_acc = ws.dq_acc;
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.dk_acc = ws.dk_acc;
+  p.dv_acc = ws.dv_acc;
+  p.dbias = dbias_table;
+  fill_runtime_knobs(&p.timeout_ns, &p.debug_flags);
+  return cuda_rc(launch_bwd(p, x.d, q, k, v, dout, x.stream, overlap_previous));
+}
+
+int bwd_finalize_impl(const XShape &x, const void *workspace, size_t workspace_bytes,
+                      float softmax_scale, void *dq, void *dk, void *dv, bool overlap_previous) {
+  if (!dq) return FAT_EINVAL_NULL;
+  if (misaligned(dq)) return FAT_EINVAL_SHAPE;
+  WorkspaceView ws{};
+  int rc = check_workspace(x, workspace, workspace_bytes, &ws);
+  if (rc) return rc;
+  FinishSegs f{};
+  long long most = 0;
+  auto add = [&](const float *acc, void *dst, float scale, long long n) {
+    if (n == 0) return;
+    f.acc[f.nseg] = reinterpret_cast<const float4 *>(acc);
+    f.out[f.nseg] = static_cast<uint4 *>(dst);
+    f.scale[f.nseg] = scale;
+    f.n8[f.nseg] = n / 8;
+    most = std::max(most, n / 8);
+    ++f.nseg;
+  };
+  add(ws.dq_acc, dq, softmax_scale, (long long)x.Tq * x.Hq * x.d);
+  if (ws.dk_acc) {  // query heads share key/value heads: dK (already scaled) and dV
+    if (!dk || !dv) return FAT_EINVAL_NULL;
+    if (misaligned(dk) || misaligned(dv)) return FAT_EINVAL_SHAPE;
+    add(ws.dk_acc, dk, 1.0f, (long long)x.Tk * x.Hkv * x.d);
+    add(ws.dv_acc, dv, 1.0f, (long long)x.Tk * x.Hkv * x.d);
+  }
+  if (f.nseg == 0) return FAT_OK;
+  const int blocks = (int)std::min<long long>((most + 255) / 256, 152LL * 8);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = x.stream;
+  if (overlap_previous) {  // programmatic dependent launch on the main backward grid
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fat_bwd_finish_kernel, f);
+  if (e != cudaSuccess) {
+    set_last_error("backward finalize launch", (int)e, cudaGetErrorString(e));
+    return FAT_ECUDA;
+  }
+  return launch_rc("backward finalize launch");
+}
+
+int bwd_impl(const XShape &x, const void *q, const void *k, const void *v,
+             const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+             const float *alibi_slopes, const int32_t *cu_q, const int32_t *cu_k, int causal,
+             float softmax_scale, const void *out, const float *lse, const void *dout,
+             void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
+             float *dbias_table) {
+  // validate everything before enqueueing anything
+  int rc = check_bwd_args_x(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                            alibi_slopes, cu_q, cu_k, out, lse, dout, dq, dk, dv, dbias_table);
+  if (rc) return rc;
+  {
+    WorkspaceView ws{};
+    rc = check_workspace(x, workspace, workspace_bytes, &ws);
+    if (rc) return rc;
+  }
+  rc = bwd_preprocess_impl(x, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
+                           true);
+  if (rc) return rc;
+  // All three grids are launched as programmatic dependents of the grid before them: each is
+  // scheduled while that grid drains and waits for its writes in-kernel (the preprocessing grid
+  // before it touches memory; the main grid before it reads D or touches the accumulators).
+  rc = bwd_main_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                     alibi_slopes, cu_q, cu_k, causal, softmax_scale, lse, dout, workspace,
+                     workspace_bytes, dk, dv, dbias_table, true);
+  if (rc) return rc;
+  rc = bwd_finalize_impl(x, workspace, workspace_bytes, softmax_scale, dq, dk, dv, true);
+  if (rc || cu_q == cu_k || x.Tk == 0 || x.n == 0) return rc;
+  // own key sequences: keys of a document without queries get zero gradients
+  fat_zero_unseen_keys_kernel<<<x.n, 256, 0, x.stream>>>(cu_q, cu_k, x.Tk, x.Hkv * x.d,
+                                                         static_cast<uint4 *>(dk),
+                                                         static_cast<uint4 *>(dv));
+  return launch_rc("unseen-key zeroing launch");
+}
+
+}  // namespace
+
+int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                   const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                   const float *alibi_slopes, const int32_t *cu_seqlens, const void *out,
+                   const float *lse, const void *dout, const void *dq, const void *dk,
+                   const void *dv, const float *dbias_table) {
+  XShape x{};
+  int rc = to_xshape(sh, &x);
+  if (rc) return rc;
+  return check_bwd_args_x(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                          alibi_slopes, cu_seqlens, cu_seqlens, out, lse, dout, dq, dk, dv,
+                          dbias_table);
+}
+
+}  // namespace fat
 
 // ---- C ABI -------------------------------------------------------------------------------------
 extern "C" {
@@ -361,204 +760,72 @@ int fat_attn_fwd(const fat_shape_t *sh, const void *q, const void *k, const void
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
                  float softmax_scale, void *out, float *lse) {
-  int rc = check_shape(sh);
+  XShape x{};
+  int rc = to_xshape(sh, &x);
   if (rc) return rc;
-  if (!q || !k || !v || !cu_seqlens || !out) return FAT_EINVAL_NULL;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) ||
-      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
-      misaligned(lse))
-    return FAT_EINVAL_SHAPE;
-  FwdParams p{};
-  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
+  return fwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens, cu_seqlens, causal, softmax_scale, out, lse, 1, nullptr, 0);
+}
+
+int fat_xattn_fwd(const fat_xshape_t *xs, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_seqlens_q,
+                  const int32_t *cu_seqlens_k, int causal, float softmax_scale, void *out,
+                  float *lse) {
+  XShape x{};
+  int rc = to_xshape(xs, &x);
   if (rc) return rc;
-  if (fwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
-  if (sh->total_tokens == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0) return FAT_OK;
-  rc = device_error_ptr(&p.err);
+  return fwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens_q, cu_seqlens_k, causal, softmax_scale, out, lse, 1, nullptr, 0);
+}
+
+int fat_xattn_splitkv_num_splits(const fat_xshape_t *xs) {
+  XShape x{};
+  if (to_xshape(xs, &x)) return 1;
+  return auto_splits(x);
+}
+
+size_t fat_xattn_splitkv_workspace_size(const fat_xshape_t *xs, int num_splits) {
+  XShape x{};
+  if (to_xshape(xs, &x) || num_splits < 1 || num_splits > 64) return 0;
+  return num_splits == 1 ? 0 : splitkv_bytes(x, num_splits);
+}
+
+int fat_xattn_fwd_splitkv(const fat_xshape_t *xs, const void *q, const void *k, const void *v,
+                          const float *bias_table, int num_buckets, int max_distance,
+                          int bidirectional, const float *alibi_slopes,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int causal,
+                          float softmax_scale, int num_splits, void *workspace,
+                          size_t workspace_bytes, void *out, float *lse) {
+  XShape x{};
+  int rc = to_xshape(xs, &x);
   if (rc) return rc;
-  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens, sh->max_seqlen};
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = softmax_scale * kLog2e;
-  p.out = static_cast<__nv_bfloat16 *>(out);
-  p.lse = lse;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    p.timeout_ns = g_timeout_ns;
-    p.debug_flags = g_debug_flags;
-  }
-  return cuda_rc(launch_fwd(p, sh->head_dim, sh->max_seqlen, q, k, v,
-                            static_cast<cudaStream_t>(sh->stream)));
+  return fwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens_q, cu_seqlens_k, causal, softmax_scale, out, lse, num_splits,
+                  workspace, workspace_bytes);
 }
 
 size_t fat_attn_bwd_workspace_size(const fat_shape_t *sh) {
-  if (check_shape(sh)) return 0;
-  const size_t T = (size_t)sh->total_tokens, H = (size_t)sh->num_heads, d = (size_t)sh->head_dim;
-  const size_t a = (T * H * d * 4 + 255) & ~(size_t)255;
-  const size_t b = (T * H * 4 + 255) & ~(size_t)255;
-  return a + b;
+  XShape x{};
+  if (to_xshape(sh, &x)) return 0;
+  return ws_layout(x).total;
 }
 
-namespace {
-struct WorkspaceView {
-  float *dq_acc;
-  float *dvec;
-};
-int check_workspace(const fat_shape_t *sh, const void *ws, size_t bytes, WorkspaceView *view) {
-  const size_t need = fat_attn_bwd_workspace_size(sh);
-  if (!ws && need) return FAT_EINVAL_NULL;
-  if (reinterpret_cast<uintptr_t>(ws) & 255u) return FAT_EINVAL_SHAPE;
-  if (bytes < need) return FAT_EINVAL_SHAPE;
-  const size_t T = (size_t)sh->total_tokens, H = (size_t)sh->num_heads, d = (size_t)sh->head_dim;
-  view->dq_acc = static_cast<float *>(const_cast<void *>(ws));
-  view->dvec = reinterpret_cast<float *>(static_cast<char *>(const_cast<void *>(ws)) +
-                                         ((T * H * d * 4 + 255) & ~(size_t)255));
-  return FAT_OK;
+size_t fat_xattn_bwd_workspace_size(const fat_xshape_t *xs) {
+  XShape x{};
+  if (to_xshape(xs, &x)) return 0;
+  return ws_layout(x).total;
 }
-bool empty_problem(const fat_shape_t *sh) {
-  return sh->total_tokens == 0 || sh->num_seqs == 0 || sh->max_seqlen == 0;
-}
-int launch_rc(const char *what) {
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) return FAT_OK;
-  set_last_error(what, (int)e, cudaGetErrorString(e));
-  return FAT_ECUDA;
-}
-}  // namespace
-
-namespace {
-int bwd_preprocess_impl(const fat_shape_t *sh, const void *out, const void *dout, void *workspace,
-                        size_t workspace_bytes, float *dbias_table, int num_buckets,
-                        bool overlap_previous) {
-  int rc = check_shape(sh);
-  if (rc) return rc;
-  if (!out || !dout) return FAT_EINVAL_NULL;
-  if (misaligned(out) || misaligned(dout) || misaligned(dbias_table)) return FAT_EINVAL_SHAPE;
-  if (dbias_table && (num_buckets < 2 || num_buckets > 256)) return FAT_EINVAL_BUCKETS;
-  WorkspaceView ws{};
-  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
-  if (rc) return rc;
-  cudaStream_t stream = static_cast<cudaStream_t>(sh->stream);
-  const int T = sh->total_tokens, H = sh->num_heads, d = sh->head_dim;
-  const int nbias = dbias_table ? num_buckets * H : 0;
-  if (T == 0) {
-    if (!nbias) return FAT_OK;
-    const cudaError_t e = cudaMemsetAsync(dbias_table, 0, sizeof(float) * nbias, stream);
-    if (e != cudaSuccess) set_last_error("cudaMemsetAsync(dbias_table)", (int)e, cudaGetErrorString(e));
-    return cuda_rc((int)e);
-  }
-  const long long rows = (long long)T * H;
-  // Enough warps for every (token, head) row group, at most eight 256-thread blocks per SM.
-  const int blocks = (int)std::min<long long>((rows + 63) / 64, 152LL * 8);
-  const auto *o = static_cast<const uint4 *>(out);
-  const auto *g = static_cast<const uint4 *>(dout);
-  float4 *acc4 = reinterpret_cast<float4 *>(ws.dq_acc);
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  if (overlap_previous) {  // it waits for the previous grid before touching memory
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  const cudaError_t e =
-      d == 64 ? cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<64>, o, g, ws.dvec, acc4, dbias_table,
-                                   nbias, T, H)
-              : cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<128>, o, g, ws.dvec, acc4,
-                                   dbias_table, nbias, T, H);
-  if (e != cudaSuccess) {
-    set_last_error("backward preprocess launch", (int)e, cudaGetErrorString(e));
-    return FAT_ECUDA;
-  }
-  return launch_rc("backward preprocess launch");
-}
-}  // namespace
 
 int fat_attn_bwd_preprocess(const fat_shape_t *sh, const void *out, const void *dout,
                             void *workspace, size_t workspace_bytes, float *dbias_table,
                             int num_buckets) {
-  return bwd_preprocess_impl(sh, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
+  XShape x{};
+  int rc = to_xshape(sh, &x);
+  if (rc) return rc;
+  return bwd_preprocess_impl(x, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
                              false);
 }
-
-namespace {
-int bwd_main_impl(const fat_shape_t *sh, const void *q, const void *k, const void *v,
-                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
-                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
-                  float softmax_scale, const float *lse, const void *dout, void *workspace,
-                  size_t workspace_bytes, void *dk, void *dv, float *dbias_table,
-                  bool overlap_previous) {
-  int rc = check_shape(sh);
-  if (rc) return rc;
-  if (!q || !k || !v || !cu_seqlens || !lse || !dout || !dk || !dv) return FAT_EINVAL_NULL;
-  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dout) || misaligned(dk) ||
-      misaligned(dv) || misaligned(lse) || misaligned(cu_seqlens) || misaligned(bias_table) ||
-      misaligned(alibi_slopes) || misaligned(dbias_table))
-    return FAT_EINVAL_SHAPE;
-  BwdParams p{};
-  rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
-  if (rc) return rc;
-  if (bwd_smem_bytes(sh->head_dim, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
-  WorkspaceView ws{};
-  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
-  if (rc) return rc;
-  if (empty_problem(sh)) return FAT_OK;
-  rc = device_error_ptr(&p.err);
-  if (rc) return rc;
-  p.seq = SeqParams{cu_seqlens, sh->num_seqs, sh->num_heads, sh->total_tokens, sh->max_seqlen};
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = softmax_scale * kLog2e;
-  p.scale = softmax_scale;
-  p.lse = lse;
-  p.dvec = ws.dvec;
-  p.dq_acc = ws.dq_acc;
-  p.dk = static_cast<__nv_bfloat16 *>(dk);
-  p.dv = static_cast<__nv_bfloat16 *>(dv);
-  p.dbias = dbias_table;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    p.timeout_ns = g_timeout_ns;
-    p.debug_flags = g_debug_flags;
-  }
-  return cuda_rc(launch_bwd(p, sh->head_dim, sh->max_seqlen, q, k, v, nullptr, dout,
-                           static_cast<cudaStream_t>(sh->stream), overlap_previous));
-}
-
-int bwd_finalize_impl(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
-                      float softmax_scale, void *dq, bool overlap_previous) {
-  int rc = check_shape(sh);
-  if (rc) return rc;
-  if (!dq) return FAT_EINVAL_NULL;
-  if (misaligned(dq)) return FAT_EINVAL_SHAPE;
-  WorkspaceView ws{};
-  rc = check_workspace(sh, workspace, workspace_bytes, &ws);
-  if (rc) return rc;
-  const long long n8 = (long long)sh->total_tokens * sh->num_heads * sh->head_dim / 8;
-  if (n8 == 0) return FAT_OK;
-  const int blocks = (int)std::min<long long>((n8 + 255) / 256, 152LL * 8);
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = static_cast<cudaStream_t>(sh->stream);
-  if (overlap_previous) {  // programmatic dependent launch on the main backward grid
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fat_bwd_finish_kernel,
-                                           reinterpret_cast<const float4 *>(ws.dq_acc),
-                                           static_cast<uint4 *>(dq), softmax_scale, n8);
-  if (e != cudaSuccess) {
-    set_last_error("backward finalize launch", (int)e, cudaGetErrorString(e));
-    return FAT_ECUDA;
-  }
-  return launch_rc("backward finalize launch");
-}
-}  // namespace
 
 int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const void *v,
                       const float *bias_table, int num_buckets, int max_distance,
@@ -566,43 +833,22 @@ int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const
                       int causal, float softmax_scale, const float *lse, const void *dout,
                       void *workspace, size_t workspace_bytes, void *dk, void *dv,
                       float *dbias_table) {
-  return bwd_main_impl(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
-                       alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
-                       workspace_bytes, dk, dv, dbias_table, false);
+  XShape x{};
+  int rc = to_xshape(sh, &x);
+  if (rc) return rc;
+  return bwd_main_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
+                       alibi_slopes, cu_seqlens, cu_seqlens, causal, softmax_scale, lse, dout,
+                       workspace, workspace_bytes, dk, dv, dbias_table, false);
 }
 
 int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
                           float softmax_scale, void *dq) {
-  return bwd_finalize_impl(sh, workspace, workspace_bytes, softmax_scale, dq, false);
-}
-
-}  // extern "C"
-
-namespace fat {
-int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const void *v,
-                   const float *bias_table, int num_buckets, int max_distance, int bidirectional,
-                   const float *alibi_slopes, const int32_t *cu_seqlens, const void *out,
-                   const float *lse, const void *dout, const void *dq, const void *dk,
-                   const void *dv, const float *dbias_table) {
-  int rc = check_shape(sh);
+  XShape x{};
+  int rc = to_xshape(sh, &x);
   if (rc) return rc;
-  if (!q || !k || !v || !cu_seqlens || !out || !lse || !dout || !dq || !dk || !dv)
-    return FAT_EINVAL_NULL;
-  if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
-      misaligned(dq) || misaligned(dk) || misaligned(dv) || misaligned(lse) ||
-      misaligned(cu_seqlens) || misaligned(bias_table) || misaligned(alibi_slopes) ||
-      misaligned(dbias_table))
-    return FAT_EINVAL_SHAPE;
-  BiasParams b{};
-  rc = fill_bias(&b, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
-  if (rc) return rc;
-  if (bwd_smem_bytes(sh->head_dim, b.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
-  return FAT_OK;
+  return bwd_finalize_impl(x, workspace, workspace_bytes, softmax_scale, dq, nullptr, nullptr,
+                           false);
 }
-}  // namespace fat
-
-extern "C" {
 
 int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
@@ -610,26 +856,26 @@ int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void
                  float softmax_scale, const void *out, const float *lse, const void *dout,
                  void *workspace, size_t workspace_bytes, void *dq, void *dk, void *dv,
                  float *dbias_table) {
-  // validate everything before enqueueing anything
-  int rc = check_bwd_args(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
-                          alibi_slopes, cu_seqlens, out, lse, dout, dq, dk, dv, dbias_table);
+  XShape x{};
+  int rc = to_xshape(sh, &x);
   if (rc) return rc;
-  {
-    WorkspaceView ws{};
-    rc = check_workspace(sh, workspace, workspace_bytes, &ws);
-    if (rc) return rc;
-  }
-  rc = bwd_preprocess_impl(sh, out, dout, workspace, workspace_bytes, dbias_table, num_buckets,
-                           true);
+  return bwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens, cu_seqlens, causal, softmax_scale, out, lse, dout, workspace,
+                  workspace_bytes, dq, dk, dv, dbias_table);
+}
+
+int fat_xattn_bwd(const fat_xshape_t *xs, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_seqlens_q,
+                  const int32_t *cu_seqlens_k, int causal, float softmax_scale, const void *out,
+                  const float *lse, const void *dout, void *workspace, size_t workspace_bytes,
+                  void *dq, void *dk, void *dv, float *dbias_table) {
+  XShape x{};
+  int rc = to_xshape(xs, &x);
   if (rc) return rc;
-  // All three grids are launched as programmatic dependents of the grid before them: each is
-  // scheduled while that grid drains and waits for its writes in-kernel (the preprocessing grid
-  // before it touches memory; the main grid before it reads D or touches the accumulators).
-  rc = bwd_main_impl(sh, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
-                     alibi_slopes, cu_seqlens, causal, softmax_scale, lse, dout, workspace,
-                     workspace_bytes, dk, dv, dbias_table, true);
-  if (rc) return rc;
-  return bwd_finalize_impl(sh, workspace, workspace_bytes, softmax_scale, dq, true);
+  return bwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens_q, cu_seqlens_k, causal, softmax_scale, out, lse, dout, workspace,
+                  workspace_bytes, dq, dk, dv, dbias_table);
 }
 
 int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,

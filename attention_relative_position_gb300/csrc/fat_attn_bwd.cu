@@ -81,9 +81,11 @@ struct BwdCfg {
 
 // One unit of work of the persistent backward: a 128-key tile of one (document, head).
 struct WorkItem {
-  int kb, h, seq_start, L;
+  int kb, h, seq_start, L;  // key tile, query head, first query row and query count
+  int hk, seq_start_k, Lk;  // key/value head, first key row and key count
+  int shift;                // query p sits at key position p + shift (= Lk - L)
   int ks;    // first key of the tile (document-local)
-  int i0;    // first query tile walked (causal: the key tile's own)
+  int i0;    // first query tile walked (causal: the first that sees the key tile)
   int nq;    // number of query tiles walked
   int qrot;  // walk offset
 };
@@ -131,6 +133,37 @@ __device__ __forceinline__ void tmem_stw(uint32_t taddr, const uint32_t (&r)[W])
     tmem_st16(taddr, r);
   else
     tmem_st8(taddr, r);
+}
+
+// 16 channels of one key row of dK (times the softmax scale) and dV, fp32 from TMEM: stored as
+// bf16 when every query head has its own key/value head, else added into the fp32 accumulators
+// that the query heads of a group share (finished to bf16 by the finishing grid).
+__device__ __forceinline__ void store_dkdv_row(const BwdParams &p, size_t off,
+                                               const uint32_t (&a)[16], const uint32_t (&b)[16]) {
+  if (p.dk_acc == nullptr) {
+    uint32_t pa[8], pb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
+                          __uint_as_float(a[2 * i + 1]) * p.scale);
+      pb[i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+    }
+    uint4 *dk4 = reinterpret_cast<uint4 *>(p.dk + off);
+    dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+    dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+    uint4 *dv4 = reinterpret_cast<uint4 *>(p.dv + off);
+    dv4[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+    dv4[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      red_add_v4(p.dk_acc + off + 4 * i, __uint_as_float(a[4 * i]) * p.scale,
+                 __uint_as_float(a[4 * i + 1]) * p.scale, __uint_as_float(a[4 * i + 2]) * p.scale,
+                 __uint_as_float(a[4 * i + 3]) * p.scale);
+      red_add_v4(p.dv_acc + off + 4 * i, __uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
+                 __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
+    }
+  }
 }
 
 // P^T of one W-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
@@ -253,21 +286,30 @@ __global__ void __launch_bounds__(640, 1)
       const int kb = (int)(rank / n_dh);
       const long long rest = rank % n_dh;
       const int h = (int)(rest % H), doc = (int)(rest / H);
-      const int s0 = __ldg(p.seq.cu_seqlens + doc), s1 = __ldg(p.seq.cu_seqlens + doc + 1);
-      if (s0 < 0 || s1 > T || s1 < s0) {  // reported by whichever thread decodes the item
+      const DocSpan sp = doc_span(p.seq, doc);
+      if (!sp.ok) {  // reported by whichever thread decodes the item
         atomicOr(p.err, FAT_DEVERR_SEQLENS);
         continue;
       }
-      // key tiles of a document longer than max_seqlen lie beyond the item space: reported
-      if (kb == 0 && s1 - s0 > p.seq.max_seqlen) atomicOr(p.err, FAT_DEVERR_SEQLENS);
-      if (kb * 128 >= s1 - s0) continue;
+      // key tiles or query rows of a document longer than the bounds lie beyond the item
+      // space: reported
+      if (kb == 0 && (sp.lq > p.seq.max_seqlen || sp.lk > p.seq.max_seqlen_k))
+        atomicOr(p.err, FAT_DEVERR_SEQLENS);
+      if (kb * 128 >= sp.lk) continue;
       w.kb = kb;
       w.h = h;
-      w.seq_start = s0;
-      w.L = s1 - s0;
+      w.seq_start = sp.sq;
+      w.L = sp.lq;
+      w.hk = h / p.seq.group;
+      w.seq_start_k = sp.sk;
+      w.Lk = sp.lk;
+      w.shift = sp.shift;
       w.ks = kb * 128;
-      w.i0 = p.causal ? w.ks / C::BQ : 0;
+      // causal: query p sees key r iff r <= p + shift, so the first query of the tile's
+      // walk is ks - shift
+      w.i0 = p.causal ? max(0, w.ks - w.shift) / C::BQ : 0;
       w.nq = (w.L + C::BQ - 1) / C::BQ - w.i0;
+      if (w.nq <= 0) continue;  // no query of the document sees this key tile
       // query tiles are walked from a per-key-tile offset, so the key-tile CTAs of one head do
       // not all add into the same dQ rows at the same time
       w.qrot = w.nq > 0 ? kb % w.nq : 0;
@@ -355,8 +397,10 @@ __global__ void __launch_bounds__(640, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
         for (int b = 0; b < C::DB; ++b) {
-          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, first.h, first.seq_start + first.ks);
-          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, first.h, first.seq_start + first.ks);
+          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, first.hk,
+                      first.seq_start_k + first.ks);
+          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, first.hk,
+                      first.seq_start_k + first.ks);
         }
       }
 #pragma unroll
@@ -427,7 +471,7 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
             for (int k = 0; k < C::BQ / 32; ++k) {
               const int q = qs + lane + 32 * k;
-              s_lse2[lane + 32 * k] = lv0[k] * kLog2e;
+              s_lse2[lane + 32 * k] = lse_to_log2_stat(lv0[k]);
               s_dvec[lane + 32 * k] =
                   q < w.L ? __ldg(p.dvec + (size_t)w.h * T + w.seq_start + q) : 0.f;
             }
@@ -441,7 +485,7 @@ __global__ void __launch_bounds__(640, 1)
           for (int k = 0; k < C::BQ / 32; ++k) {
             const int q = qs + lane + 32 * k;
             const size_t idx = (size_t)w.h * T + w.seq_start + q;
-            lv[k] = q < w.L ? __ldg(p.lse + idx) * kLog2e : 0.f;
+            lv[k] = q < w.L ? lse_to_log2_stat(__ldg(p.lse + idx)) : 0.f;
             dv[k] = q < w.L ? __ldg(p.dvec + idx) : 0.f;
           }
           if (u > 0 && !warp_wait(qd_empty + st, (u - 1) & 1, wd)) {
@@ -477,8 +521,10 @@ __global__ void __launch_bounds__(640, 1)
             if (lane == 0) {
               mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
               for (int b = 0; b < C::DB; ++b) {
-                tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, w.h, w.seq_start + w.ks);
-                tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, w.h, w.seq_start + w.ks);
+                tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, w.hk,
+                            w.seq_start_k + w.ks);
+                tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, w.hk,
+                            w.seq_start_k + w.ks);
               }
             }
             last_kv = ii;
@@ -687,10 +733,13 @@ __global__ void __launch_bounds__(640, 1)
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
         }
+        // 64-byte swizzle (the tensor map's): chunk c of row `lane` sits at c ^ ((lane / 2) % 4),
+        // so that the eight rows a store wavefront serves hit eight different bank groups
         uint4 *dst = reinterpret_cast<uint4 *>(slice + lane * 64);
+        const int sw = (lane >> 1) & 3;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(vq[4 * c], vq[4 * c + 1], vq[4 * c + 2], vq[4 * c + 3]);
+          dst[c ^ sw] = make_uint4(vq[4 * c], vq[4 * c + 1], vq[4 * c + 2], vq[4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         // rows past the document end carry zeros (their dS is masked), rows past T are clipped
@@ -715,7 +764,7 @@ __global__ void __launch_bounds__(640, 1)
     FarBias fb = far_bias_dev(w.h, H, p.bias);
     do {
       const int krow = w.ks + r;
-      const bool row_valid = krow < w.L;
+      const bool row_valid = krow < w.Lk;
       float acc_pos = 0.f, acc_neg = 0.f;  // table-gradient sums of far tiles, this item
       bool new_head = false;
       float tcol_next = 0.f, slope_next = 0.f;
@@ -742,10 +791,10 @@ __global__ void __launch_bounds__(640, 1)
             if (has_slopes) slope_next = __ldg(p.bias.slopes + hn);
           }
         }
-        const int d0 = w.ks - qs;  // delta of (key row 0, query column 0)
+        const int d0 = w.ks - qs - w.shift;  // delta of (key row 0, query column 0)
         const bool need_mask =
-            (w.ks + 128 > w.L) || (qs + C::BQ > w.L) || (p.causal && d0 + 127 > 0);
-        const int lo_j = p.causal ? krow - qs : -1;
+            (w.ks + 128 > w.Lk) || (qs + C::BQ > w.L) || (p.causal && d0 + 127 > 0);
+        const int lo_j = p.causal ? krow - w.shift - qs : -1;  // first query column that sees it
         const int hi_j = row_valid ? w.L - qs : 0;
         // side: 0 = lookup table, 1 = positive far side, 2 = negative far side, 3 = no bias
         int side;
@@ -860,8 +909,7 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_after();
       {
         const int cb = wg * (D / 4);
-        __nv_bfloat16 *dkrow = p.dk + ((size_t)(w.seq_start + krow) * H + w.h) * D + cb;
-        __nv_bfloat16 *dvrow = p.dv + ((size_t)(w.seq_start + krow) * H + w.h) * D + cb;
+        const size_t kvrow = ((size_t)(w.seq_start_k + krow) * p.seq.num_heads_kv + w.hk) * D + cb;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t a[16], b[16];
@@ -873,21 +921,7 @@ __global__ void __launch_bounds__(640, 1)
             tc_fence_before();
             mbar_arrive(dkdv_free);
           }
-          uint32_t pa[8], pb[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
-                                __uint_as_float(a[2 * i + 1]) * p.scale);
-            pb[i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-          }
-          if (row_valid) {
-            uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 16 * c);
-            dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-            dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-            uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 16 * c);
-            dv4[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-            dv4[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
-          }
+          if (row_valid) store_dkdv_row(p, kvrow + 16 * c, a, b);
         }
       }
       // ---- table gradient of the item, then the next item's bias table (between two syncs
@@ -983,18 +1017,22 @@ __global__ void __launch_bounds__(640, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb = blockIdx.x, h = blockIdx.y, doc = blockIdx.z;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
-  const int seq_start = __ldg(p.seq.cu_seqlens + doc);
-  const int seq_end = __ldg(p.seq.cu_seqlens + doc + 1);
-  if (seq_start < 0 || seq_end > T || seq_end < seq_start) {
+  const DocSpan span = doc_span(p.seq, doc);
+  if (!span.ok) {
     if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
     return;
   }
-  const int L = seq_end - seq_start;
-  if (L > p.seq.max_seqlen && kb == 0 && tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+  const int seq_start = span.sq, L = span.lq;  // queries
+  const int seq_start_k = span.sk, Lk = span.lk, shift = span.shift;  // keys
+  const int hk = h / p.seq.group;
+  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && kb == 0 && tid == 0)
+    atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int ks = kb * 128;
-  if (ks >= L) return;
-  const int i0 = p.causal ? ks / C::BQ : 0;
+  if (ks >= Lk) return;
+  // causal: query p sees key r iff r <= p + shift, so the walk starts at query ks - shift
+  const int i0 = p.causal ? max(0, ks - shift) / C::BQ : 0;
   const int nq = (L + C::BQ - 1) / C::BQ - i0;
+  if (nq <= 0) return;  // no query of the document sees this key tile
   // Query tiles are walked starting at a per-CTA offset, so the key-tile CTAs of one head do not
   // all add into the same dQ rows at the same time (same-address reductions serialise in L2).
   const int qrot = nq > 0 ? kb % nq : 0;
@@ -1067,8 +1105,8 @@ __global__ void __launch_bounds__(640, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
         for (int b = 0; b < C::DB; ++b) {
-          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, h, seq_start + ks);
-          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, h, seq_start + ks);
+          tma_load_3d(&tm_k, kv_full, sK + b * C::KBLK, 64 * b, hk, seq_start_k + ks);
+          tma_load_3d(&tm_v, kv_full, sV + b * C::KBLK, 64 * b, hk, seq_start_k + ks);
         }
       }
 #pragma unroll
@@ -1119,7 +1157,7 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
       for (int k = 0; k < C::BQ / 32; ++k) {
         const int q = qs0 + lane + 32 * k;
-        s_lse2[lane + 32 * k] = lv0[k] * kLog2e;
+        s_lse2[lane + 32 * k] = lse_to_log2_stat(lv0[k]);
         s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + (size_t)h * T + seq_start + q) : 0.f;
       }
       mbar_arrive(qd_full);
@@ -1133,7 +1171,7 @@ __global__ void __launch_bounds__(640, 1)
         for (int k = 0; k < C::BQ / 32; ++k) {
           const int q = qs + lane + 32 * k;
           const size_t idx = (size_t)h * T + seq_start + q;
-          lv[k] = q < L ? __ldg(p.lse + idx) * kLog2e : 0.f;
+          lv[k] = q < L ? lse_to_log2_stat(__ldg(p.lse + idx)) : 0.f;
           dv[k] = q < L ? __ldg(p.dvec + idx) : 0.f;
         }
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(qd_empty + st, (u - 1) & 1, wd))) break;
@@ -1292,7 +1330,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t ds_x = static_cast<uint32_t>((((c0 & 63) >> 3) ^ (r & 7)) << 4);
     const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
     const int krow = ks + r;
-    const bool row_valid = krow < L;
+    const bool row_valid = krow < Lk;
     const FarBias fb = far_bias_dev(h, H, p.bias);
     const bool has_slopes = p.bias.slopes != nullptr;
 
@@ -1313,10 +1351,12 @@ __global__ void __launch_bounds__(640, 1)
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
         }
+        // 64-byte swizzle (the tensor map's): chunk c of row `lane` sits at c ^ ((lane / 2) % 4)
         uint4 *dst = reinterpret_cast<uint4 *>(slice + lane * 64);
+        const int sw = (lane >> 1) & 3;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          dst[c ^ sw] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         // rows past the document end carry zeros (their dS is masked), rows past T are clipped
@@ -1345,9 +1385,9 @@ __global__ void __launch_bounds__(640, 1)
             __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
       if (!ok) break;
       tc_fence_after();
-      const int d0 = ks - qs;  // delta of (key row 0, query column 0)
-      const bool need_mask = (ks + 128 > L) || (qs + C::BQ > L) || (p.causal && d0 + 127 > 0);
-      const int lo_j = p.causal ? krow - qs : -1;
+      const int d0 = ks - qs - shift;  // delta of (key row 0, query column 0)
+      const bool need_mask = (ks + 128 > Lk) || (qs + C::BQ > L) || (p.causal && d0 + 127 > 0);
+      const int lo_j = p.causal ? krow - shift - qs : -1;  // first query column that sees it
       const int hi_j = row_valid ? L - qs : 0;
       // side: 0 = lookup table, 1 = positive far side, 2 = negative far side, 3 = no bias
       int side;
@@ -1462,33 +1502,16 @@ __global__ void __launch_bounds__(640, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, wd));
     if (ok) {
       tc_fence_after();
-      const bool valid = krow < L;
       const int cb = wg * (D / 4);
-      __nv_bfloat16 *dkrow = p.dk + ((size_t)(seq_start + krow) * H + h) * D + cb;
-      __nv_bfloat16 *dvrow = p.dv + ((size_t)(seq_start + krow) * H + h) * D + cb;
+      const size_t kvrow = ((size_t)(seq_start_k + krow) * p.seq.num_heads_kv + hk) * D + cb;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        uint32_t a[16];
-        tmem_ld16(tmem + lane_off + C::COL_DK + cb + 16 * c, a);
-        uint32_t pa[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
-                              __uint_as_float(a[2 * i + 1]) * p.scale);
-        if (valid) {
-          uint4 *dk4 = reinterpret_cast<uint4 *>(dkrow + 16 * c);
-          dk4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-          dk4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-        }
-        tmem_ld16(tmem + lane_off + C::COL_DV + cb + 16 * c, a);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-        if (valid) {
-          uint4 *dv4 = reinterpret_cast<uint4 *>(dvrow + 16 * c);
-          dv4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-          dv4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-        }
+        uint32_t a[16], b[16];
+        tmem_ld16_issue(tmem + lane_off + C::COL_DK + cb + 16 * c, a);
+        tmem_ld16_issue(tmem + lane_off + C::COL_DV + cb + 16 * c, b);
+        tmem_ld16_fence(a);
+        tmem_ld16_fence(b);
+        if (row_valid) store_dkdv_row(p, kvrow + 16 * c, a, b);
       }
     }
   }
@@ -1535,15 +1558,15 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
-int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, const void *out, const void *dout, cudaStream_t stream,
-               bool overlap_previous) {
-  (void)out;
+int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, const void *v,
+               const void *dout, cudaStream_t stream, bool overlap_previous) {
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  const int Tk = p.seq.total_k, Hkv = p.seq.num_heads_kv;
   const int bq = head_dim == 64 ? BwdCfg<64, 2>::BQ : BwdCfg<128, 2>::BQ;
-  if (make_tmap_thd(&mq, q, T, H, head_dim, bq) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
-      make_tmap_thd(&mv, v, T, H, head_dim, 128) || make_tmap_thd(&mdo, dout, T, H, head_dim, bq) ||
+  if (make_tmap_thd(&mq, q, T, H, head_dim, bq) || make_tmap_thd(&mk, k, Tk, Hkv, head_dim, 128) ||
+      make_tmap_thd(&mv, v, Tk, Hkv, head_dim, 128) ||
+      make_tmap_thd(&mdo, dout, T, H, head_dim, bq) ||
       make_tmap_thd_f32(&mdq, p.dq_acc, T, H, head_dim, 16, 32))
     return (int)cudaErrorInvalidValue;
   const size_t smem = bwd_smem_bytes(head_dim, p.bias.lut_len);
@@ -1551,7 +1574,7 @@ int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, 
   // Short documents with d = 64: the persistent kernel (one CTA per SM walking the items, so
   // the set-up and tail of one item overlap the next). Otherwise one CTA per key tile.
   BwdParams pp = p;
-  pp.nkb = (max_seqlen + 127) / 128;
+  pp.nkb = (p.seq.max_seqlen_k + 127) / 128;
   const bool persistent = head_dim == 64 && pp.nkb <= 64;
   const long long items = (long long)pp.nkb * H * p.seq.num_seqs;
   const int sms = sm_count();

@@ -21,6 +21,7 @@
 // d = 64 the two warpgroups take their exponential phases in turns (tile 0 of key tile j, then
 // tile 1 of key tile j, then tile 0 of key tile j + 1, ...): each finds the special-function
 // units to itself, and the other's logits and waits overlap it.
+#include <algorithm>
 #include <cstdio>
 
 #include "fat_attn_internal.cuh"
@@ -123,6 +124,31 @@ __device__ __forceinline__ void fwd_exp_pass(const uint32_t (&x)[4][32], uint64_
   }
 }
 
+// Rows that see no key (in this block's key range): out = 0 and lse = -inf, or, for a key range
+// of a split forward, a zero partial output with partial lse -inf. Threads thr, thr + nthr, ...
+// take rows row0 .. row0 + nrows - 1 (document-local) of query head h.
+template <int D>
+__device__ __forceinline__ void fwd_write_empty_rows(const FwdParams &p, int seq_start, int row0,
+                                                     int nrows, int h, int split,
+                                                     int thr = threadIdx.x,
+                                                     int nthr = blockDim.x) {
+  const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  for (int i = thr; i < nrows; i += nthr) {
+    const size_t row = (size_t)seq_start + row0 + i;
+    if (p.kv_splits == 1) {
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row * H + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse != nullptr) p.lse[(size_t)h * T + row] = -INFINITY;
+    } else {
+      float4 *dst = reinterpret_cast<float4 *>(p.o_part + (((size_t)split * T + row) * H + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.lse_part[((size_t)split * H + h) * T + row] = -INFINITY;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fat_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -133,32 +159,49 @@ __global__ void __launch_bounds__(384, 1)
   // shared array itself so every derived pointer stays a shared-memory pointer
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int doc = blockIdx.z, h = blockIdx.y;
+  const int doc = blockIdx.z / p.kv_splits, split = blockIdx.z % p.kv_splits, h = blockIdx.y;
+  const int hk = h / p.seq.group;             // key/value head read by query head h
   const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first when causal
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
 
-  const int seq_start = __ldg(p.seq.cu_seqlens + doc);
-  const int seq_end = __ldg(p.seq.cu_seqlens + doc + 1);
-  if (seq_start < 0 || seq_end > T || seq_end < seq_start) {
+  const DocSpan span = doc_span(p.seq, doc);
+  if (!span.ok) {
     if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
     return;
   }
-  const int L = seq_end - seq_start;
-  // a document longer than the caller's max_seqlen has rows no block covers: reported, once
-  if (L > p.seq.max_seqlen && blockIdx.x == 0 && tid == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+  const int seq_start = span.sq, L = span.lq, seq_start_k = span.sk, Lk = span.lk;
+  const int shift = span.shift;  // query p sits at key position p + shift
+  // a document longer than the caller's bounds has rows or keys no block covers: reported
+  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && blockIdx.x == 0 && split == 0 &&
+      tid == 0)
+    atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int q0 = qb * 256;
   if (q0 >= L) return;  // whole CTA, before any barrier or TMEM allocation
   const int ntile = (q0 + 128 < L) ? 2 : 1;
-  const int nkv_all = (L + 127) >> 7;
-  const int nkv0 = p.causal ? min((q0 >> 7) + 1, nkv_all) : nkv_all;
-  const int nkv1 = ntile == 2 ? (p.causal ? min((q0 >> 7) + 2, nkv_all) : nkv_all) : 0;
+  const int nkv_all = (Lk + 127) >> 7;
+  // Key tiles Q tile t sees: all of them, or (causal) those up to the key position of its last
+  // valid row; intersected with this block's key range [klo, khi) when the keys are split.
+  const int klo = split * p.split_tiles;
+  const int khi = min(nkv_all, klo + p.split_tiles);
+  auto visible = [&](int t) -> int {
+    if (!p.causal) return nkv_all;
+    const int last = min(L, q0 + 128 * t + 128) - 1 + shift;
+    return last < 0 ? 0 : min((last >> 7) + 1, nkv_all);
+  };
+  const int nkv0 = max(0, min(khi, visible(0)) - klo);
+  const int nkv1 = ntile == 2 ? max(0, min(khi, visible(1)) - klo) : 0;
   const int nkv_max = max(nkv0, nkv1);
+  if (nkv_max == 0) {  // no key for any row of the block (in this key range): empty rows
+    fwd_write_empty_rows<D>(p, seq_start, q0, min(L - q0, 256), h, split);
+    return;
+  }
   // Causal rows take their key tiles from the diagonal backwards: the first tile holds each
   // row's largest ALiBi bias, so the running max rarely grows afterwards. Stream position j
   // (the order of the K/V ring) holds key tile kt0 + kdir * j; Q tile t uses positions
   // [jbeg_t, jbeg_t + nkv_t).
-  const int kt0 = p.causal ? nkv_max - 1 : 0, kdir = p.causal ? -1 : 1;
+  const int kt0 = p.causal ? klo + nkv_max - 1 : klo, kdir = p.causal ? -1 : 1;
   const int jbeg0 = p.causal ? nkv_max - nkv0 : 0, jbeg1 = p.causal ? nkv_max - nkv1 : 0;
+  const int nissuers = (nkv0 > 0 ? 1 : 0) + (nkv1 > 0 ? 1 : 0);
 
   uint8_t *sQ = sm + C::OFF_Q, *sK = sm + C::OFF_K, *sV = sm + C::OFF_V;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
@@ -185,8 +228,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(v_full + s, 1);
-      mbar_init(k_empty + s, C::SEP_P ? ntile : 1);  // one release per MMA issuer
-      mbar_init(v_empty + s, C::SEP_P ? ntile : 1);
+      mbar_init(k_empty + s, C::SEP_P ? nissuers : 1);  // one release per MMA issuer
+      mbar_init(v_empty + s, C::SEP_P ? nissuers : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
@@ -211,10 +254,10 @@ __global__ void __launch_bounds__(384, 1)
                       seq_start + q0 + 128 * t);
       mbar_arrive_expect_tx(k_full, C::TILE);
       for (int b = 0; b < C::DB; ++b)
-        tma_load_3d(&tm_k, k_full, sK + b * C::BLK, 64 * b, h, seq_start + 128 * kt0);
+        tma_load_3d(&tm_k, k_full, sK + b * C::BLK, 64 * b, hk, seq_start_k + 128 * kt0);
       mbar_arrive_expect_tx(v_full, C::TILE);
       for (int b = 0; b < C::DB; ++b)
-        tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, h, seq_start + 128 * kt0);
+        tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, hk, seq_start_k + 128 * kt0);
     }
   }
   if (warp == 9) {
@@ -245,16 +288,16 @@ __global__ void __launch_bounds__(384, 1)
           if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, wd)) break;
           mbar_arrive_expect_tx(k_full + s, C::TILE);
           for (int b = 0; b < C::DB; ++b)
-            tma_load_3d(&tm_k, k_full + s, sK + s * C::TILE + b * C::BLK, 64 * b, h,
-                        seq_start + 128 * (kt0 + kdir * j));
+            tma_load_3d(&tm_k, k_full + s, sK + s * C::TILE + b * C::BLK, 64 * b, hk,
+                        seq_start_k + 128 * (kt0 + kdir * j));
 #pragma unroll
           for (int x = 0; x < C::NS; ++x)
             if (x == s) last_k[x] = u;
           if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, wd)) break;
           mbar_arrive_expect_tx(v_full + s, C::TILE);
           for (int b = 0; b < C::DB; ++b)
-            tma_load_3d(&tm_v, v_full + s, sV + s * C::TILE + b * C::BLK, 64 * b, h,
-                        seq_start + 128 * (kt0 + kdir * j));
+            tma_load_3d(&tm_v, v_full + s, sV + s * C::TILE + b * C::BLK, 64 * b, hk,
+                        seq_start_k + 128 * (kt0 + kdir * j));
 #pragma unroll
           for (int x = 0; x < C::NS; ++x)
             if (x == s) last_v[x] = u;
@@ -345,8 +388,8 @@ __global__ void __launch_bounds__(384, 1)
     // One issuing thread per Q tile, so neither tile's hand-offs wait behind the other's.
     // Each K/V stage is released once per active issuer (the barriers count ntile arrivals).
     const int t = warp - 9;
-    if (lane == 0 && t < ntile) {
-      const int nk = t == 0 ? nkv0 : nkv1;
+    const int nk = t == 0 ? nkv0 : nkv1;
+    if (lane == 0 && t < ntile && nk > 0) {
       const uint32_t dS_t = tmem + C::COL_S0 + 128 * t;
       const uint32_t dO_t = tmem + C::COL_O0 + C::O_STRIDE * t;
       const uint32_t aP_t = C::SEP_P ? tmem + C::COL_P0 + 64 * t : dS_t;
@@ -452,9 +495,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc_fence_after();
         const int ks = 128 * (kt0 + kdir * ((t == 0 ? jbeg0 : jbeg1) + j));
-        const int d0 = ks - qs;  // delta of (row 0, key 0) of the tile
-        const bool need_mask = (ks + 128 > L) || (p.causal && d0 + 127 > 0);
-        const int lim = min(L - ks, p.causal ? (qrow - ks + 1) : 128);
+        const int d0 = ks - qs - shift;  // delta of (row 0, key 0) of the tile
+        const bool need_mask = (ks + 128 > Lk) || (p.causal && d0 + 127 > 0);
+        const int lim = min(Lk - ks, p.causal ? (qrow + shift - ks + 1) : 128);
         int mode;
         float rowc = 0.f, kk = 0.f;
         if (!p.bias.has_bias) {
@@ -560,32 +603,53 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(p_ready + t);
       }
       grid_dep_launch();  // a dependent grid (the backward preprocessing) may be scheduled
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (nk - 1) & 1, wd));
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-        const bool valid = qrow < L;
-        __nv_bfloat16 *orow = p.out + ((size_t)(seq_start + qrow) * H + h) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          }
-        }
-        if (valid && p.lse != nullptr) {
+      if (nk == 0) {  // this tile sees no key (in this key range): empty rows, TMEM untouched
+        fwd_write_empty_rows<D>(p, seq_start, qs, min(L - qs, 128), h, split, r, 128);
+      } else {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (nk - 1) & 1, wd));
+        if (ok) {
+          tc_fence_after();
+          const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+          const bool valid = qrow < L;
           const float m_use = (m == -INFINITY) ? 0.f : m;
-          p.lse[(size_t)h * T + seq_start + qrow] =
-              l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+          const float lse_row = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+          if (p.kv_splits == 1) {
+            __nv_bfloat16 *orow = p.out + ((size_t)(seq_start + qrow) * H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+              if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+              }
+            }
+            if (valid && p.lse != nullptr) p.lse[(size_t)h * T + seq_start + qrow] = lse_row;
+          } else {  // partial result of this key range, normalised, in fp32
+            float *orow = p.o_part + (((size_t)split * T + seq_start + qrow) * H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              if (valid) {
+                float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4)
+                  dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv_l,
+                                        __uint_as_float(o[4 * v4 + 1]) * inv_l,
+                                        __uint_as_float(o[4 * v4 + 2]) * inv_l,
+                                        __uint_as_float(o[4 * v4 + 3]) * inv_l);
+              }
+            }
+            if (valid) p.lse_part[((size_t)split * H + h) * T + seq_start + qrow] = lse_row;
+          }
         }
       }
     }
@@ -599,15 +663,16 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, cudaStream_t stream) {
+int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, const void *v,
+               cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
-  if (make_tmap_thd(&mq, q, T, H, head_dim, 128) || make_tmap_thd(&mk, k, T, H, head_dim, 128) ||
-      make_tmap_thd(&mv, v, T, H, head_dim, 128))
+  const int Tk = p.seq.total_k, Hkv = p.seq.num_heads_kv;
+  if (make_tmap_thd(&mq, q, T, H, head_dim, 128) || make_tmap_thd(&mk, k, Tk, Hkv, head_dim, 128) ||
+      make_tmap_thd(&mv, v, Tk, Hkv, head_dim, 128))
     return (int)cudaErrorInvalidValue;
   const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
-  dim3 grid((max_seqlen + 255) / 256, H, p.seq.num_seqs);
+  dim3 grid((p.seq.max_seqlen + 255) / 256, H, p.seq.num_seqs * p.kv_splits);
   cudaError_t e;
   if (head_dim == 64) {
     e = cudaFuncSetAttribute(fat_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -637,6 +702,74 @@ int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, 
              smem);
     set_last_error("kernel launch", (int)e, msg);
   }
+  return (int)e;
+}
+
+// Merge of a split forward's partial results, one warp per (query row, head): with partial lse
+// l_s and normalised partial outputs O_s, lse = log sum_s exp(l_s) and
+// out = sum_s exp(l_s - lse) O_s (a row with no key in any range: out 0, lse -inf).
+// Memory bound: each lane reads D/32 channels of every split's row.
+template <int D>
+__global__ void __launch_bounds__(256) fat_fwd_combine_kernel(const FwdParams p) {
+  constexpr int CPL = D / 32;  // channels per lane
+  const int T = p.seq.total_tokens, H = p.seq.num_heads, S = p.kv_splits;
+  const int lane = threadIdx.x & 31;
+  const long long nrows = (long long)T * H;
+  const long long w0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long rh = w0; rh < nrows; rh += nw) {
+    const int t = (int)(rh / H), h = (int)(rh % H);
+    float m = -INFINITY;
+    for (int s = 0; s < S; ++s) m = fmaxf(m, p.lse_part[((size_t)s * H + h) * T + t]);
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const float ls = p.lse_part[((size_t)s * H + h) * T + t];
+        if (ls == -INFINITY) continue;
+        const float wgt = __expf(ls - m);
+        wsum += wgt;
+        const float *o = p.o_part + (((size_t)s * T + t) * H + h) * D + lane * CPL;
+        if constexpr (CPL == 2) {
+          const float2 v = *reinterpret_cast<const float2 *>(o);
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+        } else {
+          const float4 v = *reinterpret_cast<const float4 *>(o);
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+          acc[2] += wgt * v.z;
+          acc[3] += wgt * v.w;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+    __nv_bfloat16 *orow = p.out + ((size_t)t * H + h) * D + lane * CPL;
+    if constexpr (CPL == 2) {
+      *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    } else {
+      uint2 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(orow) = v;
+    }
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[(size_t)h * T + t] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+  }
+}
+
+int launch_fwd_combine(const FwdParams &p, int head_dim, cudaStream_t stream) {
+  const long long nrows = (long long)p.seq.total_tokens * p.seq.num_heads;
+  if (nrows == 0) return 0;
+  const int blocks = (int)std::min<long long>((nrows + 7) / 8, 152LL * 8);
+  if (head_dim == 64)
+    fat_fwd_combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
+  else
+    fat_fwd_combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) set_last_error("split forward combine launch", (int)e, cudaGetErrorString(e));
   return (int)e;
 }
 

@@ -38,11 +38,44 @@ struct BiasParams {
   int has_bias;
 };
 
+// Packed documents. Every document has a query sequence and a key/value sequence of its own
+// lengths (the same array for self-attention); query p of a document sits at key position
+// p + (Lk - Lq) (bottom-right alignment: the last query lines up with the last key), which is
+// what the relative position and the causal mask are measured from. Query head h reads
+// key/value head h / group.
 struct SeqParams {
-  const int32_t *cu_seqlens;
-  int num_seqs, num_heads, total_tokens;
-  int max_seqlen;  // the caller's bound on every document length (sizes the grids)
+  const int32_t *cu_seqlens;    // query side [num_seqs + 1]
+  const int32_t *cu_seqlens_k;  // key/value side [num_seqs + 1]
+  int num_seqs, num_heads, total_tokens;  // query heads and query rows
+  int max_seqlen;    // the caller's bound on every query length (sizes the grids)
+  int num_heads_kv, total_k;
+  int max_seqlen_k;  // the caller's bound on every key length
+  int group;         // num_heads / num_heads_kv
 };
+
+// One document's spans, read from both cu_seqlens arrays; ok = false for a corrupt entry.
+struct DocSpan {
+  int sq, lq, sk, lk, shift;  // shift = lk - lq
+  bool ok;
+};
+__device__ __forceinline__ DocSpan doc_span(const SeqParams &s, int doc) {
+  DocSpan d;
+  d.sq = __ldg(s.cu_seqlens + doc);
+  const int eq = __ldg(s.cu_seqlens + doc + 1);
+  d.sk = __ldg(s.cu_seqlens_k + doc);
+  const int ek = __ldg(s.cu_seqlens_k + doc + 1);
+  d.ok = d.sq >= 0 && eq <= s.total_tokens && eq >= d.sq && d.sk >= 0 && ek <= s.total_k &&
+         ek >= d.sk;
+  d.lq = eq - d.sq;
+  d.lk = ek - d.sk;
+  d.shift = d.lk - d.lq;
+  return d;
+}
+// natural-log lse of a row -> the log2 statistic the backward subtracts; a row that saw no key
+// (lse = -inf) gets +inf, so that every P of the row is 2^-inf = 0
+__device__ __forceinline__ float lse_to_log2_stat(float lse) {
+  return lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+}
 
 __device__ __forceinline__ int t5_bucket_dev(int delta, const BiasParams &b) {
   int off = 0, n;
@@ -103,6 +136,12 @@ struct FwdParams {
   int *err;
   long long timeout_ns;
   int debug_flags;
+  // split along keys: blockIdx.z = document * kv_splits + split; split s takes the key tiles
+  // [s * split_tiles, (s + 1) * split_tiles) and writes its normalised partial output (fp32,
+  // o_part [kv_splits, T, H, d]) and partial lse (lse_part [kv_splits, H, T]); a combine pass
+  // merges them. kv_splits = 1: whole rows, out and lse written directly.
+  int kv_splits, split_tiles;
+  float *o_part, *lse_part;
 };
 
 struct BwdParams {
@@ -115,6 +154,8 @@ struct BwdParams {
   const float *dvec;  // [H, T]: rowsum(dout * out)
   float *dq_acc;      // [T, H, d] fp32
   __nv_bfloat16 *dk, *dv;
+  float *dk_acc, *dv_acc;  // [Tk, Hkv, d] fp32 when several query heads share a key/value head
+                           // (group > 1): dK, dV accumulate there; else nullptr
   float *dbias;       // [nb, H] or nullptr
   int *err;
   int nkb;            // key tiles of the longest document (filled by the launcher)
@@ -123,14 +164,15 @@ struct BwdParams {
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t value.
-int launch_fwd(const FwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, cudaStream_t stream);
+int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, const void *v,
+               cudaStream_t stream);
+// merge the kv_splits partial results of a split forward into out (bf16) and lse
+int launch_fwd_combine(const FwdParams &p, int head_dim, cudaStream_t stream);
 size_t fwd_smem_bytes(int head_dim, int lut_len);
 // overlap_previous: launch as a programmatic dependent of the previous grid in the stream (only
 // when that grid is this library's preprocessing grid, which itself waited for its inputs).
-int launch_bwd(const BwdParams &p, int head_dim, int max_seqlen, const void *q, const void *k,
-               const void *v, const void *out, const void *dout, cudaStream_t stream,
-               bool overlap_previous);
+int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, const void *v,
+               const void *dout, cudaStream_t stream, bool overlap_previous);
 size_t bwd_smem_bytes(int head_dim, int lut_len);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);
@@ -152,8 +194,9 @@ void set_last_error(const char *what, int code, const char *text);
 // Tensor map over a [T, H, d] bf16 tensor, box = 64 channels x 1 head x box_rows tokens,
 // 128-byte swizzle (the shared-memory layout the tcgen05 descriptors expect).
 int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows);
-// Tensor map over a [T, H, d] fp32 tensor, box = box_c channels x 1 head x box_rows tokens, no
-// swizzle (for bulk reductions from a row-major shared-memory tile).
+// Tensor map over a [T, H, d] fp32 tensor, box = box_c channels x 1 head x box_rows tokens (for
+// bulk reductions from a shared-memory tile): 64-byte swizzle when a box row is 64 bytes (16-byte
+// chunk c of row r at c ^ ((r / 2) % 4)), else row-major without swizzle.
 int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_c,
                       int box_rows);
 

@@ -126,3 +126,70 @@ def make_inputs(w: Workload, device: str = "cpu", with_dout: bool = True) -> dic
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bit patterns of a bf16 tensor as numpy uint16 (exact, no conversion)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass(frozen=True)
+class XWorkload:
+    """A problem with its own query and key lengths per document (cross-attention, or queries
+    over a longer key cache) and grouped-query heads."""
+    name: str
+    qlens: Tuple[int, ...]
+    klens: Tuple[int, ...]
+    num_heads_q: int
+    num_heads_kv: int
+    head_dim: int
+    qkv_std: float = 1.0
+    t5: Optional[Tuple[int, int, bool]] = None
+    alibi: bool = False
+    causal: bool = False
+    scale: float = 1.0
+    seed: int = 0
+    table_std: float = 0.5
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.qlens))
+
+    @property
+    def total_k(self) -> int:
+        return int(sum(self.klens))
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return int(max(self.qlens)) if self.qlens else 0
+
+    @property
+    def max_seqlen_k(self) -> int:
+        return int(max(self.klens)) if self.klens else 0
+
+    def fwd_flops(self) -> float:
+        """4 * Lq * Lk * d per query head and document (the attention products a dense kernel
+        computes), halved when causal only for square documents (the diagonal mask)."""
+        f = sum(4.0 * a * b * self.head_dim for a, b in zip(self.qlens, self.klens))
+        f *= self.num_heads_q
+        return f / 2 if (self.causal and self.qlens == self.klens) else f
+
+
+def make_xinputs(w: XWorkload, device: str = "cpu") -> dict:
+    """Seeded inputs of an XWorkload (torch CPU generator, then moved to `device`): q, dout
+    [Tq, Hq, d], k, v [Tk, Hkv, d] as bf16-rounded normals, the table [nb, Hq] and the ALiBi
+    slopes [Hq] when asked for, and both cu_seqlens."""
+    g = torch.Generator().manual_seed(w.seed)
+    Tq, Tk, Hq, Hkv, d = w.total_q, w.total_k, w.num_heads_q, w.num_heads_kv, w.head_dim
+
+    def normal(*shape, std=1.0):
+        return torch.randn(*shape, generator=g, dtype=torch.float32) * std
+
+    q = normal(Tq, Hq, d, std=w.qkv_std).to(torch.bfloat16)
+    k = normal(Tk, Hkv, d, std=w.qkv_std).to(torch.bfloat16)
+    v = normal(Tk, Hkv, d, std=w.qkv_std).to(torch.bfloat16)
+    table = normal(w.t5[0], Hq, std=w.table_std) if w.t5 is not None else None
+    dout = normal(Tq, Hq, d).to(torch.bfloat16)
+    slopes = torch.from_numpy(alibi_slopes(Hq)) if w.alibi else None
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(w.qlens)]).astype(np.int32))
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(w.klens)]).astype(np.int32))
+    out = dict(q=q, k=k, v=v, table=table, slopes=slopes, dout=dout, cu_seqlens_q=cu_q,
+               cu_seqlens_k=cu_k)
+    if device != "cpu":
+        out = {key: (t.to(device) if t is not None else None) for key, t in out.items()}
+    return out

@@ -165,6 +165,82 @@ int fat_attn_bwd_noalloc(const fat_shape_t *shape, const void *q, const void *k,
                          int causal, float softmax_scale, const void *out, const float *lse,
                          const void *dout, void *dq, void *dk, void *dv, float *dbias_table);
 
+/*
+ * Cross-attention, grouped-query heads and decode (own query and key lengths per document).
+ *
+ * What is computed. The FAT5 report keeps T5's encoder-decoder architecture ("Motivation"
+ * section): the decoder attends over the encoder's output (cross-attention, query and key
+ * sequences of different lengths; T5 puts no positional bias there) and, when generating, over
+ * a key/value cache longer than the new queries; the report's plans for linear-cost inference
+ * ("La suite" section) rest on that decode step. The pages give no formulas for these; the
+ * readings, which reduce exactly to the self-attention calls above when every document has
+ * Lq = Lk and num_heads_kv = num_heads_q:
+ *   - per document, query p sits at key position p + (Lk - Lq): the last query lines up with
+ *     the last key (bottom-right alignment); the relative position of the bias is
+ *     delta = key_position - (p + Lk - Lq), and causal masks delta > 0;
+ *   - query head h reads key/value head h / (num_heads_q / num_heads_kv) (grouped-query heads);
+ *     the bias table and slopes are indexed by the query head;
+ *   - a query row that sees no key (causal with Lk < Lq, or Lk = 0) has out = 0, lse = -inf and
+ *     contributes no gradient;
+ *   - the backward sums dK, dV of a key/value head over the query heads that read it.
+ * Layout: q, out, dout, dq bf16 [total_q, num_heads_q, head_dim]; k, v, dk, dv bf16
+ * [total_k, num_heads_kv, head_dim]; lse fp32 [num_heads_q, total_q]; cu_seqlens_q and
+ * cu_seqlens_k int32 [num_seqs + 1] (device); bias_table / dbias_table fp32
+ * [num_buckets, num_heads_q]; alibi_slopes fp32 [num_heads_q]. Ownership, alignment, errors and
+ * streams as above; num_heads_q must be a multiple of num_heads_kv.
+ */
+typedef struct {
+  int32_t total_q;      /* rows of q, out, dout, dq */
+  int32_t total_k;      /* rows of k, v, dk, dv */
+  int32_t num_seqs;     /* documents; both cu_seqlens arrays have num_seqs + 1 entries */
+  int32_t max_seqlen_q; /* bound on every document's query count (a longer one is reported as
+                           FAT_DEVERR_SEQLENS) */
+  int32_t max_seqlen_k; /* bound on every document's key count (likewise) */
+  int32_t num_heads_q;
+  int32_t num_heads_kv; /* divides num_heads_q */
+  int32_t head_dim;     /* 64 or 128 */
+  void *stream;         /* cudaStream_t */
+} fat_xshape_t;
+
+/* Forward of the generalised problem (arguments as fat_attn_fwd, with both cu_seqlens). */
+int fat_xattn_fwd(const fat_xshape_t *shape, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_seqlens_q,
+                  const int32_t *cu_seqlens_k, int causal, float softmax_scale, void *out,
+                  float *lse);
+
+/*
+ * The same forward with the keys of every document split into num_splits ranges, each range
+ * computed by blocks of its own, and the partial results merged by a second grid
+ * (out = sum_s exp(lse_s - lse) out_s, lse = log sum_s exp(lse_s)). For decode steps and other
+ * problems with few query rows and long key sequences, where whole rows alone would occupy only
+ * a few SMs. num_splits in [1, 64] (1 = fat_xattn_fwd); fat_xattn_splitkv_num_splits suggests
+ * one (about two blocks per SM). The workspace (256-byte aligned, contents need not be
+ * initialised) holds the partial outputs: fat_xattn_splitkv_workspace_size bytes (0 for one
+ * split). num_seqs * num_splits must not exceed 65535 (FAT_EUNSUPPORTED).
+ */
+int fat_xattn_splitkv_num_splits(const fat_xshape_t *shape);
+size_t fat_xattn_splitkv_workspace_size(const fat_xshape_t *shape, int num_splits);
+int fat_xattn_fwd_splitkv(const fat_xshape_t *shape, const void *q, const void *k, const void *v,
+                          const float *bias_table, int num_buckets, int max_distance,
+                          int bidirectional, const float *alibi_slopes,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int causal,
+                          float softmax_scale, int num_splits, void *workspace,
+                          size_t workspace_bytes, void *out, float *lse);
+
+/* Backward workspace of the generalised problem: the fp32 dQ accumulator [total_q, Hq, d];
+   when num_heads_kv < num_heads_q also fp32 dK and dV accumulators [total_k, Hkv, d]; then D
+   [Hq, total_q]; each 256-byte aligned. */
+size_t fat_xattn_bwd_workspace_size(const fat_xshape_t *shape);
+
+/* Backward of the generalised problem (arguments as fat_attn_bwd, with both cu_seqlens). */
+int fat_xattn_bwd(const fat_xshape_t *shape, const void *q, const void *k, const void *v,
+                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                  const float *alibi_slopes, const int32_t *cu_seqlens_q,
+                  const int32_t *cu_seqlens_k, int causal, float softmax_scale, const void *out,
+                  const float *lse, const void *dout, void *workspace, size_t workspace_bytes,
+                  void *dq, void *dk, void *dv, float *dbias_table);
+
 /* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
    FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
 int fat_attn_get_device_error(void *stream, int *bits);

@@ -27,13 +27,14 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", h)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names |= set(re.findall(r"\b(fat_attn_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(fat_x?attn_\w+)\s*\(", text))
     return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
-    assert len(names) >= 8
+    assert len(names) >= 18
+    assert "fat_xattn_fwd" in names and "fat_xattn_bwd" in names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -128,3 +129,57 @@ def test_bwd_argument_errors(lib):
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     # host validation passes, the first CUDA call fails: an error code, no crash
     assert _fwd(lib, _shape()) == -4
+
+
+def _xshape(Tq=64, Tk=300, n=2, mq=40, mk=200, Hq=4, Hkv=2, d=64):
+    return fa._XShape(Tq, Tk, n, mq, mk, Hq, Hkv, d, None)
+
+
+def _xfwd(lib, sh, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=None, nb=0, md=0, bidir=1, slopes=None, cuq=FAKE,
+             cuk=FAKE, causal=0, scale=1.0, out=FAKE, lse=FAKE)
+    a.update(kw)
+    return lib.fat_xattn_fwd(ctypes.byref(sh), a["q"], a["k"], a["v"], a["table"], a["nb"],
+                             a["md"], a["bidir"], a["slopes"], a["cuq"], a["cuk"], a["causal"],
+                             a["scale"], a["out"], a["lse"])
+
+
+def test_xattn_argument_errors(lib):
+    assert lib.fat_xattn_fwd(None, FAKE, FAKE, FAKE, None, 0, 0, 1, None, FAKE, FAKE, 0, 1.0,
+                             FAKE, FAKE) == -1
+    assert _xfwd(lib, _xshape(), cuk=None) == -1
+    assert _xfwd(lib, _xshape(Hq=6, Hkv=4)) == -2   # query heads not a multiple of kv heads
+    assert _xfwd(lib, _xshape(Hkv=0)) == -2
+    assert _xfwd(lib, _xshape(d=96)) == -2
+    assert _xfwd(lib, _xshape(), k=FAKE + 4) == -2  # misaligned
+    assert _xfwd(lib, _xshape(), table=FAKE, nb=31, md=128, bidir=1) == -3
+    assert _xfwd(lib, _xshape(Tq=0, n=0, mq=0)) == 0  # nothing to do
+    # split keys: at most 64 splits, and the workspace is required and checked
+    sh = _xshape()
+    need = lib.fat_xattn_splitkv_workspace_size(ctypes.byref(sh), 4)
+    assert need >= 4 * 64 * 4 * 64 * 4
+    assert lib.fat_xattn_splitkv_workspace_size(ctypes.byref(sh), 1) == 0
+    def split(ns, ws=FAKE, wsb=need):
+        return lib.fat_xattn_fwd_splitkv(ctypes.byref(sh), FAKE, FAKE, FAKE, None, 0, 0, 1, None,
+                                         FAKE, FAKE, 0, 1.0, ns, ws, wsb, FAKE, FAKE)
+    assert split(65) == -5
+    assert split(0) == -5
+    assert split(4, ws=None) == -1
+    assert split(4, wsb=need - 1) == -2
+    assert split(4, ws=FAKE + 16) == -2
+
+
+def test_xattn_bwd_workspace_layout(lib):
+    # dQ accumulator, then (grouped heads) dK and dV accumulators, then D, each 256-aligned
+    a = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    sh = _xshape(Tq=64, Tk=300, Hq=4, Hkv=2, d=64)
+    want = a(64 * 4 * 64 * 4) + 2 * a(300 * 2 * 64 * 4) + a(4 * 64 * 4)
+    assert lib.fat_xattn_bwd_workspace_size(ctypes.byref(sh)) == want
+    sh1 = _xshape(Tq=64, Tk=300, Hq=4, Hkv=4, d=128)
+    assert lib.fat_xattn_bwd_workspace_size(ctypes.byref(sh1)) == a(64 * 4 * 128 * 4) + a(4 * 64 * 4)
+    assert fa.fat_xattn_bwd_workspace_size(64, 300, 4, 2, 64) == want
+    # self-attention is the special case
+    s = _shape(T=256, H=2, d=64)
+    x = _xshape(Tq=256, Tk=256, Hq=2, Hkv=2, d=64)
+    assert lib.fat_attn_bwd_workspace_size(ctypes.byref(s)) == \
+        lib.fat_xattn_bwd_workspace_size(ctypes.byref(x))

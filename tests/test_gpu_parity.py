@@ -8,8 +8,9 @@ import torch
 
 import oracle
 from attention_relative_position_gb300 import workloads as wl
-from gpu_common import (ATOL, LSE_ATOL, assert_dbias, check, compare_grads, grad_bounds_full,
-                        grad_bounds_rows, oracle_problem, run_gpu)
+from gpu_common import (LSE_ATOL, assert_dbias, check, compare_grads, compare_grads_exact_d,
+                        grad_bounds_full, grad_bounds_rows, grad_tol, operand_bounds,
+                        operand_bounds_full, oracle_problem, run_gpu, run_gpu_bwd_exact_d)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,29 +41,40 @@ SMALL = [
 ]
 
 
-def _full_compare(w, x, res, case=None):
+def _full_compare(w, x, res, case=None, gpu_fwd=None):
+    """Every output of a small case against the oracle: the forward, the public backward (D
+    from the bf16 output, with its propagated bound), and the same backward kernels run on the
+    oracle's exact D (no slack). gpu_fwd: the forward's (out, lse) tensors on the device."""
     case = case or w.name
     pb = oracle_problem(w, x)
     ro, rl = oracle.attn_fwd(pb)
-    check(case, "out", res["out"], ro, ATOL)
+    check(case, "out", res["out"], ro, grad_tol(ro))
     check(case, "lse", res["lse"], rl, LSE_ATOL)
     dout = oracle.widen(wl.bf16_bits(x["dout"]))
     rq, rk, rv, rt = oracle.attn_bwd(pb, dout)
-    bq, bk, _, bt = oracle.attn_bwd(oracle_problem(w, x, d_from_bf16_out=True), dout)
     dq_slack, dk_slack = grad_bounds_full(pb, dout, ro)
-    compare_grads(case, res, dict(dq=rq, dk=rk, dv=rv), dict(dq=bq, dk=bk), dq_slack, dk_slack)
+    exact = dict(dq=rq, dk=rk, dv=rv)
+    ob = operand_bounds_full(pb, dout, ro, rl)
+    compare_grads(case, res, exact, dq_slack, dk_slack, ob)
     if rt is not None:
-        # held to the backward defined on the stored bf16 output (D formed from it); the
-        # distance to the exact calculus is logged beside it
-        assert_dbias(res["dbias"], bt, case, mode="bf16-out")
+        # held norm-wise to the backward defined on the stored bf16 output (D formed from it);
+        # per-bucket error and the distance to the exact calculus are logged beside it
+        bt = oracle.attn_bwd(oracle_problem(w, x, d_from_bf16_out=True), dout)[3]
+        assert_dbias(res["dbias"], bt, case, mode="bf16-out", per_bucket=False)
         assert_dbias(res["dbias"], rt, case, mode="exact", enforce=False)
+    if gpu_fwd is not None:
+        d_exact = np.einsum("thc,thc->ht", dout, ro)  # D = rowsum(dout * out), exact
+        ex = run_gpu_bwd_exact_d(w, x, gpu_fwd[0], gpu_fwd[1], d_exact)
+        compare_grads_exact_d(case, ex, exact, ob)
+        if rt is not None:
+            assert_dbias(ex["dbias"], rt, case, mode="exact-D run")
 
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 def test_small_cases_full(w):
     x = wl.make_inputs(w, device="cuda")
-    res = run_gpu(w, x)
-    _full_compare(w, x, res)
+    res = run_gpu(w, x, keep_fwd=True)
+    _full_compare(w, x, res, gpu_fwd=res.pop("fwd_tensors"))
 
 
 def test_zero_table_equals_plain_attention():
@@ -104,9 +116,11 @@ def _sample_rows(L, n, rng):
 def test_full_size_workloads_sampled(idx):
     w = wl.WORKLOADS[idx]
     x = wl.make_inputs(w, device="cuda")
-    res = run_gpu(w, x)
+    res = run_gpu(w, x, keep_fwd=True)
     pb = oracle_problem(w, x)
     pb16 = oracle_problem(w, x, d_from_bf16_out=True)
+    d_exact = np.full((w.num_heads, w.total_tokens), np.nan)  # NaN: keep the GPU's own D
+    checks = []
     dout = wl.bf16_bits(x["dout"])
     dout64 = oracle.widen(dout)
     rng = np.random.default_rng(100 + idx)
@@ -121,19 +135,30 @@ def test_full_size_workloads_sampled(idx):
             case = f"{w.name}[doc {doc}, head {h}]"
             r = s + np.array(rows)
             o, l = oracle.attn_fwd_rows(pb, doc, h, rows)
-            check(case, "out", res["out"][r, h], o, ATOL)
+            check(case, "out", res["out"][r, h], o, grad_tol(o))
             check(case, "lse", res["lse"][h, r], l, LSE_ATOL)
             want_col = len(lens) == 1
             gq, gk, gv, gcol = oracle.attn_bwd_rows(pb, dout, doc, h, rows, rows,
                                                     want_dtable=want_col)
-            bq, bk, _, bcol = oracle.attn_bwd_rows(pb16, dout, doc, h, rows, rows,
-                                                   want_dtable=want_col)
             sq, sk = grad_bounds_rows(pb, dout64, doc, h, rows, rows)
             got = dict(dq=res["dq"][r, h], dk=res["dk"][r, h], dv=res["dv"][r, h])
-            compare_grads(case, got, dict(dq=gq, dk=gk, dv=gv), dict(dq=bq, dk=bk), sq, sk)
+            exact = dict(dq=gq, dk=gk, dv=gv)
+            o_all, l_all = oracle.attn_fwd_rows(pb, doc, h, list(range(L)))
+            ob = operand_bounds(pb, dout64, doc, h, rows, rows, o_all, l_all)
+            compare_grads(case, got, exact, sq, sk, ob)
             if gcol is not None:
-                assert_dbias(res["dbias"][:, h], bcol, case, mode="bf16-out")
+                bcol = oracle.attn_bwd_rows(pb16, dout, doc, h, [0], [0], want_dtable=True)[3]
+                assert_dbias(res["dbias"][:, h], bcol, case, mode="bf16-out", per_bucket=False)
                 assert_dbias(res["dbias"][:, h], gcol, case, mode="exact", enforce=False)
+            # the exact row statistic of this (document, head), for the exact-D run below
+            d_exact[h, s:s + L] = (dout64[s:s + L, h] * o_all).sum(-1)
+            checks.append((case, r, h, exact, gcol, ob))
+    ex = run_gpu_bwd_exact_d(w, x, res["fwd_tensors"][0], res["fwd_tensors"][1], d_exact)
+    for case, r, h, exact, gcol, ob in checks:
+        got = dict(dq=ex["dq"][r, h], dk=ex["dk"][r, h], dv=ex["dv"][r, h])
+        compare_grads_exact_d(case, got, exact, ob)
+        if gcol is not None:
+            assert_dbias(ex["dbias"][:, h], gcol, case, mode="exact-D run")
     # invariants at full size
     dvs = res["dv"].astype(np.float64)
     dos = x["dout"].float().cpu().numpy().astype(np.float64)
@@ -151,24 +176,37 @@ def test_full_size_workloads_sampled(idx):
 
 def _table_gradient_over_documents(w, heads):
     """The packed batch's table gradient, column by column, is the sum of every document's
-    contribution, each computed by the oracle from whole documents."""
+    contribution, each computed by the oracle from whole documents: the public path against the
+    bf16-output oracle (norm-wise), the exact-D run against the exact oracle (norm-wise and per
+    bucket)."""
     x = wl.make_inputs(w, device="cuda")
-    res = run_gpu(w, x)
+    res = run_gpu(w, x, keep_fwd=True)
     dout = wl.bf16_bits(x["dout"])
+    dout64 = oracle.widen(dout)
     pb = oracle_problem(w, x)
     pb16 = oracle_problem(w, x, d_from_bf16_out=True)
-    ndoc = len(x["cu_seqlens"]) - 1
+    cu = x["cu_seqlens"].cpu().numpy()
+    ndoc = len(cu) - 1
+    d_exact = np.full((w.num_heads, w.total_tokens), np.nan)
+    want = {}
     for h in heads:
         tot = np.zeros(w.t5[0])
         tot16 = np.zeros(w.t5[0])
         for doc in range(ndoc):
-            if int(x["cu_seqlens"][doc + 1] - x["cu_seqlens"][doc]) == 0:
+            s, L = int(cu[doc]), int(cu[doc + 1] - cu[doc])
+            if L == 0:
                 continue
             tot += oracle.attn_bwd_rows(pb, dout, doc, h, [0], [0], want_dtable=True)[3]
             tot16 += oracle.attn_bwd_rows(pb16, dout, doc, h, [0], [0], want_dtable=True)[3]
+            o_all, _ = oracle.attn_fwd_rows(pb, doc, h, list(range(L)))
+            d_exact[h, s:s + L] = (dout64[s:s + L, h] * o_all).sum(-1)
         case = f"{w.name}[all {ndoc} documents, head {h}]"
-        assert_dbias(res["dbias"][:, h], tot16, case, mode="bf16-out")
+        assert_dbias(res["dbias"][:, h], tot16, case, mode="bf16-out", per_bucket=False)
         assert_dbias(res["dbias"][:, h], tot, case, mode="exact", enforce=False)
+        want[h] = (case, tot)
+    ex = run_gpu_bwd_exact_d(w, x, res["fwd_tensors"][0], res["fwd_tensors"][1], d_exact)
+    for h, (case, tot) in want.items():
+        assert_dbias(ex["dbias"][:, h], tot, case, mode="exact-D run")
 
 
 def test_multi_doc_table_gradient_sums_over_documents():
