@@ -17,7 +17,8 @@ __all__ = [
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
     "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages",
     "fat_attn_bwd_noalloc", "fat_xattn_fwd", "fat_xattn_bwd", "fat_xattn_bwd_workspace_size",
-    "fat_xattn_splitkv_num_splits", "FAT_DEVERR_TIMEOUT_FWD", "FAT_DEVERR_TIMEOUT_BWD",
+    "fat_xattn_splitkv_num_splits", "fat_rope_apply", "FAT_DEVERR_TIMEOUT_FWD",
+    "FAT_DEVERR_TIMEOUT_BWD",
     "FAT_DEVERR_SEQLENS", "LIB_PATH",
 ]
 
@@ -99,6 +100,8 @@ def load(path: Optional[str] = None):
     lib.fat_xattn_bwd.argtypes = [X, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, f32, vp, vp,
                                   vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
     lib.fat_xattn_bwd.restype = i32
+    lib.fat_rope_apply.argtypes = [S, vp, vp, vp, ctypes.c_double, i32]
+    lib.fat_rope_apply.restype = i32
     lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.fat_attn_get_device_error.restype = i32
     lib.fat_attn_strerror.argtypes = [i32]
@@ -389,6 +392,27 @@ def fat_xattn_bwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     if rc != 0:
         raise FatAttnError(rc, "fat_xattn_bwd")
     return dq, dk, dv, dbias_table
+
+
+def fat_rope_apply(x, cu_seqlens, max_seqlen: int, base: float = 10000.0, inverse: bool = False,
+                   out=None, stream=None):
+    """Rotary position embedding of bf16 [T, H, d] rows, positions local to each document
+    (inverse=True turns a gradient back). out may be x itself (in place). Returns out."""
+    import torch
+    lib = load()
+    _check_tensor("x", x, torch.bfloat16, 3)
+    _check_tensor("out", out, torch.bfloat16, 3)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(x)
+    T, H, d = x.shape
+    sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, x.device))
+    with _on(x.device):
+        rc = lib.fat_rope_apply(ctypes.byref(sh), _ptr(x), _ptr(out), _ptr(cu_seqlens),
+                                float(base), int(bool(inverse)))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_rope_apply")
+    return out
 
 
 def fat_attn_get_device_error(stream=None, device=None) -> int:

@@ -139,6 +139,8 @@ int cuda_rc(int e) { return e == 0 ? FAT_OK : FAT_ECUDA; }
 
 }  // namespace
 
+int device_error_address(int **out) { return device_error_ptr(out); }
+
 int sm_count() {
   static std::mutex mu;
   static int cached[128] = {0};

@@ -38,9 +38,18 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  static constexpr int OFF_LUT = OFF_BAR + 256;
+  // the watchdog record and the far-side bias constants (read on slow paths / once per step)
+  static constexpr int OFF_WD = OFF_BAR + 256;
+  static constexpr int OFF_LUT = OFF_WD + 64;
   static_assert((1 + 4 * NS + 12) * 8 + 8 <= 256, "barrier block");
   static constexpr int NTHREADS = 384;
+  // setmaxnreg moves registers within what the block was launched with (NTHREADS x the
+  // per-thread count of the launch bound): the split (two softmax warpgroups at REG_SM, one at
+  // REG_OTHER) must fit that pool, or the increase waits forever. The launcher also checks it
+  // against the compiled count before the first launch.
+  static constexpr int REG_SM = 216, REG_OTHER = 72;
+  static constexpr int REGS_NEEDED = 256 * REG_SM + 128 * REG_OTHER;
+  static_assert(REGS_NEEDED <= NTHREADS * ((65536 / NTHREADS) & ~7), "register split");
   // TMEM columns: S_t at 128 t, O_t at 256 + O_STRIDE t. With d = 64 the O_t take 64 columns
   // each and P_t (bf16 pairs) gets its own 64 columns at 384 + 64 t, so S_t of the next key tile
   // can be computed while P_t is still being produced and consumed; with d = 128 P_t is written
@@ -266,13 +275,20 @@ __global__ void __launch_bounds__(384, 1)
   }
   for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS)
     lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
+  if (tid == 0) {
+    *reinterpret_cast<Watchdog *>(sm + C::OFF_WD) =
+        Watchdog{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+    *reinterpret_cast<FarBias *>(sm + C::OFF_WD + 32) = far_bias_dev(h, H, p.bias);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Watchdog wd{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+  // The watchdog record lives in shared memory: it is read only when a wait is slow, so the
+  // roles do not keep it in registers.
+  const Watchdog &wd = *reinterpret_cast<const Watchdog *>(sm + C::OFF_WD);
 
-  if (warp >= 8) regs_dec<72>();
+  if (warp >= 8) regs_dec<C::REG_OTHER>();
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
-    regs_inc<216>();
+    regs_inc<C::REG_SM>();
     const int t = warp >> 2;
     if (t < ntile) {
       const int nk = t == 0 ? nkv0 : nkv1;
@@ -486,7 +502,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tP = C::SEP_P ? tmem + lane_off + C::COL_P0 + 64 * t : tS;
       const int qs = q0 + 128 * t;  // document-local first row of this tile
       const int qrow = qs + r;
-      const FarBias fb = far_bias_dev(h, H, p.bias);
+      const FarBias &fb = *reinterpret_cast<const FarBias *>(sm + C::OFF_WD + 32);
       const bool has_slopes = p.bias.slopes != nullptr;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
@@ -673,6 +689,17 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
     return (int)cudaErrorInvalidValue;
   const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
   dim3 grid((p.seq.max_seqlen + 255) / 256, H, p.seq.num_seqs * p.kv_splits);
+  {  // the register re-balancing needs the launch pool the split was designed for
+    cudaFuncAttributes fa{};
+    const cudaError_t ea = head_dim == 64 ? cudaFuncGetAttributes(&fa, fat_fwd_kernel<64>)
+                                          : cudaFuncGetAttributes(&fa, fat_fwd_kernel<128>);
+    const int need = head_dim == 64 ? FwdCfg<64>::REGS_NEEDED : FwdCfg<128>::REGS_NEEDED;
+    if (ea != cudaSuccess || fa.numRegs * FwdCfg<64>::NTHREADS < need) {
+      set_last_error("forward kernel register pool smaller than its warp-role split",
+                     ea != cudaSuccess ? (int)ea : fa.numRegs, cudaGetErrorString(ea));
+      return ea != cudaSuccess ? (int)ea : (int)cudaErrorInvalidConfiguration;
+    }
+  }
   cudaError_t e;
   if (head_dim == 64) {
     e = cudaFuncSetAttribute(fat_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,

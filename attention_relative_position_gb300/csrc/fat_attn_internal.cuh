@@ -185,6 +185,9 @@ int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const vo
                    const float *lse, const void *dout, const void *dq, const void *dk,
                    const void *dv, const float *dbias_table);
 
+// Address of the current device's error word (FAT_OK, or FAT_ECUDA with the reason recorded).
+int device_error_address(int **out);
+
 // Number of SMs of the current device (cached per device; 0 if the query fails).
 int sm_count();
 

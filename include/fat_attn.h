@@ -241,6 +241,25 @@ int fat_xattn_bwd(const fat_xshape_t *shape, const void *q, const void *k, const
                   const float *lse, const void *dout, void *workspace, size_t workspace_bytes,
                   void *dq, void *dk, void *dv, float *dbias_table);
 
+/*
+ * Rotary position embedding (RoPE). The FAT5 report lists RoFormer's rotary embedding among the
+ * positional encodings its attention kernels take ("Noyau CUDA" section); it prints no formula,
+ * and the plainest reading is RoFormer's: channel pair (2i, 2i + 1) of a row at position m turns
+ * by the angle m * base^(-2i/d) (base 10000 in RoFormer), positions local to each document
+ * (restarting at every cu_seqlens boundary). Unlike the T5 and ALiBi biases it acts on Q and K
+ * rather than on the logits: rotate q and k with this call, run fat_attn_fwd / fat_attn_bwd on
+ * the rotated tensors (no bias), and turn dq and dk back with inverse = 1 (the rotation is
+ * orthogonal, so the gradient of the unrotated input is the transposed rotation of the
+ * rotated one's).
+ *   x, y: bf16 [total_tokens, num_heads, head_dim] (y may equal x: in place); head_dim 64/128;
+ *   cu_seqlens as for the attention calls; base > 1; inverse: 0 rotates, 1 turns back.
+ * Angles are reduced exactly modulo one turn (64-bit fixed-point turns per position), so cosine
+ * and sine carry fp32 accuracy at any position; the result is rounded to bf16.
+ * A document longer than max_seqlen, or a corrupt cu_seqlens entry, sets FAT_DEVERR_SEQLENS.
+ */
+int fat_rope_apply(const fat_shape_t *shape, const void *x, void *y, const int32_t *cu_seqlens,
+                   double base, int inverse);
+
 /* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
    FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
 int fat_attn_get_device_error(void *stream, int *bits);

@@ -7,7 +7,9 @@ package never imports the product library.
 The arithmetic lives in ``oracle.c`` (self-attention with the relative-position bias) and
 ``oracle_xattn.c`` (own query and key lengths per document, grouped-query heads, bottom-right
 causal alignment), plain C, fp64, OpenMP; this module compiles them with gcc and marshals numpy
-arrays through ctypes. The rotary embedding (``rope_*``) is numpy fp64 around the plain oracle.
+arrays through ctypes. The rotary embedding (``rope_*``) is numpy fp64 around the plain oracle;
+RMSNorm and the cross-entropy with z-loss (the report's other fused kernels) are numpy fp64 in
+``oracle.norm_ce``.
 Inputs may be the exact bf16 bit patterns the GPU path receives (numpy ``uint16``), fp32 or fp64
 arrays; all are widened exactly to fp64 here.
 """
