@@ -17,8 +17,8 @@ __all__ = [
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
     "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages",
     "fat_attn_bwd_noalloc", "fat_xattn_fwd", "fat_xattn_bwd", "fat_xattn_bwd_workspace_size",
-    "fat_xattn_splitkv_num_splits", "fat_rope_apply", "FAT_DEVERR_TIMEOUT_FWD",
-    "FAT_DEVERR_TIMEOUT_BWD",
+    "fat_xattn_splitkv_num_splits", "fat_rope_apply", "fat_rmsnorm_fwd", "fat_rmsnorm_bwd",
+    "fat_cross_entropy", "FAT_DEVERR_TIMEOUT_FWD", "FAT_DEVERR_TIMEOUT_BWD", "FAT_DEVERR_INDEX",
     "FAT_DEVERR_SEQLENS", "LIB_PATH",
 ]
 
@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfatattn.
 FAT_DEVERR_TIMEOUT_FWD = 1
 FAT_DEVERR_TIMEOUT_BWD = 2
 FAT_DEVERR_SEQLENS = 4
+FAT_DEVERR_INDEX = 8
 
 
 class FatAttnError(RuntimeError):
@@ -100,6 +101,13 @@ def load(path: Optional[str] = None):
     lib.fat_xattn_bwd.argtypes = [X, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32, f32, vp, vp,
                                   vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
     lib.fat_xattn_bwd.restype = i32
+    ll = ctypes.c_longlong
+    lib.fat_rmsnorm_fwd.argtypes = [ll, i32, vp, vp, f32, vp, vp, vp]
+    lib.fat_rmsnorm_fwd.restype = i32
+    lib.fat_rmsnorm_bwd.argtypes = [ll, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.fat_rmsnorm_bwd.restype = i32
+    lib.fat_cross_entropy.argtypes = [ll, i32, vp, vp, f32, f32, vp, vp, vp, vp]
+    lib.fat_cross_entropy.restype = i32
     lib.fat_rope_apply.argtypes = [S, vp, vp, vp, ctypes.c_double, i32]
     lib.fat_rope_apply.restype = i32
     lib.fat_attn_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -413,6 +421,69 @@ def fat_rope_apply(x, cu_seqlens, max_seqlen: int, base: float = 10000.0, invers
     if rc != 0:
         raise FatAttnError(rc, "fat_rope_apply")
     return out
+
+
+def fat_rmsnorm_fwd(x, weight, eps: float = 1e-6, y=None, rstd=None, stream=None):
+    """RMSNorm of the rows of x (bf16 [..., dim], contiguous) with an fp32 weight [dim].
+    Returns (y bf16 like x, rstd fp32 [rows])."""
+    import torch
+    lib = load()
+    _check_tensor("x", x, torch.bfloat16)
+    _check_tensor("weight", weight, torch.float32, 1)
+    dim = x.shape[-1]
+    rows = x.numel() // dim if dim else 0
+    y = torch.empty_like(x) if y is None else y
+    rstd = torch.empty(rows, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    with _on(x.device):
+        rc = lib.fat_rmsnorm_fwd(rows, int(dim), _ptr(x), _ptr(weight), float(eps), _ptr(y),
+                                 _ptr(rstd), _stream_ptr(stream, x.device))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_rmsnorm_fwd")
+    return y, rstd
+
+
+def fat_rmsnorm_bwd(x, weight, rstd, dy, dx=None, dweight=None, stream=None):
+    """Gradients of sum(y * dy) for fat_rmsnorm_fwd: (dx bf16 like x, dweight fp32 [dim])."""
+    import torch
+    lib = load()
+    for name, t in (("x", x), ("dy", dy), ("dx", dx)):
+        _check_tensor(name, t, torch.bfloat16)
+    _check_tensor("weight", weight, torch.float32, 1)
+    _check_tensor("rstd", rstd, torch.float32, 1)
+    dim = x.shape[-1]
+    rows = x.numel() // dim if dim else 0
+    dx = torch.empty_like(x) if dx is None else dx
+    dweight = torch.empty_like(weight) if dweight is None else dweight
+    with _on(x.device):
+        rc = lib.fat_rmsnorm_bwd(rows, int(dim), _ptr(x), _ptr(weight), _ptr(rstd), _ptr(dy),
+                                 _ptr(dx), _ptr(dweight), _stream_ptr(stream, x.device))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_rmsnorm_bwd")
+    return dx, dweight
+
+
+def fat_cross_entropy(logits, target, z_loss: float = 0.0, grad_scale: float = 1.0,
+                      want_grad: bool = True, loss=None, lse=None, dlogits=None, stream=None):
+    """Cross-entropy with a z-loss term per row of logits (bf16 [rows, vocab]) against int32
+    targets [rows] (negative = ignored); with want_grad the gradient of grad_scale * sum(loss)
+    comes from the same pass. Returns (loss fp32 [rows], lse fp32 [rows], dlogits or None)."""
+    import torch
+    lib = load()
+    _check_tensor("logits", logits, torch.bfloat16, 2)
+    _check_tensor("target", target, torch.int32, 1)
+    rows, vocab = logits.shape
+    loss = torch.empty(rows, dtype=torch.float32, device=logits.device) if loss is None else loss
+    lse = torch.empty(rows, dtype=torch.float32, device=logits.device) if lse is None else lse
+    if want_grad and dlogits is None:
+        dlogits = torch.empty_like(logits)
+    with _on(logits.device):
+        rc = lib.fat_cross_entropy(int(rows), int(vocab), _ptr(logits), _ptr(target),
+                                   float(z_loss), float(grad_scale), _ptr(loss), _ptr(lse),
+                                   _ptr(dlogits) if want_grad else None,
+                                   _stream_ptr(stream, logits.device))
+    if rc != 0:
+        raise FatAttnError(rc, "fat_cross_entropy")
+    return loss, lse, (dlogits if want_grad else None)
 
 
 def fat_attn_get_device_error(stream=None, device=None) -> int:

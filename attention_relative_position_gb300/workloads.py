@@ -193,3 +193,25 @@ def make_xinputs(w: XWorkload, device: str = "cpu") -> dict:
     if device != "cpu":
         out = {key: (t.to(device) if t is not None else None) for key, t in out.items()}
     return out
+
+
+def make_norm_inputs(rows: int, dim: int, seed: int, device: str = "cpu"):
+    """RMSNorm inputs: x bf16 [rows, dim] ~ N(0, s_r^2) with a per-row scale s_r in [0.1, 4],
+    the weight fp32 [dim] ~ 1 + 0.1 N(0, 1), and dy bf16 [rows, dim] ~ N(0, 1)."""
+    g = torch.Generator().manual_seed(seed)
+    s = 0.1 + 3.9 * torch.rand(rows, 1, generator=g)
+    x = (torch.randn(rows, dim, generator=g) * s).to(torch.bfloat16)
+    w = 1.0 + 0.1 * torch.randn(dim, generator=g)
+    dy = torch.randn(rows, dim, generator=g).to(torch.bfloat16)
+    return x.to(device), w.to(device), dy.to(device)
+
+
+def make_ce_inputs(rows: int, vocab: int, seed: int, device: str = "cpu"):
+    """Cross-entropy inputs: logits bf16 [rows, vocab] ~ N(0, 2^2), and int32 targets uniform
+    over the vocabulary with about one row in eight ignored (-100)."""
+    g = torch.Generator().manual_seed(seed)
+    z = (2.0 * torch.randn(rows, vocab, generator=g)).to(torch.bfloat16)
+    t = torch.randint(0, vocab, (rows,), generator=g, dtype=torch.int32)
+    drop = torch.rand(rows, generator=g) < 0.125
+    t[drop] = -100
+    return z.to(device), t.to(device)

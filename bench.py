@@ -451,6 +451,77 @@ def quick_other(w, device, peaks, steps=10):
     return res
 
 
+def _time_ms(torch, fn, reps=10, warm=3):
+    """Median CUDA-event time (ms) of fn() on the current stream, after warm-up calls."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def aux_kernels(device, peaks):
+    """The report's other fused kernels (RMSNorm forward/backward, cross-entropy with z-loss and
+    its gradient in one pass): HBM GB/s of algorithmic bytes over the median CUDA-event time,
+    inputs larger than L2, and the oracle's rate on a bounded sample."""
+    import numpy as np
+    import torch
+    import attention_relative_position_gb300 as fa
+    from attention_relative_position_gb300 import workloads as wl
+    res = {}
+    rows, dim = 131072, 1024  # 256 MiB of bf16 activations
+    g = torch.Generator(device=device).manual_seed(4242)
+    x = torch.randn(rows, dim, device=device, generator=g).to(torch.bfloat16)
+    dy = torch.randn(rows, dim, device=device, generator=g).to(torch.bfloat16)
+    w = 1.0 + 0.1 * torch.randn(dim, device=device, generator=g)
+    y, rstd = fa.fat_rmsnorm_fwd(x, w)
+    dx, dw = torch.empty_like(x), torch.empty_like(w)
+    t_f = _time_ms(torch, lambda: fa.fat_rmsnorm_fwd(x, w, y=y, rstd=rstd))
+    t_b = _time_ms(torch, lambda: fa.fat_rmsnorm_bwd(x, w, rstd, dy, dx=dx, dweight=dw))
+    b_f = rows * dim * 2 * 2 + rows * 4 + dim * 4             # x in, y out, rstd, w
+    b_b = rows * dim * 2 * 3 + rows * 4 + dim * 4 * 2         # x, dy in, dx out, rstd, w, dw
+    xs, ws, dys = wl.make_norm_inputs(2048, dim, seed=7)
+    from oracle import norm_ce as nc
+    t0 = time.perf_counter()
+    nc.rmsnorm_fwd(wl.bf16_bits(xs), ws.numpy(), 1e-6)
+    nc.rmsnorm_bwd(wl.bf16_bits(xs), ws.numpy(), wl.bf16_bits(dys), 1e-6)
+    t_o = time.perf_counter() - t0
+    res["rmsnorm"] = {"rows": rows, "dim": dim,
+                      "fwd_us": round(t_f * 1e3, 2), "fwd_gbs": round(b_f / t_f / 1e6, 1),
+                      "fwd_frac": round(b_f / t_f / 1e6 / peaks["hbm_gbs"], 4),
+                      "bwd_us": round(t_b * 1e3, 2), "bwd_gbs": round(b_b / t_b / 1e6, 1),
+                      "bwd_frac": round(b_b / t_b / 1e6 / peaks["hbm_gbs"], 4),
+                      "oracle_fwd_bwd_gbs": round(2048 * dim * 2 * 5 / t_o / 1e9, 3),
+                      "oracle_sample": f"2048 x {dim} rows, forward + backward, {t_o:.2f} s"}
+    del x, dy, y, dx
+    rows, vocab = 8192, 32768  # 512 MiB of bf16 logits
+    z = (2.0 * torch.randn(rows, vocab, device=device, generator=g)).to(torch.bfloat16)
+    t = torch.randint(0, vocab, (rows,), device=device, generator=g, dtype=torch.int32)
+    loss, lse, dz = fa.fat_cross_entropy(z, t, z_loss=1e-4, grad_scale=1.0 / rows)
+    t_c = _time_ms(torch, lambda: fa.fat_cross_entropy(z, t, z_loss=1e-4, grad_scale=1.0 / rows,
+                                                       loss=loss, lse=lse, dlogits=dz))
+    b_c = rows * vocab * 2 * 2 + rows * (4 + 4 + 4)
+    zs, ts = wl.make_ce_inputs(64, vocab, seed=8)
+    t0 = time.perf_counter()
+    nc.cross_entropy_fwd(wl.bf16_bits(zs), ts.numpy(), 1e-4)
+    nc.cross_entropy_bwd(wl.bf16_bits(zs), ts.numpy(), 1e-4, 1.0 / 64)
+    t_o = time.perf_counter() - t0
+    res["cross_entropy"] = {"rows": rows, "vocab": vocab, "z_loss": 1e-4,
+                            "us": round(t_c * 1e3, 2), "gbs": round(b_c / t_c / 1e6, 1),
+                            "frac": round(b_c / t_c / 1e6 / peaks["hbm_gbs"], 4),
+                            "oracle_gbs": round(64 * vocab * 2 * 2 / t_o / 1e9, 3),
+                            "oracle_sample": f"64 x {vocab} rows, loss + gradient, {t_o:.2f} s"}
+    res["peak_gbs"] = peaks["hbm_gbs"]
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -549,6 +620,7 @@ def run_ours(args, rank, world, local_rank):
                         others[ow.name]["cpu_baseline"] = {
                             "error": f"{type(e).__name__}: {e}"[:200]}
             line["other_workloads"] = others
+            line["aux_kernels"] = _guarded(aux_kernels, device, peaks)
             line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -63,6 +63,7 @@ extern "C" {
 /* bits of the device error word */
 #define FAT_DEVERR_TIMEOUT_FWD 1 /* a forward pipeline wait exceeded its time limit */
 #define FAT_DEVERR_TIMEOUT_BWD 2 /* a backward pipeline wait exceeded its time limit */
+#define FAT_DEVERR_INDEX 8       /* fat_cross_entropy: a target at or beyond the vocabulary */
 #define FAT_DEVERR_SEQLENS 4     /* cu_seqlens had an entry outside [0, total_tokens] or out of
                                     order, or a document longer than max_seqlen (its rows beyond
                                     the grid were not computed) */
@@ -259,6 +260,37 @@ int fat_xattn_bwd(const fat_xshape_t *shape, const void *q, const void *k, const
  */
 int fat_rope_apply(const fat_shape_t *shape, const void *x, void *y, const int32_t *cu_seqlens,
                    double base, int inverse);
+
+/*
+ * The FAT5 report's two other fused kernels ("Noyau Triton" section; their speed and memory are
+ * compared with PyTorch in "Torch vs Triton"). The pages print no formulas; the readings:
+ *
+ * RMSNorm, the T5 layer norm (no mean subtraction, no bias):
+ *   rstd = 1 / sqrt(mean_j x_j^2 + eps),  y = weight * x * rstd.
+ * fat_rmsnorm_fwd: x, y bf16 [rows, dim]; weight fp32 [dim]; rstd fp32 [rows] (may be NULL; the
+ *   backward needs it). dim a multiple of 256, at most 2048.
+ * fat_rmsnorm_bwd: gradients of sum(y * dy): dx bf16 [rows, dim] and dweight fp32 [dim], which is
+ *   OVERWRITTEN (zeroed by the call, then accumulated with fp32 atomics: order-dependent
+ *   rounding). x, weight and rstd as given to / returned by the forward.
+ *
+ * Cross-entropy with a z-loss term (the auxiliary loss that keeps the log-partition near 0):
+ *   lse = log sum_v exp(z_v),  loss = lse - z_target + z_loss * lse^2;
+ *   rows with a negative target are ignored (loss 0, gradient 0).
+ * fat_cross_entropy: logits bf16 [rows, vocab] (vocab a multiple of 8, at most 65536); target
+ *   int32 [rows]; loss and lse fp32 [rows] (either may be NULL). When dlogits (bf16
+ *   [rows, vocab]) is not NULL, the gradient of grad_scale * sum(loss) is written there in the
+ *   same pass (grad_scale = 1 / number of counted rows gives the mean's gradient):
+ *   dz_v = grad_scale * (softmax_v * (1 + 2 z_loss lse) - [v == target]).
+ *   A target at or beyond vocab sets FAT_DEVERR_INDEX (that row: loss 0, gradient 0).
+ * All three are asynchronous on `stream` (a cudaStream_t), allocate nothing and return FAT_*.
+ */
+int fat_rmsnorm_fwd(long long rows, int dim, const void *x, const float *weight, float eps,
+                    void *y, float *rstd, void *stream);
+int fat_rmsnorm_bwd(long long rows, int dim, const void *x, const float *weight,
+                    const float *rstd, const void *dy, void *dx, float *dweight, void *stream);
+int fat_cross_entropy(long long rows, int vocab, const void *logits, const int32_t *target,
+                      float z_loss, float grad_scale, float *loss, float *lse, void *dlogits,
+                      void *stream);
 
 /* Synchronises `stream`, reads the current GPU's device error word, clears it, and returns
    FAT_OK if it was zero, else FAT_EDEVICE with the word's bits stored in *bits (if not NULL). */
