@@ -38,6 +38,12 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                     pack_bf16x2(f[6], f[7]));
 }
+// An opaque copy: the compiler must assume the value changed, so it converts the packed logits
+// again in each pass instead of keeping every converted value live across the passes.
+__device__ __forceinline__ uint4 opaque(uint4 v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+  return v;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -145,7 +151,7 @@ __global__ void __launch_bounds__(256) fat_rmsnorm_bwd_kernel(
 }
 
 template <int CPT>
-__global__ void __launch_bounds__(256) fat_ce_kernel(const uint4 *__restrict__ z,
+__global__ void __launch_bounds__(256, 2) fat_ce_kernel(const uint4 *__restrict__ z,
                                                      const int32_t *__restrict__ target, int V,
                                                      float zc, float scale,
                                                      float *__restrict__ loss,
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(256) fat_ce_kernel(const uint4 *__restrict__ z
     for (int c = 0; c < CPT; ++c) {
       if (c * 256 + tid < n16) {
         float v[8];
-        bf16x8_to_f32(raw[c], v);
+        bf16x8_to_f32(opaque(raw[c]), v);
 #pragma unroll
         for (int k = 0; k < 8; ++k) s += ex2(fmaf(v[k], kLog2e, -ml));  // exp(z - max)
       }
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(256) fat_ce_kernel(const uint4 *__restrict__ z
         const int i = c * 256 + tid;
         if (i < n16) {
           float v[8], o[8];
-          bf16x8_to_f32(raw[c], v);
+          bf16x8_to_f32(opaque(raw[c]), v);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             o[k] = coef * ex2(fmaf(v[k], kLog2e, -ml)) - ((valid && 8 * i + k == t) ? scale : 0.f);
