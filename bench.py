@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only: no e2e, clocks, CPU baseline or extra workloads "
                          "(for profiler launch lists)")
+    ap.add_argument("--aux-kernels", action="store_true",
+                    help="only the RMSNorm and cross-entropy figures, as one JSON line (for "
+                         "profiling those kernels)")
     return ap.parse_args()
 
 
@@ -528,6 +531,12 @@ def run_ours(args, rank, world, local_rank):
     from attention_relative_position_gb300 import _build
     if rank == 0:
         _build.build()
+    if args.aux_kernels:
+        device = f"cuda:{local_rank}"
+        torch.cuda.set_device(device)
+        if rank == 0:
+            print(json.dumps({"aux_kernels": aux_kernels(device, load_peaks()[0])}), flush=True)
+        return
     if world > 1:
         dist.barrier()
     device = f"cuda:{local_rank}"
@@ -560,8 +569,12 @@ def run_ours(args, rank, world, local_rank):
     step_ms = max_over_ranks(med["step"], device)
     f = w.fwd_flops()
     value = job_tflops(3.5 * f, world, step_ms)  # TFLOP/s
+    # the backward runs as the persistent kernel for d = 64 and documents of <= 64 key tiles,
+    # else as one CTA per key tile
+    persistent = w.head_dim == 64 and (w.max_seqlen + 127) // 128 <= 64
+    bwd_name = "fat_bwd_kernel" if persistent else "fat_bwd_tiles_kernel"
     kernels = {"fwd": ("fat_fwd_kernel", f, med["fwd"], "fat_attn_fwd.cu"),
-               "bwd_main": ("fat_bwd_kernel", 2.5 * f, med["bwd_main"], "fat_attn_bwd.cu")}
+               "bwd_main": (bwd_name, 2.5 * f, med["bwd_main"], "fat_attn_bwd.cu")}
     dom = max(kernels, key=lambda k: kernels[k][2])
     kname, kflops, kms, ksrc = kernels[dom]
     achieved = kflops / kms / 1e9
