@@ -141,6 +141,58 @@ int cuda_rc(int e) { return e == 0 ? FAT_OK : FAT_ECUDA; }
 
 int device_error_address(int **out) { return device_error_ptr(out); }
 
+// Per (kernel, device): the largest dynamic shared-memory size already allowed, and whether the
+// compiled register count times the block size holds the kernel's register re-balancing.
+// Launchers call this before every launch; only the first call per size does any CUDA work.
+int prepare_kernel(const void *fn, size_t smem, int nthreads, int regs_needed) {
+  struct Entry {
+    const void *fn;
+    int dev;
+    size_t smem;
+    bool regs_ok;
+  };
+  static std::mutex mu;
+  static Entry tab[256];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  std::lock_guard<std::mutex> lk(mu);
+  Entry *en = nullptr;
+  for (int i = 0; i < used; ++i)
+    if (tab[i].fn == fn && tab[i].dev == dev) en = &tab[i];
+  if (en && en->smem >= smem && en->regs_ok) return 0;
+  if (!en) {
+    if (used == 256) used = 0;  // more kernels x devices than any build has: start over
+    en = &tab[used++];
+    *en = Entry{fn, dev, 0, false};
+  }
+  if (!en->regs_ok) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) {
+      set_last_error("cudaFuncGetAttributes", (int)e, cudaGetErrorString(e));
+      return (int)e;
+    }
+    if (fa.numRegs * nthreads < regs_needed) {
+      set_last_error("kernel register pool smaller than its warp-role split", fa.numRegs,
+                     "no launch");
+      return (int)cudaErrorInvalidConfiguration;
+    }
+    en->regs_ok = true;
+  }
+  if (en->smem < smem) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+      set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e,
+                     cudaGetErrorString(e));
+      return (int)e;
+    }
+    en->smem = smem;
+  }
+  return 0;
+}
+
 int sm_count() {
   static std::mutex mu;
   static int cached[128] = {0};
@@ -179,7 +231,44 @@ bool resolve_encode() {
 }
 }  // namespace
 
+namespace {
+// Encoded tensor maps, keyed by everything they encode (address, sizes, box, element type), so a
+// hit is byte-for-byte the map a fresh encode would give: no entry can go stale. Replacement is
+// round-robin over 128 entries.
+struct TmapKey {
+  const void *ptr;
+  int T, H, d, box_c, box_rows, fp32;
+  bool operator==(const TmapKey &o) const {
+    return ptr == o.ptr && T == o.T && H == o.H && d == o.d && box_c == o.box_c &&
+           box_rows == o.box_rows && fp32 == o.fp32;
+  }
+};
+constexpr int kTmapCache = 128;
+std::mutex g_tmap_mu;
+TmapKey g_tmap_key[kTmapCache];
+CUtensorMap g_tmap_val[kTmapCache];
+int g_tmap_used = 0, g_tmap_next = 0;
+
+bool tmap_lookup(const TmapKey &k, CUtensorMap *map) {
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  for (int i = 0; i < g_tmap_used; ++i)
+    if (g_tmap_key[i] == k) {
+      *map = g_tmap_val[i];
+      return true;
+    }
+  return false;
+}
+void tmap_store(const TmapKey &k, const CUtensorMap &map) {
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  const int i = g_tmap_used < kTmapCache ? g_tmap_used++ : (g_tmap_next++ % kTmapCache);
+  g_tmap_key[i] = k;
+  g_tmap_val[i] = map;
+}
+}  // namespace
+
 int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_rows) {
+  const TmapKey key{ptr, T, H, d, 64, box_rows, 0};
+  if (tmap_lookup(key, map)) return 0;
   if (!resolve_encode()) return -1;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
@@ -193,11 +282,14 @@ int make_tmap_thd(CUtensorMap *map, const void *ptr, int T, int H, int d, int bo
     set_last_error("cuTensorMapEncodeTiled", (int)r, "");
     return -1;
   }
+  tmap_store(key, *map);
   return 0;
 }
 
 int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, int box_c,
                       int box_rows) {
+  const TmapKey key{ptr, T, H, d, box_c, box_rows, 1};
+  if (tmap_lookup(key, map)) return 0;
   if (!resolve_encode()) return -1;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
@@ -212,6 +304,7 @@ int make_tmap_thd_f32(CUtensorMap *map, const void *ptr, int T, int H, int d, in
     set_last_error("cuTensorMapEncodeTiled(fp32)", (int)r, "");
     return -1;
   }
+  tmap_store(key, *map);
   return 0;
 }
 

@@ -1583,7 +1583,7 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
   cudaError_t e;
   bool attr_failed = false;
   auto go = [&](auto kernel) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = (cudaError_t)prepare_kernel((const void *)kernel, smem, BwdCfg<64, 2>::NTHREADS, 0);
     if (e != cudaSuccess) {
       attr_failed = true;
       return;
@@ -1611,10 +1611,7 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
   } else {
     if (ns == 3) go(fat_bwd_tiles_kernel<128, 3>); else go(fat_bwd_tiles_kernel<128, 2>);
   }
-  if (attr_failed) {
-    set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
-    return (int)e;
-  }
+  if (attr_failed) return (int)e;  // reason recorded by prepare_kernel
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};

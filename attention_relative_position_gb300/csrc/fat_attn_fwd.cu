@@ -689,33 +689,20 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
     return (int)cudaErrorInvalidValue;
   const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
   dim3 grid((p.seq.max_seqlen + 255) / 256, H, p.seq.num_seqs * p.kv_splits);
-  {  // the register re-balancing needs the launch pool the split was designed for
-    cudaFuncAttributes fa{};
-    const cudaError_t ea = head_dim == 64 ? cudaFuncGetAttributes(&fa, fat_fwd_kernel<64>)
-                                          : cudaFuncGetAttributes(&fa, fat_fwd_kernel<128>);
-    const int need = head_dim == 64 ? FwdCfg<64>::REGS_NEEDED : FwdCfg<128>::REGS_NEEDED;
-    if (ea != cudaSuccess || fa.numRegs * FwdCfg<64>::NTHREADS < need) {
-      set_last_error("forward kernel register pool smaller than its warp-role split",
-                     ea != cudaSuccess ? (int)ea : fa.numRegs, cudaGetErrorString(ea));
-      return ea != cudaSuccess ? (int)ea : (int)cudaErrorInvalidConfiguration;
-    }
-  }
+  // the register re-balancing needs the launch pool the split was designed for
   cudaError_t e;
   if (head_dim == 64) {
-    e = cudaFuncSetAttribute(fat_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<64>, smem, FwdCfg<64>::NTHREADS,
+                                    FwdCfg<64>::REGS_NEEDED);
     if (e == cudaSuccess)
       fat_fwd_kernel<64><<<grid, FwdCfg<64>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
   } else {
-    e = cudaFuncSetAttribute(fat_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<128>, smem,
+                                    FwdCfg<128>::NTHREADS, FwdCfg<128>::REGS_NEEDED);
     if (e == cudaSuccess)
       fat_fwd_kernel<128><<<grid, FwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
   }
-  if (e != cudaSuccess) {
-    set_last_error("cudaFuncSetAttribute(max dynamic shared memory)", (int)e, cudaGetErrorString(e));
-    return (int)e;
-  }
+  if (e != cudaSuccess) return (int)e;
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};

@@ -188,6 +188,11 @@ int check_bwd_args(const fat_shape_t *sh, const void *q, const void *k, const vo
 // Address of the current device's error word (FAT_OK, or FAT_ECUDA with the reason recorded).
 int device_error_address(int **out);
 
+// Before a launch: allow `smem` bytes of dynamic shared memory for kernel `fn` and check that its
+// compiled register count times nthreads holds regs_needed (0: no re-balancing), once per
+// (kernel, device, size). Returns a cudaError_t value (the reason recorded on failure).
+int prepare_kernel(const void *fn, size_t smem, int nthreads, int regs_needed);
+
 // Number of SMs of the current device (cached per device; 0 if the query fails).
 int sm_count();
 

@@ -450,6 +450,15 @@ def quick_other(w, device, peaks, steps=10):
     res = {k: round(v, 4) for k, v in res.items()}
     res["ms_per_step"] = round(step_ms, 4)
     res["hbm"] = _guarded(hbm_figures, w, per, peaks["hbm_gbs"])
+    if w.total_tokens <= 1024:  # latency-bound: beside the launch floor of this stream
+        import torch
+        one = torch.zeros(1, device=device)
+        floor = _time_ms(torch, lambda: one.zero_(), reps=50, warm=5)
+        res["latency"] = {"fwd_us": round(statistics.median(per["fwd"]) * 1e3, 2),
+                          "step_us": round(step_ms * 1e3, 2),
+                          "launches_per_step": Runner.LAUNCHES_PER_STEP,
+                          "launch_floor_us": round(floor * 1e3, 2),
+                          "floor": "CUDA-event time of one one-element kernel on the same stream"}
     del r
     return res
 

@@ -34,7 +34,9 @@
  * device error word per GPU (see fat_attn_get_device_error) and the scratch array of
  * fat_attn_bwd_noalloc (FAT_NOALLOC_SCRATCH_BYTES per GPU), both file-scope device variables
  * that every GPU on which the library's module is loaded holds until the process exits, whether
- * or not those calls are made.
+ * or not those calls are made; and a host-side cache of encoded TMA tensor maps, keyed by every
+ * field they encode (address, sizes, tile box, element type), so that a cached map is identical
+ * to a fresh one.
  *
  * Errors. Every call returns 0 on success or a negative FAT_E* code; nothing throws, exits or
  * traps. Argument errors are detected on the host before anything is enqueued. Device-side
