@@ -12,8 +12,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libfatattn.so")
-SOURCES = ["fat_attn_api.cu", "fat_attn_fwd.cu", "fat_attn_bwd.cu", "fat_attn_noalloc.cu",
-           "fat_rope.cu", "fat_norm_ce.cu"]
+SOURCES = ["fat_attn_api.cu", "fat_attn_fwd.cu", "fat_attn_bwd.cu", "fat_attn_decode.cu",
+           "fat_attn_noalloc.cu", "fat_rope.cu", "fat_norm_ce.cu"]
 HEADERS = ["sm103_ptx.cuh", "fat_attn_internal.cuh"]
 PUBLIC_HEADERS = [os.path.join(ROOT, "include", h) for h in ("fat_attn.h", "fat_attn_debug.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -542,12 +542,24 @@ size_t splitkv_bytes(const XShape &x, int splits) {
   return align256((size_t)splits * x.Tq * x.Hq * x.d * 4) + align256((size_t)splits * x.Hq * x.Tq * 4);
 }
 
-// Number of key splits: enough blocks for about two per SM when the rows alone give fewer, each
-// split keeping at least two key tiles, at most 64.
+// Rows of one few-row forward block: every query of a document times the query heads of a group.
+long long decode_row_count(const XShape &x) { return (long long)x.maxq * (x.Hq / x.Hkv); }
+
+// Number of key splits, each keeping at least two 128-key tiles, at most 64. Tiled forward:
+// enough blocks for about two per SM when the rows alone give fewer. Few-row forward (blocks of
+// (split, key/value head, document), two resident per SM): as many splits as fill one wave.
 int auto_splits(const XShape &x) {
-  const long long base = (long long)((x.maxq + 255) / 256) * x.Hq * x.n;
   const int sms = sm_count() > 0 ? sm_count() : 152;
   const int nkt = (x.maxk + 127) / 128;
+  if (decode_row_count(x) <= 8) {
+    const long long base = (long long)x.Hkv * x.n;
+    if (base <= 0 || nkt < 4) return 1;
+    long long want = (long long)decode_blocks_per_sm() * sms / base;
+    want = std::min<long long>(want, nkt / 2);
+    want = std::min<long long>(want, 64);
+    return (int)std::max<long long>(want, 1);
+  }
+  const long long base = (long long)((x.maxq + 255) / 256) * x.Hq * x.n;
   if (base <= 0 || base >= sms || nkt < 4) return 1;
   long long want = (2LL * sms + base - 1) / base;
   want = std::min<long long>(want, nkt / 2);
@@ -593,7 +605,10 @@ int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
     p.lse_part = reinterpret_cast<float *>(
         base + align256((size_t)splits * x.Tq * x.Hq * x.d * 4));
   }
-  rc = cuda_rc(launch_fwd(p, x.d, q, k, v, x.stream));
+  const bool few_rows = decode_row_count(x) <= 8 &&
+                        decode_eligible(x.d, (int)decode_row_count(x), x.Hq / x.Hkv, p.bias);
+  rc = cuda_rc(few_rows ? launch_decode(p, x.d, q, k, v, x.stream)
+                        : launch_fwd(p, x.d, q, k, v, x.stream));
   if (rc || splits == 1) return rc;
   return cuda_rc(launch_fwd_combine(p, x.d, x.stream));
 }

@@ -169,6 +169,15 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
 // merge the kv_splits partial results of a split forward into out (bf16) and lse
 int launch_fwd_combine(const FwdParams &p, int head_dim, cudaStream_t stream);
 size_t fwd_smem_bytes(int head_dim, int lut_len);
+// Few-row forward (decode steps, short query chunks): taken when max_seqlen * group rows fit
+// the kernel's row tile and its bias lookup table fits shared memory. Same FwdParams contract
+// as launch_fwd (kv_splits = 1: out and lse; more: the partials launch_fwd_combine merges).
+bool decode_eligible(int head_dim, int max_rows, int group, const BiasParams &b);
+int decode_rows(int head_dim, int rows);  // the kernel's row tile for `rows` rows (0: too many)
+size_t decode_smem_bytes(int head_dim, int R, int group, const BiasParams &b);
+int decode_blocks_per_sm();
+int launch_decode(const FwdParams &p, int head_dim, const void *q, const void *k, const void *v,
+                  cudaStream_t stream);
 // overlap_previous: launch as a programmatic dependent of the previous grid in the stream (only
 // when that grid is this library's preprocessing grid, which itself waited for its inputs).
 int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, const void *v,

@@ -38,6 +38,12 @@ SMALL = [
       False, False, 0.5, seed=22),
     W("t5dec_many_docs_causal_d64", (200,) * 16 + (1,) * 4 + (383,), 3, 64, 1.0,
       (32, 128, False), False, True, 0.5, seed=23),
+    # documents of at most 8 tokens: the forward takes the few-row kernel (rows = the
+    # document's queries), the backward the tiled kernels
+    W("tiny_docs_t5_alibi_causal_d64", (1, 3, 8, 2, 5, 0, 7, 8, 4), 4, 64, 1.0,
+      (32, 128, False), True, True, 0.5, seed=24),
+    W("tiny_docs_t5_bidir_d128", (6, 1, 8, 8, 3), 2, 128, 1.0, (32, 128, True), False, False,
+      0.3, seed=25),
 ]
 
 

@@ -170,6 +170,16 @@ DECODE = [
     # grouped heads, d 128, ALiBi, a few queries per document (chunked decode)
     XW("decode_gqa_alibi_d128", (1, 4, 2, 1), (4000, 1500, 129, 7), 8, 2, 128, 1.0, None, True,
        True, 128 ** -0.5, seed=67),
+    # the few-row kernel's row tiles: 8 rows (one query x 8 heads of a group; two queries x 4
+    # heads), 4 rows (4 heads over one key/value head), with a document without keys, a
+    # document with more queries than keys (its first query sees nothing under the causal
+    # mask) and empty key ranges when the split count exceeds the key tiles
+    XW("decode_gqa8_t5bidir_d128", (1,) * 6, (3000, 0, 1, 513, 4096, 77), 16, 2, 128, 0.5,
+       (32, 128, True), False, False, 128 ** -0.5, seed=68),
+    XW("decode_chunk2_gqa4_t5_alibi_causal_d64", (2, 1, 2, 0, 2), (700, 1, 2049, 30, 1), 8, 2,
+       64, 0.5, (32, 64, False), True, True, 0.125, seed=69),
+    XW("decode_mqa_causal_d128", (1, 1, 1), (5000, 2500, 640), 4, 1, 128, 1.0, None, False,
+       True, 128 ** -0.5, seed=70),
 ]
 
 
@@ -188,7 +198,9 @@ def test_decode_split_kv(w):
         _check_fwd(f"{w.name} ({ns} splits)", res, ro, rl)
         # the merge reproduces the unsplit result up to the bf16 rounding of out
         assert np.abs(res["out"] - whole["out"]).max() <= 2 ** -7 * max(1.0, np.abs(ro).max())
-        assert np.abs(res["lse"] - whole["lse"]).max() <= 1e-4
+        fin = np.isfinite(whole["lse"])  # rows without keys: -inf on both sides
+        assert np.array_equal(np.isfinite(res["lse"]), fin)
+        assert np.abs(res["lse"][fin] - whole["lse"][fin]).max() <= 1e-4
     # and the backward of a decode step (one query over the cache) against the oracle
     res = _gpu(w, x, num_splits=0, bwd=True)
     dout = oracle.widen(wl.bf16_bits(x["dout"]))
