@@ -4,7 +4,8 @@
 // position m turns by m * theta_i, theta_i = base^(-2i/d), positions local to each document.
 // Applied to Q and K before the attention kernels (inverse = transposed rotation for dQ, dK).
 //
-// Memory bound: one 16-byte load and store per thread step (four channel pairs). The angle is
+// Memory bound: a thread takes one (token, 16-byte chunk) position, computes its four angles
+// once and turns that chunk of every head (16-byte loads and stores). The angle is
 // taken exactly modulo one turn: each pair's rate theta_i / (2 pi) is a 64-bit fixed-point
 // fraction of a turn (from double precision on the host), so m * rate mod 1 is one integer
 // multiply that wraps, whatever the position; its top bits give the turn fraction in [0, 1), and
@@ -19,6 +20,7 @@ namespace fat {
 namespace {
 
 constexpr int kMaxPairs = 64;  // head_dim <= 128
+constexpr int kHeadBatch = 8;  // heads whose loads one thread issues together
 
 struct RopeParams {
   const int32_t *cu_seqlens;
@@ -39,32 +41,46 @@ __global__ void __launch_bounds__(256) fat_rope_kernel(const RopeParams p) {
   }
   if (e - s > p.max_seqlen && threadIdx.x == 0 && blockIdx.x == 0)
     atomicOr(p.err, FAT_DEVERR_SEQLENS);
-  const int cpr = p.H * p.d / 8;  // 16-byte chunks per token
-  const long long n = (long long)(e - s) * cpr;
-  const int cph = p.d / 8;        // chunks per head
+  // one thread per (token, 16-byte chunk of a head): its four angles are computed once and
+  // applied to that chunk of every head (the heads share the positions)
+  const int cph = p.d / 8;  // chunks per head
+  const long long n = (long long)(e - s) * cph;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const int tok = (int)(i / cpr);
-    const int c = (int)(i % cpr) % cph;  // chunk within the head: pairs 4c .. 4c + 3
+    const int tok = (int)(i / cph);
+    const int c = (int)(i % cph);  // pairs 4c .. 4c + 3
     const unsigned long long pos = (unsigned long long)tok;
-    const long long idx = (long long)(s + tok) * cpr + (i % cpr);
-    uint4 v = p.x[idx];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float cs[4], sn[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       // fraction of a turn in [0, 1): the top 24 bits of pos * rate mod 2^64
       const unsigned long long turns = pos * p.rate[4 * c + k];
-      const float frac = (float)(uint32_t)(turns >> 40) * (1.0f / 16777216.0f);  // 24 bits
-      float sn, cs;
-      sincospif(2.0f * frac, &sn, &cs);
-      if (p.inverse) sn = -sn;
-      __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162 *>(&w[k]);
-      const float2 a = __bfloat1622float2(pr);
-      const float r0 = a.x * cs - a.y * sn;
-      const float r1 = a.x * sn + a.y * cs;
-      w[k] = pack_bf16x2(r0, r1);
+      const float frac = (float)(uint32_t)(turns >> 40) * (1.0f / 16777216.0f);
+      sincospif(2.0f * frac, &sn[k], &cs[k]);
+      if (p.inverse) sn[k] = -sn[k];
     }
-    p.y[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+    const long long base = (long long)(s + tok) * p.H * cph + c;
+    // heads in groups of kHeadBatch: all loads of a group are issued before its stores, so a
+    // thread keeps several 16-byte reads in flight (x and y may be the same buffer: each
+    // thread reads and writes only its own chunks, reads first)
+    for (int h0 = 0; h0 < p.H; h0 += kHeadBatch) {
+      uint4 v[kHeadBatch];
+#pragma unroll
+      for (int j = 0; j < kHeadBatch; ++j)
+        if (h0 + j < p.H) v[j] = p.x[base + (long long)(h0 + j) * cph];
+#pragma unroll
+      for (int j = 0; j < kHeadBatch; ++j) {
+        if (h0 + j >= p.H) break;
+        uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162 *>(&w[k]);
+          const float2 a = __bfloat1622float2(pr);
+          w[k] = pack_bf16x2(a.x * cs[k] - a.y * sn[k], a.x * sn[k] + a.y * cs[k]);
+        }
+        p.y[base + (long long)(h0 + j) * cph] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
   }
 }
 
@@ -105,8 +121,11 @@ extern "C" int fat_rope_apply(const fat_shape_t *sh, const void *x, void *y,
   }
   int rc = device_error_address(&p.err);
   if (rc) return rc;
-  const long long per_doc = (long long)sh->max_seqlen * sh->num_heads * sh->head_dim / 8;
-  const int bx = (int)std::min<long long>((per_doc + 255) / 256, 64);
+  // enough blocks for every (token, chunk) of the longest document, at most ~8 per SM in all
+  const long long per_doc = (long long)sh->max_seqlen * sh->head_dim / 8;
+  const int sms = sm_count() > 0 ? sm_count() : 152;
+  const long long cap = std::max<long long>(1, (long long)sms * 8 / sh->num_seqs);
+  const int bx = (int)std::min<long long>((per_doc + 255) / 256, cap);
   const dim3 grid(bx > 0 ? bx : 1, sh->num_seqs);
   fat_rope_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(sh->stream)>>>(p);
   const cudaError_t e = cudaGetLastError();

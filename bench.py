@@ -435,6 +435,34 @@ def hbm_figures(w, per, peak_gbs):
     return res
 
 
+def graph_step(r, f):
+    """The step (forward + fused backward) captured in a CUDA graph after warm-up on the capture
+    stream (kernel attributes and tensor maps are prepared then), replayed and timed with CUDA
+    events: the device time without the host's per-launch cost."""
+    import torch
+    s = torch.cuda.Stream()
+    old = r.stream
+    r.stream = s
+    try:
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                r.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            r.step()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            ms = _time_ms(torch, g.replay, reps=50, warm=5)
+    finally:
+        r.stream = old
+    bits = r.fa.fat_attn_get_device_error()
+    if bits:
+        raise RuntimeError(f"device error word {bits}")
+    return {"step_us": round(ms * 1e3, 2), "fwd_bwd_tflops": round(3.5 * f / ms / 1e9, 3),
+            "how": "forward + fused backward captured once in a CUDA graph, replayed"}
+
+
 def quick_other(w, device, peaks, steps=10):
     r = Runner(w, device)
     for _ in range(3):
@@ -450,6 +478,8 @@ def quick_other(w, device, peaks, steps=10):
     res = {k: round(v, 4) for k, v in res.items()}
     res["ms_per_step"] = round(step_ms, 4)
     res["hbm"] = _guarded(hbm_figures, w, per, peaks["hbm_gbs"])
+    if w.total_tokens <= 8192:  # launch-bound: the same step captured once and replayed
+        res["cuda_graph"] = _guarded(graph_step, r, f)
     if w.total_tokens <= 1024:  # latency-bound: beside the launch floor of this stream
         import torch
         one = torch.zeros(1, device=device)
@@ -477,6 +507,26 @@ def _time_ms(torch, fn, reps=10, warm=3):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     return statistics.median(times)
+
+
+def _time_graph_ms(torch, fn, inner=10, reps=20):
+    """Median device time (ms) of one fn() when `inner` calls are captured in one CUDA graph and
+    replayed: the GPU time without the host's per-launch cost (warm-up on the capture stream
+    first, so kernel attributes and tensor maps are prepared outside the capture)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(inner):
+            fn()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        ms = _time_ms(torch, g.replay, reps=reps, warm=3)
+    return ms / inner
 
 
 def aux_kernels(device, peaks):
@@ -531,6 +581,80 @@ def aux_kernels(device, peaks):
                             "oracle_gbs": round(64 * vocab * 2 * 2 / t_o / 1e9, 3),
                             "oracle_sample": f"64 x {vocab} rows, loss + gradient, {t_o:.2f} s"}
     res["peak_gbs"] = peaks["hbm_gbs"]
+    return res
+
+
+def next_rows(device, peaks):
+    """Measurements of the generalised rows: T5 decoder cross-attention forward + backward
+    (TFLOP/s), a decode step over long key caches with and without key splits (HBM GB/s of the
+    cache read), and the RoPE rotation (HBM GB/s)."""
+    import torch
+    import attention_relative_position_gb300 as fa
+    from attention_relative_position_gb300 import workloads as wl
+    res = {}
+    # cross-attention: 8 documents, 512 decoder queries over 1024 encoder keys, 12 heads, d 64
+    xw = wl.XWorkload("xattn_b8_q512_k1024_h12_d64", (512,) * 8, (1024,) * 8, 12, 12, 64,
+                      qkv_std=0.5, seed=2001)
+    x = wl.make_xinputs(xw, device=device)
+    mq, mk = xw.max_seqlen_q, xw.max_seqlen_k
+
+    def xstep():
+        o, l = fa.fat_xattn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"],
+                                mq, mk)
+        fa.fat_xattn_bwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], mq, mk,
+                         o, l, x["dout"])
+
+    t_fwd = _time_ms(torch, lambda: fa.fat_xattn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"],
+                                                     x["cu_seqlens_k"], mq, mk))
+    t_step = _time_ms(torch, xstep)
+    f = xw.fwd_flops()
+    res["cross_attention"] = {"workload": xw.name, "fwd_tflops": round(f / t_fwd / 1e9, 2),
+                              "fwd_bwd_tflops": round(3.5 * f / t_step / 1e9, 2),
+                              "fwd_frac": round(f / t_fwd / 1e9 / peaks["bf16_tflops"], 4)}
+    del x
+    # decode: one query per document over its cache, causal, unidirectional T5 bias
+    for name, n, lk, hq, hkv, d in (("decode_b8_k8192_h8_d128", 8, 8192, 8, 8, 128),
+                                    ("decode_b32_k4096_gqa16x4_d128", 32, 4096, 16, 4, 128)):
+        dw = wl.XWorkload(name, (1,) * n, (lk,) * n, hq, hkv, d, 1.0, (32, 128, False),
+                          causal=True, scale=d ** -0.5, seed=2002)
+        x = wl.make_xinputs(dw, device=device)
+        kw = dict(bias_table=x["table"], num_buckets=32, max_distance=128, bidirectional=False,
+                  causal=True, softmax_scale=dw.scale)
+        ns = fa.fat_xattn_splitkv_num_splits(x["q"], x["k"], x["cu_seqlens_q"], 1, lk)
+        ws = torch.empty(1 << 26, dtype=torch.uint8, device=device)
+        t1 = _time_ms(torch, lambda: fa.fat_xattn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"],
+                                                      x["cu_seqlens_k"], 1, lk, **kw))
+        split = lambda: fa.fat_xattn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], 1, lk, num_splits=ns, workspace=ws,
+                                         **kw)
+        tn = _time_ms(torch, split)
+        tg = _time_graph_ms(torch, split)
+        cache = 2 * n * lk * hkv * d * 2  # K and V, bf16
+        res[name] = {"splits": ns, "unsplit_us": round(t1 * 1e3, 2),
+                     "split_us": round(tn * 1e3, 2),
+                     "split_gbs": round(cache / tn / 1e6, 1),
+                     "split_graph_us": round(tg * 1e3, 2),
+                     "split_graph_gbs": round(cache / tg / 1e6, 1),
+                     "split_graph_frac": round(cache / tg / 1e6 / peaks["hbm_gbs"], 4),
+                     "bytes": "the K and V cache read once",
+                     "graph": "split forward + merge captured 10 times in one CUDA graph"}
+        del x, ws
+    # RoPE on 8 documents of the 16K T5 shape (q: 131072 x 12 x 64 bf16, 201 MB, beyond L2),
+    # positions local to each document
+    g = torch.Generator(device=device).manual_seed(2003)
+    q = torch.randn(8 * 16384, 12, 64, device=device, generator=g).to(torch.bfloat16)
+    cu = torch.arange(0, 8 * 16384 + 1, 16384, dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+    rope = lambda: fa.fat_rope_apply(q, cu, 16384, out=out)
+    t_r = _time_ms(torch, rope)
+    t_g = _time_graph_ms(torch, rope)
+    b = 2 * q.numel() * 2
+    res["rope"] = {"shape": "8 x 16384 x 12 x 64", "us": round(t_r * 1e3, 2),
+                   "gbs": round(b / t_r / 1e6, 1), "frac": round(b / t_r / 1e6 / peaks["hbm_gbs"], 4),
+                   "graph_us": round(t_g * 1e3, 2), "graph_gbs": round(b / t_g / 1e6, 1),
+                   "bytes": "q read and written once"}
+    del q, out
+    res["peaks"] = {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"]}
     return res
 
 
@@ -643,6 +767,7 @@ def run_ours(args, rank, world, local_rank):
                             "error": f"{type(e).__name__}: {e}"[:200]}
             line["other_workloads"] = others
             line["aux_kernels"] = _guarded(aux_kernels, device, peaks)
+            line["next_rows"] = _guarded(next_rows, device, peaks)
             line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
