@@ -193,9 +193,13 @@ def fat_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, bias_table=None, num_buck
     return out, lse
 
 
-def fat_attn_bwd_workspace_size(total_tokens: int, num_heads: int, head_dim: int) -> int:
+def fat_attn_bwd_workspace_size(total_tokens: int, num_heads: int, head_dim: int,
+                                num_seqs: int = 1, max_seqlen: int = 1) -> int:
+    """Backward workspace bytes. With the defaults: the minimum every backward call accepts (dQ
+    accumulator and D); with the problem's num_seqs and max_seqlen: the size for its fastest
+    schedule (adds the rows of a split last wave when the shape has one)."""
     lib = load()
-    sh = _shape(total_tokens, 1, 1, num_heads, head_dim, None)
+    sh = _shape(total_tokens, num_seqs, max_seqlen, num_heads, head_dim, None)
     return int(lib.fat_attn_bwd_workspace_size(ctypes.byref(sh)))
 
 

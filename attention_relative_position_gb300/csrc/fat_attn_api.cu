@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
                                                            float *__restrict__ dvec,
                                                            float4 *__restrict__ acc,
                                                            long long n4_zero,
+                                                           float4 *__restrict__ acc2,
+                                                           long long n4_zero2,
                                                            float *__restrict__ dbias, int nbias,
                                                            int T, int H) {
   grid_dep_wait();    // the forward's outputs are complete (a no-op when launched without overlap)
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(256) fat_bwd_prep_kernel(const uint4 *__restri
     acc[i + 3 * nthreads] = z;
   }
   for (; i < n4_zero; i += nthreads) acc[i] = z;
+  for (i = gtid; i < n4_zero2; i += nthreads) acc2[i] = z;
 }
 
 // out = bf16(acc * scale) over up to three segments (dQ; dK and dV when query heads share
@@ -390,6 +393,13 @@ struct FinishSegs {
   float scale[3];
   long long n8[3];
   int nseg;
+  // split last wave of the backward (documents of equal length Lk): tail CTA c holds the dK,
+  // dV rows of key tile (tail_first + c) % nkb, head ((tail_first + c) / nkb) % H, document
+  // (tail_first + c) / (nkb H), as [c][dK, dV][128][d] fp32 (dK already scaled)
+  const float4 *tail_acc;
+  uint4 *tail_dk, *tail_dv;
+  long long tail_first;
+  int ntail, nkb, H, d8, Lk;
 };
 __global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const FinishSegs f) {
   grid_dep_wait();  // the accumulators are complete (a no-op when launched without overlap)
@@ -415,6 +425,29 @@ __global__ void __launch_bounds__(256) fat_bwd_finish_kernel(const FinishSegs f)
       dq[i + nthreads] = cvt(a1, b1);
     }
     if (i < n8) dq[i] = cvt(acc[2 * i], acc[2 * i + 1]);
+  }
+  const long long ntail8 = (long long)f.ntail * 2 * 128 * f.d8;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < ntail8;
+       i += nthreads) {
+    const int c8 = (int)(i % f.d8);
+    const long long rest = i / f.d8;
+    const int row = (int)(rest % 128);
+    const int which = (int)((rest / 128) % 2);
+    const long long c = rest / 256;
+    const long long cta = f.tail_first + c;
+    const int kb = (int)(cta % f.nkb), h = (int)((cta / f.nkb) % f.H);
+    const long long doc = cta / ((long long)f.nkb * f.H);
+    const int krow = kb * 128 + row;
+    if (krow >= f.Lk) continue;
+    const float4 *src = f.tail_acc + 2 * i;  // [c][which][row][d / 4], c8-th pair of float4
+    uint4 o;
+    const float4 a = src[0], b = src[1];
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    uint4 *dst = which ? f.tail_dv : f.tail_dk;
+    dst[((doc * f.Lk + krow) * f.H + h) * f.d8 + c8] = o;
   }
 }
 
@@ -487,39 +520,75 @@ SeqParams seq_params(const XShape &x, const int32_t *cu_q, const int32_t *cu_k) 
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// Split last wave of the backward's one-CTA-per-key-tile grid. When every document has the same
+// length (sum of lengths = documents x bound) and the grid is not a whole number of waves of
+// one CTA per SM, the CTAs of the partial last wave (at most half a wave) are each split into
+// `splits` CTAs that share the key tile's query tiles, so that wave takes 1/splits of the time.
+// (Used only without the causal mask, where every CTA carries the same work.)
+struct TailPlan {
+  long long first;  // id of the first split CTA
+  int splits, ntail;
+};
+TailPlan bwd_tail_plan(const XShape &x) {
+  TailPlan t{0, 0, 0};
+  if (x.n <= 0 || x.maxq <= 0 || x.maxk <= 0 || !bwd_uses_tiles(x.d, x.maxk)) return t;
+  if ((long long)x.n * x.maxq != x.Tq || (long long)x.n * x.maxk != x.Tk) return t;
+  const int sms = sm_count();
+  if (sms <= 0) return t;
+  const long long items = (long long)((x.maxk + 127) / 128) * x.Hq * x.n;
+  const long long whole = items / sms * sms, ntail = items - whole;
+  const int bq = bwd_query_tile(x.d);
+  const int nq = (x.maxq + bq - 1) / bq;
+  if (ntail == 0 || ntail > sms / 2) return t;
+  const int splits = (int)std::min<long long>(sms / ntail, nq / 2);
+  if (splits < 2) return t;
+  t.first = whole;
+  t.splits = splits;
+  t.ntail = (int)ntail;
+  return t;
+}
+
 // Backward workspace: fp32 dQ accumulator [Tq, Hq, d]; when query heads share key/value heads,
-// fp32 dK and dV accumulators [Tk, Hkv, d]; then D [Hq, Tq]. Each 256-byte aligned; the
-// accumulators form one contiguous region (zeroed by the preprocess).
+// fp32 dK and dV accumulators [Tk, Hkv, d]; then D [Hq, Tq] (this prefix is the minimum a call
+// accepts). When the shape has a split last wave (bwd_tail_plan) and its own key/value heads,
+// the size reported adds fp32 dK and dV rows of those key tiles [tail CTA][2][128][d], used
+// when the caller's workspace holds them. Each part 256-byte aligned; the preprocess zeroes the
+// accumulators.
 struct WsLayout {
-  size_t dk, dv, dvec, zero_bytes, total;
+  size_t dk, dv, dvec, base_total, tail, total;
 };
 WsLayout ws_layout(const XShape &x) {
   WsLayout l{};
   const size_t a = align256((size_t)x.Tq * x.Hq * x.d * 4);
   const size_t b = x.Hq != x.Hkv ? align256((size_t)x.Tk * x.Hkv * x.d * 4) : 0;
+  const TailPlan t = x.Hq == x.Hkv ? bwd_tail_plan(x) : TailPlan{0, 0, 0};
   l.dk = a;
   l.dv = a + b;
   l.dvec = a + 2 * b;
-  l.zero_bytes = a + 2 * b;
-  l.total = l.dvec + align256((size_t)x.Tq * x.Hq * 4);
+  l.base_total = l.dvec + align256((size_t)x.Tq * x.Hq * 4);
+  l.tail = l.base_total;
+  l.total = l.tail + align256((size_t)t.ntail * 2 * 128 * x.d * 4);
   return l;
 }
 
 struct WorkspaceView {
-  float *dq_acc, *dk_acc, *dv_acc, *dvec;
-  size_t zero_bytes;
+  float *dq_acc, *dk_acc, *dv_acc, *tail_acc, *dvec;
+  size_t zero_bytes, tail_bytes;  // accumulators to zero: [0, zero_bytes), tail_acc
 };
 int check_workspace(const XShape &x, const void *ws, size_t bytes, WorkspaceView *view) {
   const WsLayout l = ws_layout(x);
-  if (!ws && l.total) return FAT_EINVAL_NULL;
+  if (!ws && l.base_total) return FAT_EINVAL_NULL;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return FAT_EINVAL_SHAPE;
-  if (bytes < l.total) return FAT_EINVAL_SHAPE;
+  if (bytes < l.base_total) return FAT_EINVAL_SHAPE;
   char *base = static_cast<char *>(const_cast<void *>(ws));
   view->dq_acc = reinterpret_cast<float *>(base);
   view->dk_acc = x.Hq != x.Hkv ? reinterpret_cast<float *>(base + l.dk) : nullptr;
   view->dv_acc = x.Hq != x.Hkv ? reinterpret_cast<float *>(base + l.dv) : nullptr;
+  const bool tail = l.total > l.tail && bytes >= l.total;
+  view->tail_acc = tail ? reinterpret_cast<float *>(base + l.tail) : nullptr;
+  view->tail_bytes = tail ? l.total - l.tail : 0;
   view->dvec = reinterpret_cast<float *>(base + l.dvec);
-  view->zero_bytes = l.zero_bytes;
+  view->zero_bytes = l.dvec;
   return FAT_OK;
 }
 
@@ -660,6 +729,8 @@ int bwd_preprocess_impl(const XShape &x, const void *out, const void *dout, void
   const auto *o = static_cast<const uint4 *>(out);
   const auto *g = static_cast<const uint4 *>(dout);
   float4 *acc4 = reinterpret_cast<float4 *>(ws.dq_acc);
+  float4 *tail4 = reinterpret_cast<float4 *>(ws.tail_acc);
+  const long long n4_tail = (long long)(ws.tail_bytes / 16);
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(blocks);
@@ -673,9 +744,9 @@ int bwd_preprocess_impl(const XShape &x, const void *out, const void *dout, void
   }
   const cudaError_t e =
       d == 64 ? cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<64>, o, g, ws.dvec, acc4, n4,
-                                   dbias_table, nbias, T, H)
+                                   tail4, n4_tail, dbias_table, nbias, T, H)
               : cudaLaunchKernelEx(&cfg, fat_bwd_prep_kernel<128>, o, g, ws.dvec, acc4, n4,
-                                   dbias_table, nbias, T, H);
+                                   tail4, n4_tail, dbias_table, nbias, T, H);
   if (e != cudaSuccess) {
     set_last_error("backward preprocess launch", (int)e, cudaGetErrorString(e));
     return FAT_ECUDA;
@@ -688,7 +759,7 @@ int bwd_main_impl(const XShape &x, const void *q, const void *k, const void *v,
                   const float *alibi_slopes, const int32_t *cu_q, const int32_t *cu_k,
                   int causal, float softmax_scale, const float *lse, const void *dout,
                   void *workspace, size_t workspace_bytes, void *dk, void *dv,
-                  float *dbias_table, bool overlap_previous) {
+                  float *dbias_table, bool overlap_previous, bool split_tail) {
   if (!q || !k || !v || !cu_q || !cu_k || !lse || !dout || !dk || !dv) return FAT_EINVAL_NULL;
   if (dbias_table && !bias_table) return FAT_EUNSUPPORTED;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dout) || misaligned(dk) ||
@@ -718,11 +789,18 @@ int bwd_main_impl(const XShape &x, const void *q, const void *k, const void *v,
   p.dv_acc = ws.dv_acc;
   p.dbias = dbias_table;
   fill_runtime_knobs(&p.timeout_ns, &p.debug_flags);
+  if (split_tail && !causal && (ws.tail_acc || ws.dk_acc)) {
+    const TailPlan t = bwd_tail_plan(x);
+    p.tail_first = t.first;
+    p.tail_splits = t.splits;
+    p.tail_acc = ws.tail_acc;
+  }
   return cuda_rc(launch_bwd(p, x.d, q, k, v, dout, x.stream, overlap_previous));
 }
 
 int bwd_finalize_impl(const XShape &x, const void *workspace, size_t workspace_bytes,
-                      float softmax_scale, void *dq, void *dk, void *dv, bool overlap_previous) {
+                      float softmax_scale, void *dq, void *dk, void *dv, bool overlap_previous,
+                      bool split_tail) {
   if (!dq) return FAT_EINVAL_NULL;
   if (misaligned(dq)) return FAT_EINVAL_SHAPE;
   WorkspaceView ws{};
@@ -746,7 +824,22 @@ int bwd_finalize_impl(const XShape &x, const void *workspace, size_t workspace_b
     add(ws.dk_acc, dk, 1.0f, (long long)x.Tk * x.Hkv * x.d);
     add(ws.dv_acc, dv, 1.0f, (long long)x.Tk * x.Hkv * x.d);
   }
-  if (f.nseg == 0) return FAT_OK;
+  if (split_tail && ws.tail_acc) {  // the split last wave's dK, dV rows
+    if (!dk || !dv) return FAT_EINVAL_NULL;
+    if (misaligned(dk) || misaligned(dv)) return FAT_EINVAL_SHAPE;
+    const TailPlan t = bwd_tail_plan(x);
+    f.tail_acc = reinterpret_cast<const float4 *>(ws.tail_acc);
+    f.tail_dk = static_cast<uint4 *>(dk);
+    f.tail_dv = static_cast<uint4 *>(dv);
+    f.tail_first = t.first;
+    f.ntail = t.ntail;
+    f.nkb = (x.maxk + 127) / 128;
+    f.H = x.Hq;
+    f.d8 = x.d / 8;
+    f.Lk = x.maxk;
+    most = std::max(most, (long long)t.ntail * 2 * 128 * (x.d / 8));
+  }
+  if (f.nseg == 0 && f.ntail == 0) return FAT_OK;
   const int blocks = (int)std::min<long long>((most + 255) / 256, 152LL * 8);
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
@@ -790,9 +883,10 @@ int bwd_impl(const XShape &x, const void *q, const void *k, const void *v,
   // before it touches memory; the main grid before it reads D or touches the accumulators).
   rc = bwd_main_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
                      alibi_slopes, cu_q, cu_k, causal, softmax_scale, lse, dout, workspace,
-                     workspace_bytes, dk, dv, dbias_table, true);
+                     workspace_bytes, dk, dv, dbias_table, true, !causal);
   if (rc) return rc;
-  rc = bwd_finalize_impl(x, workspace, workspace_bytes, softmax_scale, dq, dk, dv, true);
+  rc = bwd_finalize_impl(x, workspace, workspace_bytes, softmax_scale, dq, dk, dv, true,
+                         !causal);
   if (rc || cu_q == cu_k || x.Tk == 0 || x.n == 0) return rc;
   // own key sequences: keys of a document without queries get zero gradients
   fat_zero_unseen_keys_kernel<<<x.n, 256, 0, x.stream>>>(cu_q, cu_k, x.Tk, x.Hkv * x.d,
@@ -948,7 +1042,7 @@ int fat_attn_bwd_main(const fat_shape_t *sh, const void *q, const void *k, const
   if (rc) return rc;
   return bwd_main_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional,
                        alibi_slopes, cu_seqlens, cu_seqlens, causal, softmax_scale, lse, dout,
-                       workspace, workspace_bytes, dk, dv, dbias_table, false);
+                       workspace, workspace_bytes, dk, dv, dbias_table, false, false);
 }
 
 int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t workspace_bytes,
@@ -957,7 +1051,7 @@ int fat_attn_bwd_finalize(const fat_shape_t *sh, const void *workspace, size_t w
   int rc = to_xshape(sh, &x);
   if (rc) return rc;
   return bwd_finalize_impl(x, workspace, workspace_bytes, softmax_scale, dq, nullptr, nullptr,
-                           false);
+                           false, false);
 }
 
 int fat_attn_bwd(const fat_shape_t *sh, const void *q, const void *k, const void *v,

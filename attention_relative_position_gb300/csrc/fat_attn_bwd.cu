@@ -110,6 +110,11 @@ int bwd_stages(int head_dim, int lut_len) {
                                       : bwd_smem_bytes_t<128, 3>(lut_len);
   return three <= (size_t)kSmemLimit ? 3 : 2;
 }
+bool bwd_uses_tiles(int head_dim, int max_seqlen_k) {
+  return !(head_dim == 64 && (max_seqlen_k + 127) / 128 <= 64);
+}
+int bwd_query_tile(int head_dim) { return head_dim == 64 ? BwdCfg<64, 2>::BQ : BwdCfg<128, 2>::BQ; }
+
 size_t bwd_smem_bytes(int head_dim, int lut_len) {
   const int ns = bwd_stages(head_dim, lut_len);
   if (head_dim == 64)
@@ -163,6 +168,24 @@ __device__ __forceinline__ void store_dkdv_row(const BwdParams &p, size_t off,
       red_add_v4(p.dv_acc + off + 4 * i, __uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
                  __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
     }
+  }
+}
+
+// 16 channels of key row r of a split last-wave CTA's dK and dV (partial sums over its share of
+// the query tiles), added into that key tile's fp32 rows of tail_acc (dK scaled here, as above).
+template <int D>
+__device__ __forceinline__ void add_dkdv_tail(const BwdParams &p, long long tail_cta, int r,
+                                              int col, const uint32_t (&a)[16],
+                                              const uint32_t (&b)[16]) {
+  float *dk = p.tail_acc + ((size_t)tail_cta * 2 * 128 + r) * D + col;
+  float *dv = dk + (size_t)128 * D;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    red_add_v4(dk + 4 * i, __uint_as_float(a[4 * i]) * p.scale,
+               __uint_as_float(a[4 * i + 1]) * p.scale, __uint_as_float(a[4 * i + 2]) * p.scale,
+               __uint_as_float(a[4 * i + 3]) * p.scale);
+    red_add_v4(dv + 4 * i, __uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
+               __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
   }
 }
 
@@ -1003,7 +1026,10 @@ __global__ void __launch_bounds__(640, 1)
 // The same backward as a plain grid of one CTA per (key tile, head, document), used for long
 // documents: each CTA walks many query tiles, so there is no set-up to hide, and the hardware
 // hands out CTAs in key-tile order (the CTAs in flight share few heads) and balances them.
-template <int D, int NSTAGES>
+// TAIL: the launch that takes the split last wave (see BwdParams::tail_first): CTA t of its 1-D
+// grid takes part t % tail_splits of key tile CTA tail_first + t / tail_splits; the main launch
+// (TAIL = false) leaves those CTAs out.
+template <int D, int NSTAGES, bool TAIL>
 __global__ void __launch_bounds__(640, 1)
     fat_bwd_tiles_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1015,30 +1041,50 @@ __global__ void __launch_bounds__(640, 1)
   // shared array itself so every derived pointer stays a shared-memory pointer
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kb = blockIdx.x, h = blockIdx.y, doc = blockIdx.z;
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  int kb, h, doc, part = 0, nparts = 1;
+  if constexpr (TAIL) {
+    const long long cta = p.tail_first + blockIdx.x / p.tail_splits;
+    part = (int)(blockIdx.x % p.tail_splits);
+    nparts = p.tail_splits;
+    kb = (int)(cta % p.nkb);
+    h = (int)((cta / p.nkb) % H);
+    doc = (int)(cta / ((long long)p.nkb * H));
+  } else {
+    kb = blockIdx.x;
+    h = blockIdx.y;
+    doc = blockIdx.z;
+    // the split last wave is another launch's
+    if (p.tail_splits > 0 &&
+        kb + (long long)gridDim.x * (h + (long long)gridDim.y * doc) >= p.tail_first)
+      return;
+  }
   const DocSpan span = doc_span(p.seq, doc);
   if (!span.ok) {
-    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    if (tid == 0 && kb == 0 && h == 0 && part == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
     return;
   }
   const int seq_start = span.sq, L = span.lq;  // queries
   const int seq_start_k = span.sk, Lk = span.lk, shift = span.shift;  // keys
   const int hk = h / p.seq.group;
-  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && kb == 0 && tid == 0)
+  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && kb == 0 && part == 0 && tid == 0)
     atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int ks = kb * 128;
   if (ks >= Lk) return;
   // causal: query p sees key r iff r <= p + shift, so the walk starts at query ks - shift
   const int i0 = p.causal ? max(0, ks - shift) / C::BQ : 0;
-  const int nq = (L + C::BQ - 1) / C::BQ - i0;
-  if (nq <= 0) return;  // no query of the document sees this key tile
+  const int nq_all = (L + C::BQ - 1) / C::BQ - i0;
+  if (nq_all <= 0) return;  // no query of the document sees this key tile
+  // this CTA's share of the walk: steps [it_lo, it_lo + nq)
+  const int it_lo = (int)((long long)part * nq_all / nparts);
+  const int nq = (int)((long long)(part + 1) * nq_all / nparts) - it_lo;
+  if (nq <= 0) return;
   // Query tiles are walked starting at a per-CTA offset, so the key-tile CTAs of one head do not
   // all add into the same dQ rows at the same time (same-address reductions serialise in L2).
-  const int qrot = nq > 0 ? kb % nq : 0;
+  const int rot = it_lo + kb % nq_all;  // < 2 nq_all
   auto qtile_start = [&](int it) {
-    const int k = it + qrot;
-    return (i0 + (k >= nq ? k - nq : k)) * C::BQ;
+    const int k = it + rot;
+    return (i0 + (k >= nq_all ? k - nq_all : k)) * C::BQ;
   };
   const bool do_dbias = p.dbias != nullptr && p.bias.table != nullptr;
 
@@ -1511,7 +1557,11 @@ __global__ void __launch_bounds__(640, 1)
         tmem_ld16_issue(tmem + lane_off + C::COL_DV + cb + 16 * c, b);
         tmem_ld16_fence(a);
         tmem_ld16_fence(b);
-        if (row_valid) store_dkdv_row(p, kvrow + 16 * c, a, b);
+        if (!row_valid) continue;
+        if (TAIL && p.dk_acc == nullptr)
+          add_dkdv_tail<D>(p, blockIdx.x / p.tail_splits, r, cb + 16 * c, a, b);
+        else
+          store_dkdv_row(p, kvrow + 16 * c, a, b);
       }
     }
   }
@@ -1575,14 +1625,22 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
   // the set-up and tail of one item overlap the next). Otherwise one CTA per key tile.
   BwdParams pp = p;
   pp.nkb = (p.seq.max_seqlen_k + 127) / 128;
-  const bool persistent = head_dim == 64 && pp.nkb <= 64;
+  const bool persistent = !bwd_uses_tiles(head_dim, p.seq.max_seqlen_k);
   const long long items = (long long)pp.nkb * H * p.seq.num_seqs;
   const int sms = sm_count();
+  // one CTA per key tile; a split last wave (CTAs tail_first .. items - 1 in key-tile-fastest
+  // order) runs as a second launch of tail_splits CTAs per key tile
+  if (persistent || pp.tail_splits <= 1 || pp.tail_first < 0 || pp.tail_first >= items) {
+    pp.tail_splits = 0;
+    pp.tail_first = items;
+  }
+  const long long tail_ctas = (items - pp.tail_first) * pp.tail_splits;
+  if (tail_ctas > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
   const dim3 grid = persistent ? dim3((unsigned)std::min<long long>(items, sms > 0 ? sms : 1))
                                : dim3((unsigned)pp.nkb, H, p.seq.num_seqs);
   cudaError_t e;
   bool attr_failed = false;
-  auto go = [&](auto kernel) {
+  auto go = [&](auto kernel, dim3 g, bool overlap) {
     e = (cudaError_t)prepare_kernel((const void *)kernel, smem, BwdCfg<64, 2>::NTHREADS, 0);
     if (e != cudaSuccess) {
       attr_failed = true;
@@ -1590,11 +1648,11 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
     }
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = grid;
+    cfg.gridDim = g;
     cfg.blockDim = dim3(BwdCfg<64, 2>::NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    if (overlap_previous) {  // programmatic dependent launch on the preprocessing grid
+    if (overlap) {  // programmatic dependent launch on the preprocessing grid
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
@@ -1602,14 +1660,25 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
     }
     e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, mdq, pp);
   };
+  // the split last wave: ordered after the main grid by the stream
+  const dim3 tail_grid((unsigned)tail_ctas);
   if (head_dim == 64) {
     if (persistent) {
-      if (ns == 3) go(fat_bwd_kernel<64, 3>); else go(fat_bwd_kernel<64, 2>);
+      if (ns == 3) go(fat_bwd_kernel<64, 3>, grid, overlap_previous);
+      else go(fat_bwd_kernel<64, 2>, grid, overlap_previous);
+    } else if (ns == 3) {
+      go(fat_bwd_tiles_kernel<64, 3, false>, grid, overlap_previous);
+      if (e == cudaSuccess && tail_ctas) go(fat_bwd_tiles_kernel<64, 3, true>, tail_grid, false);
     } else {
-      if (ns == 3) go(fat_bwd_tiles_kernel<64, 3>); else go(fat_bwd_tiles_kernel<64, 2>);
+      go(fat_bwd_tiles_kernel<64, 2, false>, grid, overlap_previous);
+      if (e == cudaSuccess && tail_ctas) go(fat_bwd_tiles_kernel<64, 2, true>, tail_grid, false);
     }
+  } else if (ns == 3) {
+    go(fat_bwd_tiles_kernel<128, 3, false>, grid, overlap_previous);
+    if (e == cudaSuccess && tail_ctas) go(fat_bwd_tiles_kernel<128, 3, true>, tail_grid, false);
   } else {
-    if (ns == 3) go(fat_bwd_tiles_kernel<128, 3>); else go(fat_bwd_tiles_kernel<128, 2>);
+    go(fat_bwd_tiles_kernel<128, 2, false>, grid, overlap_previous);
+    if (e == cudaSuccess && tail_ctas) go(fat_bwd_tiles_kernel<128, 2, true>, tail_grid, false);
   }
   if (attr_failed) return (int)e;  // reason recorded by prepare_kernel
   if (e == cudaSuccess) e = cudaGetLastError();

@@ -161,6 +161,14 @@ struct BwdParams {
   int nkb;            // key tiles of the longest document (filled by the launcher)
   long long timeout_ns;
   int debug_flags;
+  // Balanced last wave of the one-CTA-per-key-tile grid (documents of equal length, no causal
+  // mask, so every CTA carries the same work): CTA ids >= tail_first come in groups of
+  // tail_splits, each group sharing the query tiles of key tile tail_first + (id - tail_first) /
+  // tail_splits. Their dK, dV rows are added into tail_acc [tail CTA][dK, dV][128 keys][d] fp32
+  // (or into dk_acc / dv_acc when those exist). tail_splits = 0: no split.
+  long long tail_first;
+  int tail_splits;
+  float *tail_acc;
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t value.
@@ -183,6 +191,10 @@ int launch_decode(const FwdParams &p, int head_dim, const void *q, const void *k
 int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, const void *v,
                const void *dout, cudaStream_t stream, bool overlap_previous);
 size_t bwd_smem_bytes(int head_dim, int lut_len);
+// Whether the backward of this head dimension and key bound runs one CTA per key tile (the grid
+// whose last wave can be split), and that grid's query-tile height.
+bool bwd_uses_tiles(int head_dim, int max_seqlen_k);
+int bwd_query_tile(int head_dim);
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream);
 

@@ -187,7 +187,8 @@ class Runner:
         self.dk = torch.empty_like(x["q"])
         self.dv = torch.empty_like(x["q"])
         self.dtab = torch.empty_like(x["table"]) if x["table"] is not None else None
-        nws = fa.fat_attn_bwd_workspace_size(w.total_tokens, w.num_heads, w.head_dim)
+        nws = fa.fat_attn_bwd_workspace_size(w.total_tokens, w.num_heads, w.head_dim,
+                                             len(w.seqlens), w.max_seqlen)
         self.ws = torch.empty(nws, dtype=torch.uint8, device=device)
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.stream = torch.cuda.current_stream(device)

@@ -96,8 +96,15 @@ int fat_attn_fwd(const fat_shape_t *shape, const void *q, const void *k, const v
                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
                  float softmax_scale, void *out, float *lse);
 
-/* Bytes of device workspace fat_attn_bwd needs: an fp32 dQ accumulator [T, H, d] and the fp32
-   row statistics D = rowsum(dout * out) [H, T], each 256-byte aligned. */
+/* Bytes of device workspace for fat_attn_bwd at its fastest. The layout starts with an fp32 dQ
+   accumulator [T, H, d] and the fp32 row statistics D = rowsum(dout * out) [H, T], each
+   256-byte aligned: that prefix is the minimum every backward call accepts. Shapes whose
+   documents all have length max_seqlen (total_tokens = num_seqs * max_seqlen) and whose
+   one-CTA-per-key-tile backward grid ends in a partial wave (head_dim 128, or more than 8192
+   keys at head_dim 64) add fp32 dK/dV rows for splitting that wave along the queries, which
+   fat_attn_bwd uses without the causal mask when the workspace holds them (the dK/dV of those
+   rows are then summed with fp32 atomics: order-dependent rounding). The size depends on the
+   current device's SM count. */
 size_t fat_attn_bwd_workspace_size(const fat_shape_t *shape);
 
 /*
@@ -233,7 +240,9 @@ int fat_xattn_fwd_splitkv(const fat_xshape_t *shape, const void *q, const void *
 
 /* Backward workspace of the generalised problem: the fp32 dQ accumulator [total_q, Hq, d];
    when num_heads_kv < num_heads_q also fp32 dK and dV accumulators [total_k, Hkv, d]; then D
-   [Hq, total_q]; each 256-byte aligned. */
+   [Hq, total_q]; each 256-byte aligned (the minimum a call accepts); then, as for
+   fat_attn_bwd_workspace_size, the rows of a split last wave when the shape has one (own
+   key/value heads; with grouped heads the split wave adds into the dK/dV accumulators). */
 size_t fat_xattn_bwd_workspace_size(const fat_xshape_t *shape);
 
 /* Backward of the generalised problem (arguments as fat_attn_bwd, with both cu_seqlens). */

@@ -44,6 +44,10 @@ SMALL = [
       (32, 128, False), True, True, 0.5, seed=24),
     W("tiny_docs_t5_bidir_d128", (6, 1, 8, 8, 3), 2, 128, 1.0, (32, 128, True), False, False,
       0.3, seed=25),
+    # documents of equal length, no causal mask: the backward's one-CTA-per-key-tile grid is
+    # less than a wave, so its CTAs are split along the query tiles (dK, dV summed in fp32)
+    W("t5enc_equal_docs_split_bwd_d128", (384,) * 3, 4, 128, 1.0, (32, 128, True), False, False,
+      0.3, seed=26),
 ]
 
 

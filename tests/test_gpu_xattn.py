@@ -30,6 +30,10 @@ CASES = [
     # bidirectional T5 + ALiBi with grouped heads, non-causal, d 128
     XW("xattn_t5_alibi_gqa_d128", (129, 77), (200, 333), 4, 2, 128, 0.6, (32, 128, True), True,
        False, 0.3, seed=64),
+    # equal documents, grouped heads, no causal mask: the backward's key-tile CTAs are split
+    # along the query tiles, their dK, dV added into the grouped-head accumulators
+    XW("xattn_equal_docs_split_bwd_gqa_d128", (300,) * 3, (520,) * 3, 4, 2, 128, 0.6,
+       (32, 128, True), True, False, 0.3, seed=71),
 ]
 
 
