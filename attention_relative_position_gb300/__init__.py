@@ -13,7 +13,8 @@ import os
 from typing import Optional
 
 __all__ = [
-    "FatAttnError", "load", "fat_attn_fwd", "fat_attn_bwd", "fat_attn_bwd_workspace_size",
+    "FatAttnError", "load", "fat_attn_fwd", "fat_attn_fwd_workspace_size", "fat_attn_bwd",
+    "fat_attn_bwd_workspace_size",
     "fat_attn_get_device_error", "fat_attn_strerror", "fat_attn_bucket_thresholds",
     "fat_attn_debug_buckets", "fat_attn_debug_set_watchdog", "fat_attn_bwd_stages",
     "fat_attn_bwd_noalloc", "fat_xattn_fwd", "fat_xattn_bwd", "fat_xattn_bwd_workspace_size",
@@ -71,6 +72,11 @@ def load(path: Optional[str] = None):
     S = ctypes.POINTER(_Shape)
     lib.fat_attn_fwd.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp]
     lib.fat_attn_fwd.restype = i32
+    lib.fat_attn_fwd_ws.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp,
+                                    vp, ctypes.c_size_t]
+    lib.fat_attn_fwd_ws.restype = i32
+    lib.fat_attn_fwd_workspace_size.argtypes = [S]
+    lib.fat_attn_fwd_workspace_size.restype = ctypes.c_size_t
     lib.fat_attn_bwd_workspace_size.argtypes = [S]
     lib.fat_attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fat_attn_bwd.argtypes = [S, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp,
@@ -167,9 +173,10 @@ def _check_tensor(name, t, dtype, ndim=None):
 def fat_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, bias_table=None, num_buckets: int = 0,
                  max_distance: int = 0, bidirectional: bool = True, alibi_slopes=None,
                  causal: bool = False, softmax_scale: float = 1.0, out=None, lse=None,
-                 stream=None):
+                 workspace=None, stream=None):
     """Forward pass. q, k, v: bf16 [T, H, d] (CUDA, contiguous); cu_seqlens: int32 [n+1] (CUDA).
-    Returns (out bf16 [T, H, d], lse fp32 [H, T])."""
+    workspace: device bytes for a split last wave (fat_attn_fwd_workspace_size); None allocates
+    what the shape uses, False runs without one. Returns (out bf16 [T, H, d], lse fp32 [H, T])."""
     import torch
     lib = load()
     T, H, d = q.shape
@@ -183,14 +190,29 @@ def fat_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, bias_table=None, num_buck
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     sh = _shape(T, cu_seqlens.numel() - 1, max_seqlen, H, d, _stream_ptr(stream, q.device))
+    args = (ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), int(num_buckets),
+            int(max_distance), int(bool(bidirectional)), _ptr(alibi_slopes), _ptr(cu_seqlens),
+            int(bool(causal)), float(softmax_scale), _ptr(out), _ptr(lse))
+    if workspace is None and not causal:
+        need = int(lib.fat_attn_fwd_workspace_size(ctypes.byref(sh)))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     with _on(q.device):
-        rc = lib.fat_attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table),
-                              int(num_buckets), int(max_distance), int(bool(bidirectional)),
-                              _ptr(alibi_slopes), _ptr(cu_seqlens), int(bool(causal)),
-                              float(softmax_scale), _ptr(out), _ptr(lse))
+        if workspace is None or workspace is False:
+            rc = lib.fat_attn_fwd(*args)
+        else:
+            rc = lib.fat_attn_fwd_ws(*args, _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()))
     if rc != 0:
         raise FatAttnError(rc, "fat_attn_fwd")
     return out, lse
+
+
+def fat_attn_fwd_workspace_size(total_tokens: int, num_seqs: int, max_seqlen: int,
+                                num_heads: int, head_dim: int) -> int:
+    """Device bytes that let the forward split its last wave for this shape (0: none)."""
+    sh = _shape(total_tokens, num_seqs, max_seqlen, num_heads, head_dim, None)
+    return int(load().fat_attn_fwd_workspace_size(ctypes.byref(sh)))
 
 
 def fat_attn_bwd_workspace_size(total_tokens: int, num_heads: int, head_dim: int,

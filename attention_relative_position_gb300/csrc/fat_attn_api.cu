@@ -636,6 +636,37 @@ int auto_splits(const XShape &x) {
   return (int)std::max<long long>(want, 1);
 }
 
+// Split last wave of the forward grid (one CTA per 256 query rows x head x document, one CTA
+// per SM): documents of equal length, no causal mask, a partial last wave of at most half the
+// SMs; its CTAs are each split into `splits` key ranges (at least two key tiles each) whose
+// partial rows a merge pass combines. bytes: the partial rows and lse the split needs.
+struct FwdTail {
+  long long first;
+  int splits, ntail, gx;
+  size_t o_bytes, bytes;
+};
+FwdTail fwd_tail_plan(const XShape &x) {
+  FwdTail t{0, 0, 0, 0, 0, 0};
+  if (x.n <= 0 || x.maxq <= 0 || x.maxk <= 0 || decode_row_count(x) <= 8) return t;
+  if ((long long)x.n * x.maxq != x.Tq || (long long)x.n * x.maxk != x.Tk) return t;
+  const int sms = sm_count();
+  if (sms <= 0) return t;
+  const int gx = (x.maxq + 255) / 256;
+  const long long items = (long long)gx * x.Hq * x.n;
+  const long long whole = items / sms * sms, ntail = items - whole;
+  const int nkv = (x.maxk + 127) / 128;
+  if (ntail == 0 || ntail > sms / 2) return t;
+  const int splits = (int)std::min<long long>(sms / ntail, nkv / 2);
+  if (splits < 2) return t;
+  t.first = whole;
+  t.splits = splits;
+  t.ntail = (int)ntail;
+  t.gx = gx;
+  t.o_bytes = align256((size_t)ntail * splits * 256 * x.d * 4);
+  t.bytes = t.o_bytes + align256((size_t)ntail * splits * 256 * 4);
+  return t;
+}
+
 int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
              const float *bias_table, int num_buckets, int max_distance, int bidirectional,
              const float *alibi_slopes, const int32_t *cu_q, const int32_t *cu_k, int causal,
@@ -655,6 +686,8 @@ int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) ||
         workspace_bytes < splitkv_bytes(x, splits))
       return FAT_EINVAL_SHAPE;
+  } else if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+    return FAT_EINVAL_SHAPE;
   }
   if (x.Tq == 0 || x.n == 0 || x.maxq == 0) return FAT_OK;
   rc = device_error_ptr(&p.err);
@@ -676,6 +709,17 @@ int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
   }
   const bool few_rows = decode_row_count(x) <= 8 &&
                         decode_eligible(x.d, (int)decode_row_count(x), x.Hq / x.Hkv, p.bias);
+  if (splits == 1 && workspace && !causal && !few_rows) {
+    const FwdTail t = fwd_tail_plan(x);
+    if (t.splits > 0 && workspace_bytes >= t.bytes) {
+      p.tail_first = t.first;
+      p.tail_splits = t.splits;
+      p.tail_gx = t.gx;
+      p.tail_ntail = t.ntail;
+      p.tail_o = static_cast<float *>(workspace);
+      p.tail_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + t.o_bytes);
+    }
+  }
   rc = cuda_rc(few_rows ? launch_decode(p, x.d, q, k, v, x.stream)
                         : launch_fwd(p, x.d, q, k, v, x.stream));
   if (rc || splits == 1) return rc;
@@ -969,6 +1013,25 @@ int fat_attn_fwd(const fat_shape_t *sh, const void *q, const void *k, const void
   if (rc) return rc;
   return fwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
                   cu_seqlens, cu_seqlens, causal, softmax_scale, out, lse, 1, nullptr, 0);
+}
+
+size_t fat_attn_fwd_workspace_size(const fat_shape_t *sh) {
+  XShape x{};
+  if (to_xshape(sh, &x)) return 0;
+  return fwd_tail_plan(x).bytes;
+}
+
+int fat_attn_fwd_ws(const fat_shape_t *sh, const void *q, const void *k, const void *v,
+                    const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                    const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                    float softmax_scale, void *out, float *lse, void *workspace,
+                    size_t workspace_bytes) {
+  XShape x{};
+  int rc = to_xshape(sh, &x);
+  if (rc) return rc;
+  return fwd_impl(x, q, k, v, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes,
+                  cu_seqlens, cu_seqlens, causal, softmax_scale, out, lse, 1, workspace,
+                  workspace_bytes);
 }
 
 int fat_xattn_fwd(const fat_xshape_t *xs, const void *q, const void *k, const void *v,

@@ -136,15 +136,21 @@ __device__ __forceinline__ void fwd_exp_pass(const uint32_t (&x)[4][32], uint64_
 // Rows that see no key (in this block's key range): out = 0 and lse = -inf, or, for a key range
 // of a split forward, a zero partial output with partial lse -inf. Threads thr, thr + nthr, ...
 // take rows row0 .. row0 + nrows - 1 (document-local) of query head h.
-template <int D>
+template <int D, bool TAIL>
 __device__ __forceinline__ void fwd_write_empty_rows(const FwdParams &p, int seq_start, int row0,
-                                                     int nrows, int h, int split,
+                                                     int nrows, int h, int split, int q0,
                                                      int thr = threadIdx.x,
                                                      int nthr = blockDim.x) {
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
   for (int i = thr; i < nrows; i += nthr) {
     const size_t row = (size_t)seq_start + row0 + i;
-    if (p.kv_splits == 1) {
+    if (TAIL) {  // partial rows of a split last-wave CTA
+      const size_t t = (size_t)blockIdx.x * 256 + (row0 - q0 + i);
+      float4 *dst = reinterpret_cast<float4 *>(p.tail_o + t * D);
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.tail_lse[t] = -INFINITY;
+    } else if (p.kv_splits == 1) {
       uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row * H + h) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -158,7 +164,9 @@ __device__ __forceinline__ void fwd_write_empty_rows(const FwdParams &p, int seq
   }
 }
 
-template <int D>
+// TAIL: the launch that takes a split last wave (FwdParams::tail_first); the main launch
+// (TAIL = false) leaves those CTAs out.
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(384, 1)
     fat_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -168,21 +176,36 @@ __global__ void __launch_bounds__(384, 1)
   // shared array itself so every derived pointer stays a shared-memory pointer
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int doc = blockIdx.z / p.kv_splits, split = blockIdx.z % p.kv_splits, h = blockIdx.y;
-  const int hk = h / p.seq.group;             // key/value head read by query head h
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first when causal
   const int T = p.seq.total_tokens, H = p.seq.num_heads;
+  int doc, split, h, qb;
+  if constexpr (TAIL) {  // split = this CTA's share of the key tiles
+    const long long cta = p.tail_first + blockIdx.x / p.tail_splits;
+    split = (int)(blockIdx.x % p.tail_splits);
+    h = (int)((cta / p.tail_gx) % H);
+    doc = (int)(cta / ((long long)p.tail_gx * H));
+    qb = p.tail_gx - 1 - (int)(cta % p.tail_gx);
+  } else {
+    doc = blockIdx.z / p.kv_splits;
+    split = blockIdx.z % p.kv_splits;
+    h = blockIdx.y;
+    qb = gridDim.x - 1 - blockIdx.x;  // longest rows first when causal
+    // the split last wave is another launch's
+    if (p.tail_splits > 0 &&
+        blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z) >=
+            p.tail_first)
+      return;
+  }
+  const int hk = h / p.seq.group;  // key/value head read by query head h
 
   const DocSpan span = doc_span(p.seq, doc);
   if (!span.ok) {
-    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    if (tid == 0 && qb == 0 && h == 0 && split == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
     return;
   }
   const int seq_start = span.sq, L = span.lq, seq_start_k = span.sk, Lk = span.lk;
   const int shift = span.shift;  // query p sits at key position p + shift
   // a document longer than the caller's bounds has rows or keys no block covers: reported
-  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && blockIdx.x == 0 && split == 0 &&
-      tid == 0)
+  if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && qb == 0 && split == 0 && tid == 0)
     atomicOr(p.err, FAT_DEVERR_SEQLENS);
   const int q0 = qb * 256;
   if (q0 >= L) return;  // whole CTA, before any barrier or TMEM allocation
@@ -190,8 +213,14 @@ __global__ void __launch_bounds__(384, 1)
   const int nkv_all = (Lk + 127) >> 7;
   // Key tiles Q tile t sees: all of them, or (causal) those up to the key position of its last
   // valid row; intersected with this block's key range [klo, khi) when the keys are split.
-  const int klo = split * p.split_tiles;
-  const int khi = min(nkv_all, klo + p.split_tiles);
+  int klo, khi;
+  if constexpr (TAIL) {
+    klo = (int)((long long)split * nkv_all / p.tail_splits);
+    khi = (int)((long long)(split + 1) * nkv_all / p.tail_splits);
+  } else {
+    klo = split * p.split_tiles;
+    khi = min(nkv_all, klo + p.split_tiles);
+  }
   auto visible = [&](int t) -> int {
     if (!p.causal) return nkv_all;
     const int last = min(L, q0 + 128 * t + 128) - 1 + shift;
@@ -201,7 +230,7 @@ __global__ void __launch_bounds__(384, 1)
   const int nkv1 = ntile == 2 ? max(0, min(khi, visible(1)) - klo) : 0;
   const int nkv_max = max(nkv0, nkv1);
   if (nkv_max == 0) {  // no key for any row of the block (in this key range): empty rows
-    fwd_write_empty_rows<D>(p, seq_start, q0, min(L - q0, 256), h, split);
+    fwd_write_empty_rows<D, TAIL>(p, seq_start, q0, min(L - q0, 256), h, split, q0);
     return;
   }
   // Causal rows take their key tiles from the diagonal backwards: the first tile holds each
@@ -620,7 +649,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       grid_dep_launch();  // a dependent grid (the backward preprocessing) may be scheduled
       if (nk == 0) {  // this tile sees no key (in this key range): empty rows, TMEM untouched
-        fwd_write_empty_rows<D>(p, seq_start, qs, min(L - qs, 128), h, split, r, 128);
+        fwd_write_empty_rows<D, TAIL>(p, seq_start, qs, min(L - qs, 128), h, split, q0, r, 128);
       } else {
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_ready + t, (nk - 1) & 1, wd));
         if (ok) {
@@ -629,7 +658,7 @@ __global__ void __launch_bounds__(384, 1)
           const bool valid = qrow < L;
           const float m_use = (m == -INFINITY) ? 0.f : m;
           const float lse_row = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
-          if (p.kv_splits == 1) {
+          if (!TAIL && p.kv_splits == 1) {
             __nv_bfloat16 *orow = p.out + ((size_t)(seq_start + qrow) * H + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -649,7 +678,9 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (valid && p.lse != nullptr) p.lse[(size_t)h * T + seq_start + qrow] = lse_row;
           } else {  // partial result of this key range, normalised, in fp32
-            float *orow = p.o_part + (((size_t)split * T + seq_start + qrow) * H + h) * D;
+            const size_t trow = (size_t)blockIdx.x * 256 + (qrow - q0);
+            float *orow = TAIL ? p.tail_o + trow * D
+                               : p.o_part + (((size_t)split * T + seq_start + qrow) * H + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -664,7 +695,12 @@ __global__ void __launch_bounds__(384, 1)
                                         __uint_as_float(o[4 * v4 + 3]) * inv_l);
               }
             }
-            if (valid) p.lse_part[((size_t)split * H + h) * T + seq_start + qrow] = lse_row;
+            if (valid) {
+              if (TAIL)
+                p.tail_lse[trow] = lse_row;
+              else
+                p.lse_part[((size_t)split * H + h) * T + seq_start + qrow] = lse_row;
+            }
           }
         }
       }
@@ -679,6 +715,104 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Merge of a split last wave: one warp per (split CTA row), the tail_splits partial rows (each
+// normalised, with its lse) combined as in the split-key merge below, written to out and lse.
+// Documents have equal length (the condition of the split), so row q of document doc is token
+// doc * max_seqlen + q.
+template <int D>
+__global__ void __launch_bounds__(256) fat_fwd_tail_combine_kernel(const FwdParams p) {
+  constexpr int CPL = D / 32;
+  const int T = p.seq.total_tokens, H = p.seq.num_heads, S = p.tail_splits;
+  const int L = p.seq.max_seqlen;
+  const int lane = threadIdx.x & 31;
+  const long long nrows = (long long)p.tail_ntail * 256;
+  const long long w0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long rw = w0; rw < nrows; rw += nw) {
+    const long long c = rw / 256;
+    const int row = (int)(rw % 256);
+    const long long cta = p.tail_first + c;
+    const int h = (int)((cta / p.tail_gx) % H);
+    const long long doc = cta / ((long long)p.tail_gx * H);
+    const int q = (p.tail_gx - 1 - (int)(cta % p.tail_gx)) * 256 + row;
+    if (q >= L) continue;
+    const long long tok = doc * L + q;
+    float m = -INFINITY;
+    for (int s = 0; s < S; ++s) m = fmaxf(m, p.tail_lse[(c * S + s) * 256 + row]);
+    float acc[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const size_t t = (size_t)(c * S + s) * 256 + row;
+        const float ls = p.tail_lse[t];
+        if (ls == -INFINITY) continue;
+        const float wgt = __expf(ls - m);
+        wsum += wgt;
+        const float *o = p.tail_o + t * D + lane * CPL;
+#pragma unroll
+        for (int i = 0; i < CPL; i += 2) {
+          const float2 v = *reinterpret_cast<const float2 *>(o + i);
+          acc[i] += wgt * v.x;
+          acc[i + 1] += wgt * v.y;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+    __nv_bfloat16 *orow = p.out + ((size_t)tok * H + h) * D + lane * CPL;
+    if constexpr (CPL == 2) {
+      *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    } else {
+      uint2 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(orow) = v;
+    }
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[(size_t)h * T + tok] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+  }
+}
+
+template <int D>
+int launch_fwd_t(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                 const CUtensorMap &mv, size_t smem, cudaStream_t stream) {
+  const dim3 grid((p.seq.max_seqlen + 255) / 256, p.seq.num_heads,
+                  p.seq.num_seqs * p.kv_splits);
+  // the register re-balancing needs the launch pool the split was designed for
+  cudaError_t e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, false>, smem,
+                                              FwdCfg<D>::NTHREADS, FwdCfg<D>::REGS_NEEDED);
+  if (e != cudaSuccess) return (int)e;  // reason recorded by prepare_kernel
+  fat_fwd_kernel<D, false><<<grid, FwdCfg<D>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
+  e = cudaGetLastError();
+  const long long tail_ctas = (long long)p.tail_ntail * p.tail_splits;
+  if (e == cudaSuccess && p.tail_splits > 0 && tail_ctas > 0) {
+    // the split last wave, then its merge (ordered by the stream)
+    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, true>, smem,
+                                    FwdCfg<D>::NTHREADS, FwdCfg<D>::REGS_NEEDED);
+    if (e != cudaSuccess) return (int)e;
+    fat_fwd_kernel<D, true><<<(unsigned)tail_ctas, FwdCfg<D>::NTHREADS, smem, stream>>>(
+        mq, mk, mv, p);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      const int blocks = (int)std::min<long long>(((long long)p.tail_ntail * 256 + 7) / 8,
+                                                  152LL * 8);
+      fat_fwd_tail_combine_kernel<D><<<blocks, 256, 0, stream>>>(p);
+      e = cudaGetLastError();
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, fat_fwd_kernel<D, false>);
+    char msg[160];
+    snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
+             cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
+             smem);
+    set_last_error("kernel launch", (int)e, msg);
+  }
+  return (int)e;
+}
+
 int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, const void *v,
                cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
@@ -688,35 +822,8 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
       make_tmap_thd(&mv, v, Tk, Hkv, head_dim, 128))
     return (int)cudaErrorInvalidValue;
   const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
-  dim3 grid((p.seq.max_seqlen + 255) / 256, H, p.seq.num_seqs * p.kv_splits);
-  // the register re-balancing needs the launch pool the split was designed for
-  cudaError_t e;
-  if (head_dim == 64) {
-    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<64>, smem, FwdCfg<64>::NTHREADS,
-                                    FwdCfg<64>::REGS_NEEDED);
-    if (e == cudaSuccess)
-      fat_fwd_kernel<64><<<grid, FwdCfg<64>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
-  } else {
-    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<128>, smem,
-                                    FwdCfg<128>::NTHREADS, FwdCfg<128>::REGS_NEEDED);
-    if (e == cudaSuccess)
-      fat_fwd_kernel<128><<<grid, FwdCfg<128>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
-  }
-  if (e != cudaSuccess) return (int)e;
-  e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    cudaFuncAttributes fa{};
-    if (head_dim == 64)
-      cudaFuncGetAttributes(&fa, fat_fwd_kernel<64>);
-    else
-      cudaFuncGetAttributes(&fa, fat_fwd_kernel<128>);
-    char msg[160];
-    snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
-             cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
-             smem);
-    set_last_error("kernel launch", (int)e, msg);
-  }
-  return (int)e;
+  return head_dim == 64 ? launch_fwd_t<64>(p, mq, mk, mv, smem, stream)
+                        : launch_fwd_t<128>(p, mq, mk, mv, smem, stream);
 }
 
 // Merge of a split forward's partial results, one warp per (query row, head): with partial lse

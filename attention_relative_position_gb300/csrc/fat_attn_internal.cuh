@@ -142,6 +142,14 @@ struct FwdParams {
   // merges them. kv_splits = 1: whole rows, out and lse written directly.
   int kv_splits, split_tiles;
   float *o_part, *lse_part;
+  // Balanced last wave (documents of equal length, no causal mask, kv_splits = 1): the CTAs
+  // from linear id tail_first on (x fastest in the (tail_gx, H, documents) grid) run as a second
+  // launch in which CTA t takes key-tile share t % tail_splits of CTA tail_first +
+  // t / tail_splits, writing its normalised partial rows to tail_o [t][256][d] and partial lse
+  // to tail_lse [t][256]; a merge pass writes out and lse. tail_splits = 0: no split.
+  long long tail_first;
+  int tail_splits, tail_gx, tail_ntail;
+  float *tail_o, *tail_lse;
 };
 
 struct BwdParams {

@@ -190,6 +190,14 @@ class Runner:
         nws = fa.fat_attn_bwd_workspace_size(w.total_tokens, w.num_heads, w.head_dim,
                                              len(w.seqlens), w.max_seqlen)
         self.ws = torch.empty(nws, dtype=torch.uint8, device=device)
+        nfws = fa.fat_attn_fwd_workspace_size(w.total_tokens, len(w.seqlens), w.max_seqlen,
+                                              w.num_heads, w.head_dim)
+        self.fws = torch.empty(nfws, dtype=torch.uint8, device=device) if nfws else False
+        # kernels one step launches: forward (+ split last wave and its merge), backward
+        # preprocess, main (+ split last wave), finalize
+        bws_min = fa.fat_attn_bwd_workspace_size(w.total_tokens, w.num_heads, w.head_dim)
+        self.launches_per_step = 4 + (0 if w.causal else (2 if nfws else 0) +
+                                      (1 if nws > bws_min else 0))
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.stream = torch.cuda.current_stream(device)
 
@@ -198,7 +206,7 @@ class Runner:
         whose main and finishing grids overlap the set-up of the grid before them)."""
         fa, x, w = self.fa, self.x, self.w
         fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, out=self.out,
-                        lse=self.lse, stream=self.stream, **self.kw)
+                        lse=self.lse, workspace=self.fws, stream=self.stream, **self.kw)
         fa.fat_attn_bwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, self.out,
                         self.lse, x["dout"], workspace=self.ws, dq=self.dq, dk=self.dk,
                         dv=self.dv, dbias_table=self.dtab, stream=self.stream, **self.kw)
@@ -209,7 +217,7 @@ class Runner:
         fa, x, w = self.fa, self.x, self.w
         events[0].record(self.stream)
         fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, out=self.out,
-                        lse=self.lse, stream=self.stream, **self.kw)
+                        lse=self.lse, workspace=self.fws, stream=self.stream, **self.kw)
         between = None
         if events is not None:
             def between(i):
@@ -225,7 +233,6 @@ class Runner:
     def flush_l2(self):
         self.flush.zero_()
 
-    LAUNCHES_PER_STEP = 4  # forward, backward preprocess, backward main, backward finalize
 
 
 def time_steps(r, steps, flush=True):
@@ -487,7 +494,7 @@ def quick_other(w, device, peaks, steps=10):
         floor = _time_ms(torch, lambda: one.zero_(), reps=50, warm=5)
         res["latency"] = {"fwd_us": round(statistics.median(per["fwd"]) * 1e3, 2),
                           "step_us": round(step_ms * 1e3, 2),
-                          "launches_per_step": Runner.LAUNCHES_PER_STEP,
+                          "launches_per_step": r.launches_per_step,
                           "launch_floor_us": round(floor * 1e3, 2),
                           "floor": "CUDA-event time of one one-element kernel on the same stream"}
     del r
@@ -732,7 +739,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic_for(f"{kname}<{w.head_dim}>@{w.name}"),
                      "algorithmic_flops_per_launch": kflops},
         "hbm": _guarded(hbm_figures, w, per, peaks["hbm_gbs"]),
-        "gpu_launches": steps * Runner.LAUNCHES_PER_STEP,
+        "gpu_launches": steps * r.launches_per_step,
         "timed_wall_s": round(wall, 4),
     }
     if clocks is not None:

@@ -96,6 +96,25 @@ int fat_attn_fwd(const fat_shape_t *shape, const void *q, const void *k, const v
                  const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
                  float softmax_scale, void *out, float *lse);
 
+/*
+ * fat_attn_fwd with a caller-owned device workspace (may be NULL). When every document has
+ * length max_seqlen (total_tokens = num_seqs * max_seqlen), there is no causal mask, and the
+ * forward grid (one CTA per 256 query rows x head x document, one per SM) ends in a partial
+ * wave, a workspace of at least fat_attn_fwd_workspace_size(shape) bytes (256-byte aligned;
+ * contents need not be initialised) lets the library split that wave's CTAs along the keys
+ * and merge their partial rows in a second pass, so the last wave no longer leaves most SMs
+ * idle. A smaller workspace (or NULL) gives the fat_attn_fwd schedule; results agree up to the
+ * rounding of the merge. Errors as fat_attn_fwd; a misaligned workspace: FAT_EINVAL_SHAPE.
+ */
+int fat_attn_fwd_ws(const fat_shape_t *shape, const void *q, const void *k, const void *v,
+                    const float *bias_table, int num_buckets, int max_distance, int bidirectional,
+                    const float *alibi_slopes, const int32_t *cu_seqlens, int causal,
+                    float softmax_scale, void *out, float *lse, void *workspace,
+                    size_t workspace_bytes);
+/* Bytes fat_attn_fwd_ws uses for this shape on the current device (its SM count sets the
+   waves): 0 when the shape has no split last wave. */
+size_t fat_attn_fwd_workspace_size(const fat_shape_t *shape);
+
 /* Bytes of device workspace for fat_attn_bwd at its fastest. The layout starts with an fp32 dQ
    accumulator [T, H, d] and the fp32 row statistics D = rowsum(dout * out) [H, T], each
    256-byte aligned: that prefix is the minimum every backward call accepts. Shapes whose
