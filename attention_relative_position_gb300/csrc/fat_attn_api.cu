@@ -1161,9 +1161,18 @@ int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_d
 }  // extern "C"
 
 namespace fat {
+// Both device bucket functions the kernels use: the staged binary search (bias tables) and the
+// direct count (saturated sides, the few-row kernel); -1 where they disagree.
 __global__ void fat_debug_buckets_kernel(const BiasParams b, long long lo, int n, int32_t *out) {
+  __shared__ int thr_s[kMaxThresholds];
+  for (int i = threadIdx.x; i < b.n_thr; i += blockDim.x) thr_s[i] = b.thr[i];
+  __syncthreads();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) out[i] = t5_bucket_dev((int)(lo + i), b);
+  if (i < n) {
+    const int direct = t5_bucket_dev((int)(lo + i), b);
+    const int staged = t5_bucket_staged((int)(lo + i), b, thr_s);
+    out[i] = direct == staged ? staged : -1;
+  }
 }
 int launch_debug_buckets(const BiasParams &b, long long lo, int n, int32_t *out,
                          cudaStream_t stream) {

@@ -100,9 +100,10 @@ constexpr int kItemSlots = 8;
 
 template <int D, int NS>
 size_t bwd_smem_bytes_t(int lut_len) {
-  // lut, diag (fp32), bucket ids (bytes), one table column (256 fp32), the item ring
+  // lut, diag (fp32), bucket ids (bytes), one table column (256 fp32), the staged thresholds
+  // (64 int), the item ring
   return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 9 + 16 + 1024 +
-         kItemSlots * sizeof(ItemSlot);
+         kMaxThresholds * 4 + kItemSlots * sizeof(ItemSlot);
 }
 // Three Q/dO stages when they fit next to the bias table, else two.
 int bwd_stages(int head_dim, int lut_len) {
@@ -377,7 +378,8 @@ __global__ void __launch_bounds__(640, 1)
   float *diag = lut + p.bias.lut_len;
   uint8_t *lbk = reinterpret_cast<uint8_t *>(diag + p.bias.lut_len);
   float *tcol_s = reinterpret_cast<float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15));
-  ItemSlot *slots = reinterpret_cast<ItemSlot *>(tcol_s + 256);
+  int *thr_s = reinterpret_cast<int *>(tcol_s + 256);
+  ItemSlot *slots = reinterpret_cast<ItemSlot *>(thr_s + kMaxThresholds);
 
   // The producer warp sets up the barriers and starts the first item's first step (K, V, the
   // first Q/dO tile and the loads of its lse) before the rest of the block builds its tables, so
@@ -448,12 +450,17 @@ __global__ void __launch_bounds__(640, 1)
   // bias table of the first item's head; bucket ids (head-independent) for the table gradient
   // and for rebuilding the table when the head changes
   const bool has_table = p.bias.table != nullptr;
-  for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
-    const int delta = p.bias.lut_lo + i;
-    const int b = has_table ? t5_bucket_dev(delta, p.bias) : 0;
-    lut[i] = bias_log2_bucket_dev(b, delta, first.h, H, p.bias);
-    diag[i] = 0.f;
-    lbk[i] = static_cast<uint8_t>(b);
+  bias_stage(p.bias, first.h, H, thr_s, tcol_s, tid, C::NTHREADS);
+  {
+    const float slope = p.bias.slopes != nullptr ? __ldg(p.bias.slopes + first.h) : 0.f;
+    __syncthreads();
+    for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
+      const int delta = p.bias.lut_lo + i;
+      const int b = has_table ? t5_bucket_staged(delta, p.bias, thr_s) : 0;
+      lut[i] = bias_log2_staged(b, delta, slope, p.bias, tcol_s);
+      diag[i] = 0.f;
+      lbk[i] = static_cast<uint8_t>(b);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1174,11 +1181,20 @@ __global__ void __launch_bounds__(640, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
-    lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
-    if (do_dbias) {
-      diag[i] = 0.f;
-      lbk[i] = static_cast<uint8_t>(t5_bucket_dev(p.bias.lut_lo + i, p.bias));
+  {  // bias table of head h; bucket ids and zeroed per-delta sums for the table gradient
+    float *col_s = reinterpret_cast<float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15));
+    int *thr_s = reinterpret_cast<int *>(col_s + 256);
+    bias_stage(p.bias, h, H, thr_s, col_s, tid, C::NTHREADS);
+    const float slope = p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) : 0.f;
+    __syncthreads();
+    for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
+      const int delta = p.bias.lut_lo + i;
+      const int b = p.bias.table ? t5_bucket_staged(delta, p.bias, thr_s) : 0;
+      lut[i] = bias_log2_staged(b, delta, slope, p.bias, col_s);
+      if (do_dbias) {
+        diag[i] = 0.f;
+        lbk[i] = static_cast<uint8_t>(b);
+      }
     }
   }
   tc_fence_before();

@@ -61,9 +61,10 @@ struct FwdCfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V (MN-major)
 };
 
+// the bias table, then the staged thresholds (64 int) and table column (256 fp32)
 size_t fwd_smem_bytes(int head_dim, int lut_len) {
   size_t base = head_dim == 64 ? (size_t)FwdCfg<64>::OFF_LUT : (size_t)FwdCfg<128>::OFF_LUT;
-  return 1024 + base + (size_t)lut_len * 4;
+  return 1024 + base + (((size_t)lut_len * 4 + 15) & ~(size_t)15) + kMaxThresholds * 4 + 256 * 4;
 }
 
 // Load the S row from TMEM (all four 32-column loads in flight), form
@@ -302,8 +303,18 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS)
-    lut[i] = bias_log2_dev(p.bias.lut_lo + i, h, H, p.bias);
+  {  // bias table of head h over the block's deltas
+    int *thr_s = reinterpret_cast<int *>(sm + C::OFF_LUT + ((p.bias.lut_len * 4 + 15) & ~15));
+    float *col_s = reinterpret_cast<float *>(thr_s + kMaxThresholds);
+    bias_stage(p.bias, h, H, thr_s, col_s, tid, C::NTHREADS);
+    const float slope = p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) : 0.f;
+    __syncthreads();
+    for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
+      const int delta = p.bias.lut_lo + i;
+      const int bk = p.bias.table ? t5_bucket_staged(delta, p.bias, thr_s) : 0;
+      lut[i] = bias_log2_staged(bk, delta, slope, p.bias, col_s);
+    }
+  }
   if (tid == 0) {
     *reinterpret_cast<Watchdog *>(sm + C::OFF_WD) =
         Watchdog{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};

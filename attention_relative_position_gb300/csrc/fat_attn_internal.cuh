@@ -105,6 +105,45 @@ __device__ __forceinline__ float bias_log2_dev(int delta, int h, int H, const Bi
   return bias_log2_bucket_dev(b.table ? t5_bucket_dev(delta, b) : 0, delta, h, H, b);
 }
 
+// Building a block's bias table over delta without a global load per entry: the thresholds and
+// head h's table column are first staged in shared memory (bias_stage, one load per value, all
+// in flight together), then each entry's bucket is a binary search over the staged thresholds
+// (the same integer function as t5_bucket_dev: the count of thresholds <= n) and its bias the
+// same arithmetic as bias_log2_bucket_dev.
+__device__ __forceinline__ void bias_stage(const BiasParams &b, int h, int H, int *thr_s,
+                                           float *col_s, int tid, int nthreads) {
+  for (int i = tid; i < b.n_thr; i += nthreads) thr_s[i] = b.thr[i];
+  if (b.table)
+    for (int i = tid; i < b.nb; i += nthreads) col_s[i] = __ldg(b.table + (size_t)i * H + h);
+}
+__device__ __forceinline__ int t5_bucket_staged(int delta, const BiasParams &b,
+                                                const int *thr_s) {
+  int off = 0, n;
+  if (b.bidir) {
+    off = delta > 0 ? b.nbh : 0;
+    n = delta < 0 ? -delta : delta;
+  } else {
+    n = delta < 0 ? -delta : 0;
+  }
+  if (n < b.me) return off + n;
+  int lo = 0, hi = b.n_thr;  // thresholds ascend: the first index whose threshold exceeds n
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (thr_s[mid] <= n)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return off + b.me + lo;
+}
+__device__ __forceinline__ float bias_log2_staged(int bucket, int delta, float slope,
+                                                  const BiasParams &b, const float *col_s) {
+  float v = 0.f;
+  if (b.table) v += col_s[bucket];
+  if (b.slopes) v -= slope * (float)(delta < 0 ? -delta : delta);
+  return v * kLog2e;
+}
+
 // Closed-form bias on the far sides, in log2 units: bias(delta) = c + k * delta.
 struct FarBias {
   float c_pos, k_pos, c_neg, k_neg;

@@ -14,8 +14,10 @@ extern "C" {
 
 /*
  * Writes, for delta = delta_lo .. delta_lo + n - 1, the T5 bucket id the attention kernels use
- * (same device function and host thresholds) into out_dev[0 .. n-1] (device int32). Asynchronous
- * on `stream`. Errors as in fat_attn.h (FAT_EINVAL_BUCKETS for bad bucket arguments).
+ * (same device functions and host thresholds) into out_dev[0 .. n-1] (device int32): the kernels
+ * compute it two ways (a binary search over thresholds staged in shared memory for their bias
+ * tables, a direct count elsewhere); an entry where the two disagree is -1. Asynchronous on
+ * `stream`. Errors as in fat_attn.h (FAT_EINVAL_BUCKETS for bad bucket arguments).
  */
 int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_distance,
                            int bidirectional, int32_t *out_dev, void *stream);
