@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only: no e2e, clocks, CPU baseline or extra workloads "
                          "(for profiler launch lists)")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="only the cross-attention, decode and RoPE figures, as one JSON line (for "
+                         "profiling those kernels)")
     ap.add_argument("--aux-kernels", action="store_true",
                     help="only the RMSNorm and cross-entropy figures, as one JSON line (for "
                          "profiling those kernels)")
@@ -677,6 +680,12 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.set_device(device)
         if rank == 0:
             print(json.dumps({"aux_kernels": aux_kernels(device, load_peaks()[0])}), flush=True)
+        return
+    if args.next_rows:
+        device = f"cuda:{local_rank}"
+        torch.cuda.set_device(device)
+        if rank == 0:
+            print(json.dumps({"next_rows": next_rows(device, load_peaks()[0])}), flush=True)
         return
     if world > 1:
         dist.barrier()
