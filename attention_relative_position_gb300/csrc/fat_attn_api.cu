@@ -79,7 +79,7 @@ int check_buckets(int nb, int md, int bidir, int *nbh_out) {
   return FAT_OK;
 }
 
-int thresholds(int nbh, int md, int32_t *thr, int *count, int *sat) {
+int thresholds_exact(int nbh, int md, int32_t *thr, int *count, int *sat) {
   const int me = nbh / 2, E = nbh - me;
   for (int t = 1; t < E; ++t) {
     long long lo = me, hi = md;  // predicate false below the answer, true at md
@@ -94,6 +94,43 @@ int thresholds(int nbh, int md, int32_t *thr, int *count, int *sat) {
   }
   *count = E - 1;
   *sat = E >= 2 ? thr[E - 2] : me;
+  return FAT_OK;
+}
+
+// The thresholds depend on (buckets per side, max distance) only, and their exact big-integer
+// search costs tens of microseconds of host time: computed once per pair and kept (a few
+// entries, replaced in turn), so a call pays a lookup.
+int thresholds(int nbh, int md, int32_t *thr, int *count, int *sat) {
+  struct Entry {
+    int nbh, md, count, sat;
+    int32_t thr[kMaxThresholds];
+  };
+  constexpr int kEntries = 16;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].nbh == nbh && cache[i].md == md) {
+        std::copy(cache[i].thr, cache[i].thr + cache[i].count, thr);
+        *count = cache[i].count;
+        *sat = cache[i].sat;
+        return FAT_OK;
+      }
+  }
+  Entry e{};
+  e.nbh = nbh;
+  e.md = md;
+  const int rc = thresholds_exact(nbh, md, e.thr, &e.count, &e.sat);
+  if (rc) return rc;
+  std::copy(e.thr, e.thr + e.count, thr);
+  *count = e.count;
+  *sat = e.sat;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = e;
+  next = (next + 1) % kEntries;
+  used = used < kEntries ? used + 1 : used;
   return FAT_OK;
 }
 
