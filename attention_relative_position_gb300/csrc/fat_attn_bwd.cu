@@ -791,7 +791,8 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     int ii = 0, gs = 0;
     WorkItem w = first;
-    FarBias fb = far_bias_dev(w.h, H, p.bias);
+    FarBias fb = far_bias_staged(p.bias, thr_s, tcol_s,
+                                 has_slopes ? __ldg(p.bias.slopes + w.h) : 0.f);
     do {
       const int krow = w.ks + r;
       const bool row_valid = krow < w.Lk;
@@ -1393,7 +1394,10 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tDQ = tmem + lane_off + C::COL_DQ + 16 * wg;  // this warpgroup's dQ quarter
     const int krow = ks + r;
     const bool row_valid = krow < Lk;
-    const FarBias fb = far_bias_dev(h, H, p.bias);
+    const FarBias fb = far_bias_staged(
+        p.bias, reinterpret_cast<const int *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15) + 1024),
+        reinterpret_cast<const float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15)),
+        p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) : 0.f);
     const bool has_slopes = p.bias.slopes != nullptr;
 
     // dQ tile `it` (quarter of its 64 columns) into the fp32 accumulator

@@ -314,11 +314,12 @@ __global__ void __launch_bounds__(384, 1)
       const int bk = p.bias.table ? t5_bucket_staged(delta, p.bias, thr_s) : 0;
       lut[i] = bias_log2_staged(bk, delta, slope, p.bias, col_s);
     }
-  }
-  if (tid == 0) {
-    *reinterpret_cast<Watchdog *>(sm + C::OFF_WD) =
-        Watchdog{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
-    *reinterpret_cast<FarBias *>(sm + C::OFF_WD + 32) = far_bias_dev(h, H, p.bias);
+    if (tid == 0) {
+      *reinterpret_cast<Watchdog *>(sm + C::OFF_WD) =
+          Watchdog{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+      *reinterpret_cast<FarBias *>(sm + C::OFF_WD + 32) =
+          far_bias_staged(p.bias, thr_s, col_s, slope);
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -162,6 +162,22 @@ __device__ __forceinline__ FarBias far_bias_dev(int h, int H, const BiasParams &
   return f;
 }
 
+// far_bias_dev from the staged thresholds and table column (no global load but the slope's)
+__device__ __forceinline__ FarBias far_bias_staged(const BiasParams &b, const int *thr_s,
+                                                   const float *col_s, float slope) {
+  FarBias f{0.f, 0.f, 0.f, 0.f};
+  if (b.table) {
+    f.c_pos = col_s[t5_bucket_staged(b.sat_pos, b, thr_s)] * kLog2e;
+    f.c_neg = col_s[t5_bucket_staged(-b.sat_neg, b, thr_s)] * kLog2e;
+  }
+  if (b.slopes) {
+    const float s = slope * kLog2e;
+    f.k_pos = -s;
+    f.k_neg = s;
+  }
+  return f;
+}
+
 // ---------------------------------------------------------------------------------------------
 // host-side launch descriptors (filled by the API layer)
 // ---------------------------------------------------------------------------------------------

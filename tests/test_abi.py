@@ -56,6 +56,19 @@ def test_thresholds_are_exact(lib, nb, md, bidir):
     assert sat == (want[-1] if want else nbh // 2)
 
 
+def test_threshold_cache_returns_exact_values_after_eviction(lib):
+    """The library keeps the thresholds of a few (buckets, distance) pairs; a run over more
+    pairs than it keeps, twice, must return the exact values every time (first computation,
+    cached copy, recomputation after the entry was replaced)."""
+    pairs = [(16 + 2 * (i % 8), 40 + 37 * i, True) for i in range(24)]
+    for _ in range(2):
+        for nb, md, bidir in pairs:
+            thr, sat = fa.fat_attn_bucket_thresholds(nb, md, bidir)
+            want = exact_thresholds(nb // 2, md)
+            assert thr == want, (nb, md)
+            assert sat == (want[-1] if want else nb // 4)
+
+
 def test_known_saturation_distances(lib):
     # thresholds derived by hand in tests/golden/t5_buckets.txt
     assert fa.fat_attn_bucket_thresholds(32, 128, True) == ([12, 16, 23, 32, 46, 64, 91], 91)
