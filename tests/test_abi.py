@@ -117,6 +117,22 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, _shape(T=0, n=0, maxL=0)) == 0
 
 
+def test_fwd_ws_argument_errors(lib):
+    def fwd_ws(sh, ws, wsb, **kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, cu=FAKE, causal=0)
+        a.update(kw)
+        return lib.fat_attn_fwd_ws(ctypes.byref(sh), a["q"], a["k"], a["v"], None, 0, 0, 1, None,
+                                   a["cu"], a["causal"], 1.0, FAKE, FAKE, ws, wsb)
+    assert fwd_ws(_shape(), FAKE, 1 << 20, q=None) == -1
+    assert fwd_ws(_shape(d=96), FAKE, 1 << 20) == -2
+    assert fwd_ws(_shape(), FAKE + 16, 1 << 20) == -2  # the workspace must be 256-byte aligned
+    assert fwd_ws(_shape(T=0, n=0, maxL=0), None, 0) == 0  # nothing to do
+    # the split needs the device's SM count: without a device no shape has one
+    assert lib.fat_attn_fwd_workspace_size(ctypes.byref(_shape(T=16384, n=1, maxL=16384,
+                                                               H=12))) == 0
+    assert lib.fat_attn_fwd_workspace_size(None) == 0
+
+
 def test_bwd_argument_errors(lib):
     sh = _shape()
     need = lib.fat_attn_bwd_workspace_size(ctypes.byref(sh))

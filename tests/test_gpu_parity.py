@@ -278,3 +278,40 @@ def test_split_last_wave_matches_whole_ctas():
         err = (u - v).abs() - 2 ** -8 * v.abs()
         assert (err <= 1e-3 * v.abs().max()).all(), (name, err.max().item())
     torch.testing.assert_close(g1[3], g2[3], rtol=1e-4, atol=1e-3)
+
+
+def test_split_schedules_fall_back_without_room():
+    """Equal documents without a causal mask, grids of less than a wave: a forward workspace
+    smaller than fat_attn_fwd_workspace_size runs the one-launch schedule (bit-identical to no
+    workspace), and a backward given only the minimum workspace does not split either (dK, dV
+    bit-identical to the stage calls, which never split)."""
+    w = wl.Workload("equal_docs_fallback_d128", (520,) * 3, 4, 128, 1.0, (32, 128, True), False,
+                    False, 0.3, seed=27)
+    x = wl.make_inputs(w, device="cuda")
+    kw = dict(bias_table=x["table"], num_buckets=32, max_distance=128, bidirectional=True,
+              causal=False, softmax_scale=w.scale)
+    T, H, d = x["q"].shape
+    need = fa.fat_attn_fwd_workspace_size(T, 3, w.max_seqlen, H, d)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    o1, l1 = fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen,
+                             workspace=False, **kw)
+    o2, l2 = fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen,
+                             workspace=small, **kw)
+    o3, l3 = fa.fat_attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert ((o1.float() - o3.float()).abs() <= 2e-2 + 2 ** -8 * o1.float().abs()).all()
+    minimum = fa.fat_attn_bwd_workspace_size(T, H, d)
+    assert fa.fat_attn_bwd_workspace_size(T, H, d, 3, w.max_seqlen) > minimum
+    ws = torch.empty(minimum, dtype=torch.uint8, device="cuda")
+    g1 = fa.fat_attn_bwd(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, o1, l1, x["dout"],
+                         workspace=ws, **kw)
+    g2 = fa.fat_attn_bwd_stages(x["q"], x["k"], x["v"], x["cu_seqlens"], w.max_seqlen, o1, l1,
+                                x["dout"], torch.empty_like(ws), torch.empty_like(x["q"]),
+                                torch.empty_like(x["q"]), torch.empty_like(x["q"]),
+                                dbias_table=torch.empty_like(x["table"]), **kw)
+    torch.cuda.synchronize()
+    assert fa.fat_attn_get_device_error() == 0
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    torch.testing.assert_close(g1[0].float(), g2[0].float(), rtol=2 ** -7, atol=1e-3)
