@@ -686,6 +686,7 @@ FwdTail fwd_tail_plan(const XShape &x) {
   FwdTail t{0, 0, 0, 0, 0, 0};
   if (x.n <= 0 || x.maxq <= 0 || x.maxk <= 0 || decode_row_count(x) <= 8) return t;
   if ((long long)x.n * x.maxq != x.Tq || (long long)x.n * x.maxk != x.Tk) return t;
+  if (fwd_tiles_per_cta(x.d, x.maxq) == 1) return t;  // one-tile CTAs, two per SM: not planned
   const int sms = sm_count();
   if (sms <= 0) return t;
   const int gx = (x.maxq + 255) / 256;
@@ -716,7 +717,7 @@ int fwd_impl(const XShape &x, const void *q, const void *k, const void *v,
   FwdParams p{};
   int rc = fill_bias(&p.bias, bias_table, num_buckets, max_distance, bidirectional, alibi_slopes);
   if (rc) return rc;
-  if (fwd_smem_bytes(x.d, p.bias.lut_len) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
+  if (fwd_smem_bytes(x.d, p.bias.lut_len, 2) > (size_t)kSmemLimit) return FAT_EUNSUPPORTED;
   if (splits < 1 || splits > 64 || (long long)x.n * splits > 65535) return FAT_EUNSUPPORTED;
   if (splits > 1) {
     if (!workspace) return FAT_EINVAL_NULL;

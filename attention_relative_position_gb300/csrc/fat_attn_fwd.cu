@@ -5,7 +5,8 @@
 // P = softmax(S') computed cumulatively (online), O = P V, and O is written back once.
 //
 // GB300 design (one CTA = one document x head x 256 query rows = two 128-row Q tiles; three
-// warpgroups, so that every SM sub-partition holds one warp of each):
+// warpgroups, so that every SM sub-partition holds one warp of each; short documents at d = 64
+// use CTAs of one Q tile, two per SM, with the roles below renumbered):
 //   warp 8      TMA producer: Q tiles once, K/V tiles through an NS-stage shared-memory ring.
 //   warps 9-10  MMA issuers: S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05.mma, accumulators
 //               in tensor memory (TMEM). d = 64: one issuing thread per Q tile, P_t in its own
@@ -28,42 +29,57 @@
 
 namespace fat {
 
-template <int D>
+// NT = Q tiles (128 rows each, one softmax warpgroup each) per CTA. NT = 2: one CTA per SM, both
+// tiles share every K/V tile (long documents). NT = 1 (d = 64, short documents): half the
+// threads, tensor memory and shared memory, so two CTAs share an SM and one's set-up, first
+// loads and epilogue overlap the other's steps.
+template <int D, int NT = 2>
 struct FwdCfg {
+  static_assert(NT == 2 || (NT == 1 && D == 64), "one-tile CTAs are built for d = 64");
   static constexpr int DB = D / 64;           // 64-channel blocks (one 128-byte swizzle row)
   static constexpr int BLK = 128 * 128;       // bytes: 128 rows x 64 bf16
   static constexpr int TILE = DB * BLK;       // bytes: 128 rows x D bf16
-  static constexpr int NS = (D == 64) ? 3 : 2;
+  static constexpr int NS = (D == 64 && NT == 2) ? 3 : 2;
+  static constexpr int ROWS = 128 * NT;       // query rows per CTA
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_K = OFF_Q + NT * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
   // the watchdog record and the far-side bias constants (read on slow paths / once per step)
   static constexpr int OFF_WD = OFF_BAR + 256;
   static constexpr int OFF_LUT = OFF_WD + 64;
   static_assert((1 + 4 * NS + 12) * 8 + 8 <= 256, "barrier block");
-  static constexpr int NTHREADS = 384;
+  // warps 0 .. 4 NT - 1: softmax warpgroups; then the TMA producer, the MMA issuer(s) (the
+  // first also allocates tensor memory) and idle warps completing the last warpgroup
+  static constexpr int NTHREADS = 128 * NT + 128;
+  static constexpr int MIN_BLOCKS = NT == 1 ? 2 : 1;  // CTAs per SM
+  static constexpr int WARP_PROD = 4 * NT, WARP_MMA = WARP_PROD + 1;
   // setmaxnreg moves registers within what the block was launched with (NTHREADS x the
-  // per-thread count of the launch bound): the split (two softmax warpgroups at REG_SM, one at
+  // per-thread count of the launch bound): the split (softmax warpgroups at REG_SM, the other at
   // REG_OTHER) must fit that pool, or the increase waits forever. The launcher also checks it
   // against the compiled count before the first launch.
-  static constexpr int REG_SM = 216, REG_OTHER = 72;
-  static constexpr int REGS_NEEDED = 256 * REG_SM + 128 * REG_OTHER;
-  static_assert(REGS_NEEDED <= NTHREADS * ((65536 / NTHREADS) & ~7), "register split");
-  // TMEM columns: S_t at 128 t, O_t at 256 + O_STRIDE t. With d = 64 the O_t take 64 columns
-  // each and P_t (bf16 pairs) gets its own 64 columns at 384 + 64 t, so S_t of the next key tile
-  // can be computed while P_t is still being produced and consumed; with d = 128 P_t is written
-  // over S_t.
+  static constexpr int REG_SM = NT == 2 ? 216 : 200, REG_OTHER = NT == 2 ? 72 : 56;
+  static constexpr int REGS_NEEDED = 128 * NT * REG_SM + 128 * REG_OTHER;
+  static_assert(REGS_NEEDED <= NTHREADS * ((65536 / (NTHREADS * MIN_BLOCKS)) & ~7),
+                "register split");
+  // TMEM columns: S_t at 128 t, O_t at 128 NT + O_STRIDE t. With d = 64 the O_t take 64
+  // columns each and P_t (bf16 pairs) gets its own 64 columns after them, so S_t of the next key
+  // tile can be computed while P_t is still being produced and consumed; with d = 128 P_t is
+  // written over S_t.
   static constexpr bool SEP_P = (D == 64);
-  static constexpr uint32_t COL_S0 = 0, COL_O0 = 256, O_STRIDE = SEP_P ? 64 : 128, COL_P0 = 384;
-  static_assert(!SEP_P || COL_O0 + 2 * O_STRIDE <= COL_P0, "TMEM column budget");
+  static constexpr uint32_t COL_S0 = 0, COL_O0 = 128 * NT, O_STRIDE = SEP_P ? 64 : 128;
+  static constexpr uint32_t COL_P0 = COL_O0 + NT * O_STRIDE;
+  static constexpr uint32_t TMEM_COLS = NT == 2 ? 512 : 256;
+  static_assert(COL_P0 + (SEP_P ? 64 * NT : 0) <= TMEM_COLS, "TMEM column budget");
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major), K (K-major)
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V (MN-major)
 };
 
 // the bias table, then the staged thresholds (64 int) and table column (256 fp32)
-size_t fwd_smem_bytes(int head_dim, int lut_len) {
-  size_t base = head_dim == 64 ? (size_t)FwdCfg<64>::OFF_LUT : (size_t)FwdCfg<128>::OFF_LUT;
+size_t fwd_smem_bytes(int head_dim, int lut_len, int nt) {
+  size_t base = head_dim == 64 ? (nt == 1 ? (size_t)FwdCfg<64, 1>::OFF_LUT
+                                          : (size_t)FwdCfg<64>::OFF_LUT)
+                               : (size_t)FwdCfg<128>::OFF_LUT;
   return 1024 + base + (((size_t)lut_len * 4 + 15) & ~(size_t)15) + kMaxThresholds * 4 + 256 * 4;
 }
 
@@ -167,11 +183,11 @@ __device__ __forceinline__ void fwd_write_empty_rows(const FwdParams &p, int seq
 
 // TAIL: the launch that takes a split last wave (FwdParams::tail_first); the main launch
 // (TAIL = false) leaves those CTAs out.
-template <int D, bool TAIL>
-__global__ void __launch_bounds__(384, 1)
+template <int D, bool TAIL, int NT = 2>
+__global__ void __launch_bounds__(FwdCfg<D, NT>::NTHREADS, FwdCfg<D, NT>::MIN_BLOCKS)
     fat_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (the 128-byte swizzle atoms need it), reached by indexing the
   // shared array itself so every derived pointer stays a shared-memory pointer
@@ -185,6 +201,29 @@ __global__ void __launch_bounds__(384, 1)
     h = (int)((cta / p.tail_gx) % H);
     doc = (int)(cta / ((long long)p.tail_gx * H));
     qb = p.tail_gx - 1 - (int)(cta % p.tail_gx);
+  } else if (NT == 1 && p.flat) {
+    // the last document whose first block id is <= this one (ids rise with the document); the
+    // block within it is reversed below (longest rows first when causal)
+    const int b = blockIdx.x;
+    int lo = 0, hi = p.seq.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((__ldg(p.seq.cu_seqlens + mid) >> 7) + mid <= b)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    doc = lo;
+    split = 0;
+    h = blockIdx.y;
+    qb = b - ((__ldg(p.seq.cu_seqlens + lo) >> 7) + lo);
+    if (b == 0 && h == 0) {  // the whole cu_seqlens array, once (a corrupt one may hide rows)
+      const int *cu = p.seq.cu_seqlens;
+      for (int i = threadIdx.x; i < p.seq.num_seqs; i += blockDim.x)
+        if (__ldg(cu + i) < 0 || __ldg(cu + i + 1) < __ldg(cu + i) ||
+            __ldg(cu + i + 1) > p.seq.total_tokens)
+          atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    }
   } else {
     doc = blockIdx.z / p.kv_splits;
     split = blockIdx.z % p.kv_splits;
@@ -208,9 +247,14 @@ __global__ void __launch_bounds__(384, 1)
   // a document longer than the caller's bounds has rows or keys no block covers: reported
   if ((L > p.seq.max_seqlen || Lk > p.seq.max_seqlen_k) && qb == 0 && split == 0 && tid == 0)
     atomicOr(p.err, FAT_DEVERR_SEQLENS);
-  const int q0 = qb * 256;
+  if (NT == 1 && !TAIL && p.flat) {
+    const int nblk = (L + 127) >> 7;
+    if (qb >= nblk) return;
+    qb = nblk - 1 - qb;
+  }
+  const int q0 = qb * C::ROWS;
   if (q0 >= L) return;  // whole CTA, before any barrier or TMEM allocation
-  const int ntile = (q0 + 128 < L) ? 2 : 1;
+  const int ntile = (NT == 2 && q0 + 128 < L) ? 2 : 1;
   const int nkv_all = (Lk + 127) >> 7;
   // Key tiles Q tile t sees: all of them, or (causal) those up to the key position of its last
   // valid row; intersected with this block's key range [klo, khi) when the keys are split.
@@ -231,7 +275,7 @@ __global__ void __launch_bounds__(384, 1)
   const int nkv1 = ntile == 2 ? max(0, min(khi, visible(1)) - klo) : 0;
   const int nkv_max = max(nkv0, nkv1);
   if (nkv_max == 0) {  // no key for any row of the block (in this key range): empty rows
-    fwd_write_empty_rows<D, TAIL>(p, seq_start, q0, min(L - q0, 256), h, split, q0);
+    fwd_write_empty_rows<D, TAIL>(p, seq_start, q0, min(L - q0, C::ROWS), h, split, q0);
     return;
   }
   // Causal rows take their key tiles from the diagonal backwards: the first tile holds each
@@ -262,7 +306,7 @@ __global__ void __launch_bounds__(384, 1)
   // The producer thread sets up the barriers and starts the first copies (Q, K_0, V_0) before
   // the block builds its bias table, so the load latency overlaps it.
   const bool early = !(p.debug_flags & 1);
-  if (warp == 8 && lane == 0) {
+  if (warp == C::WARP_PROD && lane == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(k_full + s, 1);
@@ -299,8 +343,8 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(&tm_v, v_full, sV + b * C::BLK, 64 * b, hk, seq_start_k + 128 * kt0);
     }
   }
-  if (warp == 9) {
-    tmem_alloc(tmem_slot, 512);
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   {  // bias table of head h over the block's deltas
@@ -329,9 +373,9 @@ __global__ void __launch_bounds__(384, 1)
   // roles do not keep it in registers.
   const Watchdog &wd = *reinterpret_cast<const Watchdog *>(sm + C::OFF_WD);
 
-  if (warp >= 8) regs_dec<C::REG_OTHER>();
+  if (warp >= C::WARP_PROD) regs_dec<C::REG_OTHER>();
 
-  if (warp == 8) {
+  if (warp == C::WARP_PROD) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int last_k[C::NS], last_v[C::NS];
@@ -368,7 +412,7 @@ __global__ void __launch_bounds__(384, 1)
         if (last_v[s] >= 0) mbar_wait_teardown(v_full + s, last_v[s] & 1, kTeardownNs);
       }
     }
-  } else if (warp == 9 && !C::SEP_P) {
+  } else if (warp == C::WARP_MMA && !C::SEP_P) {
     // ------------------------------------------------------------------ MMA issuer (d = 128)
     // One thread issues for both Q tiles (S_t is overwritten only after P_t V is issued).
     if (lane == 0) {
@@ -440,11 +484,11 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(mma_done);
       mbar_wait_teardown(mma_done, 0, kTeardownNs);
     }
-  } else if (C::SEP_P && (warp == 9 || warp == 10)) {
+  } else if (C::SEP_P && warp >= C::WARP_MMA && warp < C::WARP_MMA + NT) {
     // ------------------------------------------------------------------ MMA issuers (d = 64)
     // One issuing thread per Q tile, so neither tile's hand-offs wait behind the other's.
     // Each K/V stage is released once per active issuer (the barriers count ntile arrivals).
-    const int t = warp - 9;
+    const int t = warp - C::WARP_MMA;
     const int nk = t == 0 ? nkv0 : nkv1;
     if (lane == 0 && t < ntile && nk > 0) {
       const uint32_t dS_t = tmem + C::COL_S0 + 128 * t;
@@ -529,7 +573,7 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(mma_done + t);
       mbar_wait_teardown(mma_done + t, 0, kTeardownNs);
     }
-  } else if (warp < 8) {
+  } else if (warp < 4 * NT) {
     // ------------------------------------------------------------------ softmax warpgroups
     regs_inc<C::REG_SM>();
     const int t = warp >> 2;
@@ -721,9 +765,9 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -786,24 +830,30 @@ __global__ void __launch_bounds__(256) fat_fwd_tail_combine_kernel(const FwdPara
   }
 }
 
-template <int D>
+template <int D, int NT>
 int launch_fwd_t(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                 const CUtensorMap &mv, size_t smem, cudaStream_t stream) {
-  const dim3 grid((p.seq.max_seqlen + 255) / 256, p.seq.num_heads,
-                  p.seq.num_seqs * p.kv_splits);
+                 const CUtensorMap &mv, cudaStream_t stream) {
+  using C = FwdCfg<D, NT>;
+  const size_t smem = fwd_smem_bytes(D, p.bias.lut_len, NT);
+  const dim3 grid = (NT == 1 && p.flat)
+                        ? dim3((unsigned)(p.seq.total_tokens / 128 + p.seq.num_seqs),
+                               p.seq.num_heads, 1)
+                        : dim3((p.seq.max_seqlen + C::ROWS - 1) / C::ROWS, p.seq.num_heads,
+                               p.seq.num_seqs * p.kv_splits);
   // the register re-balancing needs the launch pool the split was designed for
-  cudaError_t e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, false>, smem,
-                                              FwdCfg<D>::NTHREADS, FwdCfg<D>::REGS_NEEDED);
+  cudaError_t e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, false, NT>, smem,
+                                              C::NTHREADS, C::REGS_NEEDED);
   if (e != cudaSuccess) return (int)e;  // reason recorded by prepare_kernel
-  fat_fwd_kernel<D, false><<<grid, FwdCfg<D>::NTHREADS, smem, stream>>>(mq, mk, mv, p);
+  fat_fwd_kernel<D, false, NT><<<grid, C::NTHREADS, smem, stream>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   const long long tail_ctas = (long long)p.tail_ntail * p.tail_splits;
+  if constexpr (NT == 2) {
   if (e == cudaSuccess && p.tail_splits > 0 && tail_ctas > 0) {
     // the split last wave, then its merge (ordered by the stream)
-    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, true>, smem,
-                                    FwdCfg<D>::NTHREADS, FwdCfg<D>::REGS_NEEDED);
+    e = (cudaError_t)prepare_kernel((const void *)fat_fwd_kernel<D, true, NT>, smem,
+                                    C::NTHREADS, C::REGS_NEEDED);
     if (e != cudaSuccess) return (int)e;
-    fat_fwd_kernel<D, true><<<(unsigned)tail_ctas, FwdCfg<D>::NTHREADS, smem, stream>>>(
+    fat_fwd_kernel<D, true, NT><<<(unsigned)tail_ctas, C::NTHREADS, smem, stream>>>(
         mq, mk, mv, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) {
@@ -813,9 +863,10 @@ int launch_fwd_t(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &m
       e = cudaGetLastError();
     }
   }
+  }
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
-    cudaFuncGetAttributes(&fa, fat_fwd_kernel<D, false>);
+    cudaFuncGetAttributes(&fa, fat_fwd_kernel<D, false, NT>);
     char msg[160];
     snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
              cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
@@ -823,6 +874,10 @@ int launch_fwd_t(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &m
     set_last_error("kernel launch", (int)e, msg);
   }
   return (int)e;
+}
+
+int fwd_tiles_per_cta(int head_dim, int max_seqlen) {
+  return head_dim == 64 && max_seqlen <= kFwdOneTileMaxRows ? 1 : 2;
 }
 
 int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, const void *v,
@@ -833,9 +888,17 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
   if (make_tmap_thd(&mq, q, T, H, head_dim, 128) || make_tmap_thd(&mk, k, Tk, Hkv, head_dim, 128) ||
       make_tmap_thd(&mv, v, Tk, Hkv, head_dim, 128))
     return (int)cudaErrorInvalidValue;
-  const size_t smem = fwd_smem_bytes(head_dim, p.bias.lut_len);
-  return head_dim == 64 ? launch_fwd_t<64>(p, mq, mk, mv, smem, stream)
-                        : launch_fwd_t<128>(p, mq, mk, mv, smem, stream);
+  if (head_dim == 128) return launch_fwd_t<128, 2>(p, mq, mk, mv, stream);
+  // a split last wave is planned for two-tile CTAs
+  if (p.tail_splits == 0 && fwd_tiles_per_cta(head_dim, p.seq.max_seqlen) == 1) {
+    FwdParams pf = p;
+    // documents of different lengths: the flat grid, when it has fewer blocks
+    const long long blocks_3d = (long long)((p.seq.max_seqlen + 127) / 128) * p.seq.num_seqs;
+    const long long blocks_flat = (long long)p.seq.total_tokens / 128 + p.seq.num_seqs;
+    pf.flat = p.kv_splits == 1 && p.seq.num_seqs > 1 && blocks_flat < blocks_3d;
+    return launch_fwd_t<64, 1>(pf, mq, mk, mv, stream);
+  }
+  return launch_fwd_t<64, 2>(p, mq, mk, mv, stream);
 }
 
 // Merge of a split forward's partial results, one warp per (query row, head): with partial lse

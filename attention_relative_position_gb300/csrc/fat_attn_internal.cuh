@@ -205,6 +205,11 @@ struct FwdParams {
   long long tail_first;
   int tail_splits, tail_gx, tail_ntail;
   float *tail_o, *tail_lse;
+  // One-tile CTAs over documents of different lengths (kv_splits = 1): blockIdx.x enumerates the
+  // 128-row blocks of all documents, document i owning ids [cu[i] / 128 + i, cu[i + 1] / 128 +
+  // i + 1) (at least its ceil(L_i / 128) blocks; an extra id exits at once), so no CTA is spent
+  // on rows a short document does not have. 0: the (block, head, document) grid.
+  int flat;
 };
 
 struct BwdParams {
@@ -239,7 +244,12 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
                cudaStream_t stream);
 // merge the kv_splits partial results of a split forward into out (bf16) and lse
 int launch_fwd_combine(const FwdParams &p, int head_dim, cudaStream_t stream);
-size_t fwd_smem_bytes(int head_dim, int lut_len);
+// Forward CTAs take two 128-row Q tiles (one CTA per SM), or, at d = 64 when no document is
+// longer than kFwdOneTileMaxRows, one tile (two CTAs per SM: short documents are bound by each
+// CTA's fixed costs, which a second resident CTA overlaps).
+constexpr int kFwdOneTileMaxRows = 2048;
+int fwd_tiles_per_cta(int head_dim, int max_seqlen);
+size_t fwd_smem_bytes(int head_dim, int lut_len, int nt);
 // Few-row forward (decode steps, short query chunks): taken when max_seqlen * group rows fit
 // the kernel's row tile and its bias lookup table fits shared memory. Same FwdParams contract
 // as launch_fwd (kv_splits = 1: out and lse; more: the partials launch_fwd_combine merges).
