@@ -59,8 +59,10 @@ struct BwdCfg {
   static constexpr bool DQ_TMA = (D == 64);
   static constexpr int DQS_SLICE = 32 * 16 * 4;  // one warp: 32 rows x 16 channels fp32
   static constexpr int OFF_DQS = OFF_DS + 2 * DSTILE;
-  static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 16 * DQS_SLICE : 0);  // lse2, dvec
-  static constexpr int OFF_BAR = OFF_STAT + NS * 2 * BQ * 4;
+  // per Q/dO stage: lse2, dvec, and (one-CTA-per-key-tile kernel) the column terms of linear
+  // far-side tiles, -k * j - lse2 for each side's slope term
+  static constexpr int OFF_STAT = OFF_DQS + (DQ_TMA ? 16 * DQS_SLICE : 0);
+  static constexpr int OFF_BAR = OFF_STAT + NS * 4 * BQ * 4;
   // lut[lut_len] (bias, log2 units), diag[lut_len] (bias-gradient sums per delta), then the
   // bucket of each delta as bytes
   static constexpr int OFF_LUT = OFF_BAR + 256;
@@ -193,7 +195,9 @@ __device__ __forceinline__ void add_dkdv_tail(const BwdParams &p, long long tail
 // P^T of one W-column chunk: x = S^T * scale_log2 + bias (log2 units), masked, P = 2^(x - lse2).
 // Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Works on column pairs with
 // packed fp32x2 arithmetic. Bias forms are compile-time so the unrolled loop carries no
-// branches: BIAS 0 = lookup table (lut_row[-j]), 1 = constant rowc, 2 = rowc + kq * j.
+// branches: BIAS 0 = lookup table (lut_row[-j]), 1 = constant rowc, 2 = rowc + kq * j, 3 = the
+// same linear form with kq * j - lse2 staged per column (lse4 then points at those terms, and
+// x = S^T * scale_log2 + (rowc + term) needs no separate subtraction).
 template <int W, int BIAS, bool MASK>
 __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W / 2],
                                             const float4 *lse4, const float *lut_row, int jc,
@@ -216,12 +220,17 @@ __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W
         b2 = f2_pack(lut_row[-j], lut_row[-j - 1]);
       else if (BIAS == 1)
         b2 = rc2;
-      else
+      else if (BIAS == 2)
         b2 = f2_fma(kq2, f2_pack(jcf + (float)t, jcf + (float)(t + 1)), rc2);
+      else
+        b2 = f2_add(rc2, lv2[h]);
       const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(raw[t]), __uint_as_float(raw[t + 1])),
                                  sl2, b2);
       float x0, x1;
-      f2_unpack(f2_sub(x2, lv2[h]), x0, x1);
+      if (BIAS == 3)
+        f2_unpack(x2, x0, x1);
+      else
+        f2_unpack(f2_sub(x2, lv2[h]), x0, x1);
       if (MASK) {
         x0 = (j >= lo_j && j < hi_j) ? x0 : -INFINITY;
         x1 = (j + 1 >= lo_j && j + 1 < hi_j) ? x1 : -INFINITY;
@@ -1101,6 +1110,8 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t *sDQS = sm + C::OFF_DQS;
   float *s_lse2 = reinterpret_cast<float *>(sm + C::OFF_STAT);
   float *s_dvec = s_lse2 + C::NS * C::BQ;
+  float *s_colneg = s_dvec + C::NS * C::BQ;  // -k_neg * j - lse2 (negative far side)
+  float *s_colpos = s_colneg + C::NS * C::BQ;  // -k_pos * j - lse2 (positive far side)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
   uint64_t *kv_full = bars;
   uint64_t *qd_full = kv_full + 1;       // [NS]
@@ -1214,14 +1225,23 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
     for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
     const bool kv_issued = early_q && lane == 0;
+    // the linear far-side terms use the slope in log2 units (as far_bias_staged)
+    const float s2e = p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) * kLog2e : 0.f;
+    auto stage_stats = [&](int st, int k, float lv, float dv) {
+      const int j = lane + 32 * k;
+      s_lse2[st * C::BQ + j] = lv;
+      s_dvec[st * C::BQ + j] = dv;
+      s_colneg[st * C::BQ + j] = fmaf(-s2e, (float)j, -lv);
+      s_colpos[st * C::BQ + j] = fmaf(s2e, (float)j, -lv);
+    };
     if (early_q) {
       // step 0: copies started with the block set-up; store its statistics and arrive
       const int qs0 = qtile_start(0);
 #pragma unroll
       for (int k = 0; k < C::BQ / 32; ++k) {
         const int q = qs0 + lane + 32 * k;
-        s_lse2[lane + 32 * k] = lse_to_log2_stat(lv0[k]);
-        s_dvec[lane + 32 * k] = q < L ? __ldg(p.dvec + (size_t)h * T + seq_start + q) : 0.f;
+        stage_stats(0, k, lse_to_log2_stat(lv0[k]),
+                    q < L ? __ldg(p.dvec + (size_t)h * T + seq_start + q) : 0.f);
       }
       mbar_arrive(qd_full);
       if (lane == 0) last_q[0] = 0;
@@ -1239,10 +1259,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(qd_empty + st, (u - 1) & 1, wd))) break;
 #pragma unroll
-        for (int k = 0; k < C::BQ / 32; ++k) {
-          s_lse2[st * C::BQ + lane + 32 * k] = lv[k];
-          s_dvec[st * C::BQ + lane + 32 * k] = dv[k];
-        }
+        for (int k = 0; k < C::BQ / 32; ++k) stage_stats(st, k, lv[k], dv[k]);
         if (lane == 0) {
           mbar_arrive_expect_tx(qd_full + st, 2 * C::QTILE);
           for (int b = 0; b < C::DB; ++b) {
@@ -1475,6 +1492,9 @@ __global__ void __launch_bounds__(640, 1)
       const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
       const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
       const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
+      // linear far sides: -k * j - lse2 per column, staged by the producer
+      const float4 *col4 = reinterpret_cast<const float4 *>(
+          (side == 1 ? s_colpos : s_colneg) + st * C::BQ + c0);
       // ---- one pass per 16 query columns: P^T = 2^(x - lse2) (bf16 to TMEM for the dV
       // product), dS^T = P^T (dP^T - D) in fp32 from the same registers (bf16, swizzled, to
       // shared memory for the dK / dQ products). Table gradient: far tiles add into one register
@@ -1504,8 +1524,8 @@ __global__ void __launch_bounds__(640, 1)
               tc_fence_before();
               mbar_arrive(s_consumed);
             }
-            bwd_p_chunk<16, BIAS, MASK>(raw, pk, lse4 + 4 * sub, lut_row, c0 + 16 * sub, rowc, kq,
-                                        sl, lo_j, hi_j);
+            bwd_p_chunk<16, BIAS, MASK>(raw, pk, (BIAS == 3 ? col4 : lse4) + 4 * sub, lut_row,
+                                        c0 + 16 * sub, rowc, kq, sl, lo_j, hi_j);
             if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
               if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
               tc_fence_after();
@@ -1525,7 +1545,7 @@ __global__ void __launch_bounds__(640, 1)
         };
         using B0 = std::integral_constant<int, 0>;
         using B1 = std::integral_constant<int, 1>;
-        using B2 = std::integral_constant<int, 2>;
+        using B3 = std::integral_constant<int, 3>;
         using Y = std::true_type;
         using N = std::false_type;
         if (side == 0) {  // lookup table
@@ -1535,8 +1555,8 @@ __global__ void __launch_bounds__(640, 1)
             ok = need_mask ? pass(B0{}, Y{}, N{}) : pass(B0{}, N{}, N{});
         } else if (!linear) {  // constant over the tile
           ok = need_mask ? pass(B1{}, Y{}, N{}) : pass(B1{}, N{}, N{});
-        } else {  // linear in the query index
-          ok = need_mask ? pass(B2{}, Y{}, N{}) : pass(B2{}, N{}, N{});
+        } else {  // linear in the query index (column terms staged with the statistics)
+          ok = need_mask ? pass(B3{}, Y{}, N{}) : pass(B3{}, N{}, N{});
         }
         if (!ok) break;
         tmem_st_wait();
