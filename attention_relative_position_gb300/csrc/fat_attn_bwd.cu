@@ -247,7 +247,8 @@ __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W
 // packed to bf16 pairs; returns the chunk's sum. NEAR also reduces the 32-row block along its
 // diagonals: lane m accumulates the sum over delta = base + m in acc_a and over
 // delta = base + m - 32 in acc_b (base = delta of lane 0, column 0 of the group).
-template <int W, bool NEAR, int T0>
+// SUM = false: the chunk's sum is not wanted (no far-side table gradient), so not formed.
+template <int W, bool NEAR, int T0, bool SUM = true>
 __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uint32_t (&dp)[W],
                                               const float4 *dvs4, uint32_t (&pk)[W / 2],
                                               int lane, float &acc_a, float &acc_b) {
@@ -263,7 +264,7 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
       const uint64_t p2 = f2_pack(__uint_as_float(pf[t]), __uint_as_float(pf[t + 1]));
       const uint64_t dp2 = f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1]));
       const uint64_t ds2 = f2_mul(p2, f2_sub(dp2, dv2[h]));
-      part2[h] = f2_add(part2[h], ds2);
+      if (SUM) part2[h] = f2_add(part2[h], ds2);
       float ds[2];
       f2_unpack(ds2, ds[0], ds[1]);
       pk[t / 2] = pack_bf16x2(ds[0], ds[1]);
@@ -284,6 +285,7 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
     acc_a += a[0] + a[1];
     acc_b += b[0] + b[1];
   }
+  if (!SUM) return 0.f;
   float p0, p1;
   f2_unpack(f2_add(part2[0], part2[1]), p0, p1);
   return p0 + p1;
@@ -1509,10 +1511,11 @@ __global__ void __launch_bounds__(640, 1)
         float acc_a = 0.f, acc_b = 0.f, part = 0.f;
         // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
         // once per tile, so no chunk carries the other forms' instructions.
-        auto pass = [&](auto bias_c, auto mask_c, auto near_c) -> bool {
+        auto pass = [&](auto bias_c, auto mask_c, auto near_c, auto sum_c) -> bool {
           constexpr int BIAS = decltype(bias_c)::value;
           constexpr bool MASK = decltype(mask_c)::value;
           constexpr bool NEAR = decltype(near_c)::value;
+          constexpr bool SUM = decltype(sum_c)::value;  // far-side table-gradient sum wanted
 #pragma unroll
           for (int sub = 0; sub < QW / 16; ++sub) {
             uint32_t raw[16], dp[16], pk[8];
@@ -1533,9 +1536,9 @@ __global__ void __launch_bounds__(640, 1)
             tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
             const float4 *d4 = dvs4 + 4 * sub;
             if (sub == 0)
-              part += bwd_ds_chunk<16, NEAR, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
+              part += bwd_ds_chunk<16, NEAR, 0, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
             else
-              part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
+              part += bwd_ds_chunk<16, NEAR, 16, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
 #pragma unroll
             for (int gg = 0; gg < 2; ++gg)  // groups of 8 queries = 16 bytes each
               st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), pk[4 * gg], pk[4 * gg + 1],
@@ -1548,15 +1551,22 @@ __global__ void __launch_bounds__(640, 1)
         using B3 = std::integral_constant<int, 3>;
         using Y = std::true_type;
         using N = std::false_type;
+        // the far sides' sums feed only the table gradient
         if (side == 0) {  // lookup table
           if (near_db)
-            ok = need_mask ? pass(B0{}, Y{}, Y{}) : pass(B0{}, N{}, Y{});
+            ok = need_mask ? pass(B0{}, Y{}, Y{}, N{}) : pass(B0{}, N{}, Y{}, N{});
           else
-            ok = need_mask ? pass(B0{}, Y{}, N{}) : pass(B0{}, N{}, N{});
+            ok = need_mask ? pass(B0{}, Y{}, N{}, N{}) : pass(B0{}, N{}, N{}, N{});
         } else if (!linear) {  // constant over the tile
-          ok = need_mask ? pass(B1{}, Y{}, N{}) : pass(B1{}, N{}, N{});
+          if (do_dbias)
+            ok = need_mask ? pass(B1{}, Y{}, N{}, Y{}) : pass(B1{}, N{}, N{}, Y{});
+          else
+            ok = need_mask ? pass(B1{}, Y{}, N{}, N{}) : pass(B1{}, N{}, N{}, N{});
         } else {  // linear in the query index (column terms staged with the statistics)
-          ok = need_mask ? pass(B3{}, Y{}, N{}) : pass(B3{}, N{}, N{});
+          if (do_dbias)
+            ok = need_mask ? pass(B3{}, Y{}, N{}, Y{}) : pass(B3{}, N{}, N{}, Y{});
+          else
+            ok = need_mask ? pass(B3{}, Y{}, N{}, N{}) : pass(B3{}, N{}, N{}, N{});
         }
         if (!ok) break;
         tmem_st_wait();
