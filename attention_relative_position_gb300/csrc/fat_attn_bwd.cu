@@ -872,10 +872,11 @@ __global__ void __launch_bounds__(640, 1)
           float acc_a = 0.f, acc_b = 0.f, part = 0.f;
           // The whole pass is instantiated per (bias form, mask, diagonal reduction) and chosen
           // once per tile, so no chunk carries the other forms' instructions.
-          auto pass = [&](auto bias_c, auto mask_c, auto near_c) -> bool {
+          auto pass = [&](auto bias_c, auto mask_c, auto near_c, auto sum_c) -> bool {
             constexpr int BIAS = decltype(bias_c)::value;
             constexpr bool MASK = decltype(mask_c)::value;
             constexpr bool NEAR = decltype(near_c)::value;
+            constexpr bool SUM = decltype(sum_c)::value;  // far-side table-gradient sum wanted
 #pragma unroll
             for (int sub = 0; sub < QW / 16; ++sub) {
               uint32_t raw[16], dp[16], pk[8];
@@ -896,9 +897,9 @@ __global__ void __launch_bounds__(640, 1)
               tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
               const float4 *d4 = dvs4 + 4 * sub;
               if (sub == 0)
-                part += bwd_ds_chunk<16, NEAR, 0>(raw, dp, d4, pk, lane, acc_a, acc_b);
+                part += bwd_ds_chunk<16, NEAR, 0, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
               else
-                part += bwd_ds_chunk<16, NEAR, 16>(raw, dp, d4, pk, lane, acc_a, acc_b);
+                part += bwd_ds_chunk<16, NEAR, 16, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
 #pragma unroll
               for (int gg = 0; gg < 2; ++gg)  // groups of 8 queries = 16 bytes each
                 st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), pk[4 * gg], pk[4 * gg + 1],
@@ -911,15 +912,22 @@ __global__ void __launch_bounds__(640, 1)
           using B2 = std::integral_constant<int, 2>;
           using Y = std::true_type;
           using N = std::false_type;
+          // the far sides' sums feed only the table gradient
           if (side == 0) {  // lookup table
             if (near_db)
-              ok = need_mask ? pass(B0{}, Y{}, Y{}) : pass(B0{}, N{}, Y{});
+              ok = need_mask ? pass(B0{}, Y{}, Y{}, N{}) : pass(B0{}, N{}, Y{}, N{});
             else
-              ok = need_mask ? pass(B0{}, Y{}, N{}) : pass(B0{}, N{}, N{});
+              ok = need_mask ? pass(B0{}, Y{}, N{}, N{}) : pass(B0{}, N{}, N{}, N{});
           } else if (!linear) {  // constant over the tile
-            ok = need_mask ? pass(B1{}, Y{}, N{}) : pass(B1{}, N{}, N{});
+            if (do_dbias)
+              ok = need_mask ? pass(B1{}, Y{}, N{}, Y{}) : pass(B1{}, N{}, N{}, Y{});
+            else
+              ok = need_mask ? pass(B1{}, Y{}, N{}, N{}) : pass(B1{}, N{}, N{}, N{});
           } else {  // linear in the query index
-            ok = need_mask ? pass(B2{}, Y{}, N{}) : pass(B2{}, N{}, N{});
+            if (do_dbias)
+              ok = need_mask ? pass(B2{}, Y{}, N{}, Y{}) : pass(B2{}, N{}, N{}, Y{});
+            else
+              ok = need_mask ? pass(B2{}, Y{}, N{}, N{}) : pass(B2{}, N{}, N{}, N{});
           }
           if (!ok) break;
           tmem_st_wait();
