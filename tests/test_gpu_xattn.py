@@ -184,6 +184,10 @@ DECODE = [
        64, 0.5, (32, 64, False), True, True, 0.125, seed=69),
     XW("decode_mqa_causal_d128", (1, 1, 1), (5000, 2500, 640), 4, 1, 128, 1.0, None, False,
        True, 128 ** -0.5, seed=70),
+    # query chunks of up to 64 rows with grouped heads at d 64: too many rows for the few-row
+    # kernel, so the tiled forward with one Q tile per CTA takes the key splits
+    XW("chunk64_gqa2_t5_causal_splitkv_d64", (20, 3, 64), (900, 2000, 700), 4, 2, 64, 0.5,
+       (32, 128, False), causal=True, seed=72),
 ]
 
 
