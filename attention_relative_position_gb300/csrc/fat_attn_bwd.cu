@@ -196,8 +196,10 @@ __device__ __forceinline__ void add_dkdv_tail(const BwdParams &p, long long tail
 // Writes fp32 P into raw (in place of S) and bf16 pairs into pk. Works on column pairs with
 // packed fp32x2 arithmetic. Bias forms are compile-time so the unrolled loop carries no
 // branches: BIAS 0 = lookup table (lut_row[-j]), 1 = constant rowc, 2 = rowc + kq * j, 3 = the
-// same linear form with kq * j - lse2 staged per column (lse4 then points at those terms, and
-// x = S^T * scale_log2 + (rowc + term) needs no separate subtraction).
+// same linear form with c + kq * j - lse2 staged per column (lse4 then points at those terms,
+// rowc holds the row's part, and x = S^T * scale_log2 + (rowc + term) needs no separate
+// subtraction), 4 = a constant bias with c - lse2 staged per column (x = S^T * scale_log2 +
+// term).
 template <int W, int BIAS, bool MASK>
 __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W / 2],
                                             const float4 *lse4, const float *lut_row, int jc,
@@ -222,12 +224,14 @@ __device__ __forceinline__ void bwd_p_chunk(uint32_t (&raw)[W], uint32_t (&pk)[W
         b2 = rc2;
       else if (BIAS == 2)
         b2 = f2_fma(kq2, f2_pack(jcf + (float)t, jcf + (float)(t + 1)), rc2);
-      else
+      else if (BIAS == 3)
         b2 = f2_add(rc2, lv2[h]);
+      else
+        b2 = lv2[h];
       const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(raw[t]), __uint_as_float(raw[t + 1])),
                                  sl2, b2);
       float x0, x1;
-      if (BIAS == 3)
+      if (BIAS >= 3)
         f2_unpack(x2, x0, x1);
       else
         f2_unpack(f2_sub(x2, lv2[h]), x0, x1);
@@ -1120,8 +1124,9 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t *sDQS = sm + C::OFF_DQS;
   float *s_lse2 = reinterpret_cast<float *>(sm + C::OFF_STAT);
   float *s_dvec = s_lse2 + C::NS * C::BQ;
-  float *s_colneg = s_dvec + C::NS * C::BQ;  // -k_neg * j - lse2 (negative far side)
-  float *s_colpos = s_colneg + C::NS * C::BQ;  // -k_pos * j - lse2 (positive far side)
+  // far sides: the bias c + kq * j of column j (kq = -k of the side) minus lse2, per column
+  float *s_colneg = s_dvec + C::NS * C::BQ;
+  float *s_colpos = s_colneg + C::NS * C::BQ;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
   uint64_t *kv_full = bars;
   uint64_t *qd_full = kv_full + 1;       // [NS]
@@ -1235,14 +1240,17 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
     for (int x = 0; x < C::NS; ++x) last_q[x] = -1;
     const bool kv_issued = early_q && lane == 0;
-    // the linear far-side terms use the slope in log2 units (as far_bias_staged)
-    const float s2e = p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) * kLog2e : 0.f;
+    // the far-side constants and slope in log2 units (as the P/dS warpgroups' FarBias)
+    const FarBias pfb = far_bias_staged(
+        p.bias, reinterpret_cast<const int *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15) + 1024),
+        reinterpret_cast<const float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15)),
+        p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) : 0.f);
     auto stage_stats = [&](int st, int k, float lv, float dv) {
       const int j = lane + 32 * k;
       s_lse2[st * C::BQ + j] = lv;
       s_dvec[st * C::BQ + j] = dv;
-      s_colneg[st * C::BQ + j] = fmaf(-s2e, (float)j, -lv);
-      s_colpos[st * C::BQ + j] = fmaf(s2e, (float)j, -lv);
+      s_colneg[st * C::BQ + j] = fmaf(-pfb.k_neg, (float)j, pfb.c_neg - lv);
+      s_colpos[st * C::BQ + j] = fmaf(-pfb.k_pos, (float)j, pfb.c_pos - lv);
     };
     if (early_q) {
       // step 0: copies started with the block set-up; store its statistics and arrive
@@ -1489,11 +1497,11 @@ __global__ void __launch_bounds__(640, 1)
         side = 3;
       } else if (d0 - (C::BQ - 1) >= p.bias.sat_pos) {
         side = 1;
-        rowc = fmaf(fb.k_pos, (float)(d0 + r), fb.c_pos);
+        rowc = fb.k_pos * (float)(d0 + r);  // the row's part; c is in the column terms
         kq = -fb.k_pos;
       } else if (d0 + 127 <= -p.bias.sat_neg) {
         side = 2;
-        rowc = fmaf(fb.k_neg, (float)(d0 + r), fb.c_neg);
+        rowc = fb.k_neg * (float)(d0 + r);
         kq = -fb.k_neg;
       } else {
         side = 0;
@@ -1502,7 +1510,7 @@ __global__ void __launch_bounds__(640, 1)
       const int lut_base = d0 + r - p.bias.lut_lo;  // index of (r, j) is lut_base - j
       const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse2 + st * C::BQ + c0);
       const float4 *dvs4 = reinterpret_cast<const float4 *>(s_dvec + st * C::BQ + c0);
-      // linear far sides: -k * j - lse2 per column, staged by the producer
+      // far sides (and no bias at all): c + kq * j - lse2 per column, staged by the producer
       const float4 *col4 = reinterpret_cast<const float4 *>(
           (side == 1 ? s_colpos : s_colneg) + st * C::BQ + c0);
       // ---- one pass per 16 query columns: P^T = 2^(x - lse2) (bf16 to TMEM for the dV
@@ -1535,7 +1543,7 @@ __global__ void __launch_bounds__(640, 1)
               tc_fence_before();
               mbar_arrive(s_consumed);
             }
-            bwd_p_chunk<16, BIAS, MASK>(raw, pk, (BIAS == 3 ? col4 : lse4) + 4 * sub, lut_row,
+            bwd_p_chunk<16, BIAS, MASK>(raw, pk, (BIAS >= 3 ? col4 : lse4) + 4 * sub, lut_row,
                                         c0 + 16 * sub, rowc, kq, sl, lo_j, hi_j);
             if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
               if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
@@ -1555,8 +1563,8 @@ __global__ void __launch_bounds__(640, 1)
           return true;
         };
         using B0 = std::integral_constant<int, 0>;
-        using B1 = std::integral_constant<int, 1>;
         using B3 = std::integral_constant<int, 3>;
+        using B4 = std::integral_constant<int, 4>;
         using Y = std::true_type;
         using N = std::false_type;
         // the far sides' sums feed only the table gradient
@@ -1565,11 +1573,11 @@ __global__ void __launch_bounds__(640, 1)
             ok = need_mask ? pass(B0{}, Y{}, Y{}, N{}) : pass(B0{}, N{}, Y{}, N{});
           else
             ok = need_mask ? pass(B0{}, Y{}, N{}, N{}) : pass(B0{}, N{}, N{}, N{});
-        } else if (!linear) {  // constant over the tile
+        } else if (!linear) {  // constant over the tile (or no bias): the column terms alone
           if (do_dbias)
-            ok = need_mask ? pass(B1{}, Y{}, N{}, Y{}) : pass(B1{}, N{}, N{}, Y{});
+            ok = need_mask ? pass(B4{}, Y{}, N{}, Y{}) : pass(B4{}, N{}, N{}, Y{});
           else
-            ok = need_mask ? pass(B1{}, Y{}, N{}, N{}) : pass(B1{}, N{}, N{}, N{});
+            ok = need_mask ? pass(B4{}, Y{}, N{}, N{}) : pass(B4{}, N{}, N{}, N{});
         } else {  // linear in the query index (column terms staged with the statistics)
           if (do_dbias)
             ok = need_mask ? pass(B3{}, Y{}, N{}, Y{}) : pass(B3{}, N{}, N{}, Y{});
