@@ -694,7 +694,8 @@ FwdTail fwd_tail_plan(const XShape &x) {
   const long long whole = items / sms * sms, ntail = items - whole;
   const int nkv = (x.maxk + 127) / 128;
   if (ntail == 0 || ntail > sms / 2) return t;
-  const int splits = (int)std::min<long long>(sms / ntail, nkv / 2);
+  // at most 64 parts per CTA (the merge takes one or two per lane)
+  const int splits = (int)std::min<long long>(std::min<long long>(sms / ntail, nkv / 2), 64);
   if (splits < 2) return t;
   t.first = whole;
   t.splits = splits;

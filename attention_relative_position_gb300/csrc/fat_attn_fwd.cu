@@ -771,13 +771,67 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::NTHREADS, FwdCfg<D, NT>::MIN_BL
   }
 }
 
+// One output row merged from S <= 64 normalised partial rows o_s with their (natural) lse l_s
+// by one warp: lse = log sum_s exp(l_s), out = sum_s exp(l_s - lse) o_s; a row with no key in
+// any range gets out 0, lse -inf. Lane s loads l_s and l_{s+32} (all S loads in flight at once),
+// the maximum and the weights' sum are warp reductions, and the partial rows are read four
+// splits at a time with each weight broadcast from its lane. Writes out (bf16, this lane's
+// D / 32 channels) and, from lane 0, lse when lse_out is not null.
+template <int D>
+__device__ __forceinline__ void merge_partial_rows(const float *lse_p, size_t lse_stride,
+                                                   const float *o_p, size_t o_stride, int S,
+                                                   int lane, __nv_bfloat16 *orow, float *lse_out) {
+  constexpr int CPL = D / 32;
+  const float l0 = lane < S ? lse_p[(size_t)lane * lse_stride] : -INFINITY;
+  const float l1 = lane + 32 < S ? lse_p[(size_t)(lane + 32) * lse_stride] : -INFINITY;
+  float m = fmaxf(l0, l1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float w0 = (m == -INFINITY || l0 == -INFINITY) ? 0.f : __expf(l0 - m);
+  const float w1 = (m == -INFINITY || l1 == -INFINITY) ? 0.f : __expf(l1 - m);
+  float wsum = w0 + w1;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+  float acc[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+  const float *o = o_p + lane * CPL;
+#pragma unroll 4
+  for (int sp = 0; sp < S; ++sp) {
+    const float wgt = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+    if (wgt == 0.f) continue;  // the same for every lane
+    const float *os = o + (size_t)sp * o_stride;
+    if constexpr (CPL == 2) {
+      const float2 v = *reinterpret_cast<const float2 *>(os);
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+    } else {
+      const float4 v = *reinterpret_cast<const float4 *>(os);
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+      acc[2] += wgt * v.z;
+      acc[3] += wgt * v.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+  __nv_bfloat16 *dst = orow + lane * CPL;
+  if constexpr (CPL == 2) {
+    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+    uint2 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2 *>(dst) = v;
+  }
+  if (lane == 0 && lse_out != nullptr) *lse_out = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+}
+
 // Merge of a split last wave: one warp per (split CTA row), the tail_splits partial rows (each
 // normalised, with its lse) combined as in the split-key merge below, written to out and lse.
 // Documents have equal length (the condition of the split), so row q of document doc is token
 // doc * max_seqlen + q.
 template <int D>
 __global__ void __launch_bounds__(256) fat_fwd_tail_combine_kernel(const FwdParams p) {
-  constexpr int CPL = D / 32;
   const int T = p.seq.total_tokens, H = p.seq.num_heads, S = p.tail_splits;
   const int L = p.seq.max_seqlen;
   const int lane = threadIdx.x & 31;
@@ -793,40 +847,10 @@ __global__ void __launch_bounds__(256) fat_fwd_tail_combine_kernel(const FwdPara
     const int q = (p.tail_gx - 1 - (int)(cta % p.tail_gx)) * 256 + row;
     if (q >= L) continue;
     const long long tok = doc * L + q;
-    float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, p.tail_lse[(c * S + s) * 256 + row]);
-    float acc[CPL];
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    if (m != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const size_t t = (size_t)(c * S + s) * 256 + row;
-        const float ls = p.tail_lse[t];
-        if (ls == -INFINITY) continue;
-        const float wgt = __expf(ls - m);
-        wsum += wgt;
-        const float *o = p.tail_o + t * D + lane * CPL;
-#pragma unroll
-        for (int i = 0; i < CPL; i += 2) {
-          const float2 v = *reinterpret_cast<const float2 *>(o + i);
-          acc[i] += wgt * v.x;
-          acc[i + 1] += wgt * v.y;
-        }
-      }
-    }
-    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-    __nv_bfloat16 *orow = p.out + ((size_t)tok * H + h) * D + lane * CPL;
-    if constexpr (CPL == 2) {
-      *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    } else {
-      uint2 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2 *>(orow) = v;
-    }
-    if (lane == 0 && p.lse != nullptr)
-      p.lse[(size_t)h * T + tok] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+    merge_partial_rows<D>(p.tail_lse + (size_t)c * S * 256 + row, 256,
+                          p.tail_o + ((size_t)c * S * 256 + row) * D, (size_t)256 * D, S, lane,
+                          p.out + ((size_t)tok * H + h) * D,
+                          p.lse != nullptr ? p.lse + (size_t)h * T + tok : nullptr);
   }
 }
 
@@ -907,7 +931,6 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
 // Memory bound: each lane reads D/32 channels of every split's row.
 template <int D>
 __global__ void __launch_bounds__(256) fat_fwd_combine_kernel(const FwdParams p) {
-  constexpr int CPL = D / 32;  // channels per lane
   const int T = p.seq.total_tokens, H = p.seq.num_heads, S = p.kv_splits;
   const int lane = threadIdx.x & 31;
   const long long nrows = (long long)T * H;
@@ -915,44 +938,10 @@ __global__ void __launch_bounds__(256) fat_fwd_combine_kernel(const FwdParams p)
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long rh = w0; rh < nrows; rh += nw) {
     const int t = (int)(rh / H), h = (int)(rh % H);
-    float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, p.lse_part[((size_t)s * H + h) * T + t]);
-    float acc[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    float wsum = 0.f;
-    if (m != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float ls = p.lse_part[((size_t)s * H + h) * T + t];
-        if (ls == -INFINITY) continue;
-        const float wgt = __expf(ls - m);
-        wsum += wgt;
-        const float *o = p.o_part + (((size_t)s * T + t) * H + h) * D + lane * CPL;
-        if constexpr (CPL == 2) {
-          const float2 v = *reinterpret_cast<const float2 *>(o);
-          acc[0] += wgt * v.x;
-          acc[1] += wgt * v.y;
-        } else {
-          const float4 v = *reinterpret_cast<const float4 *>(o);
-          acc[0] += wgt * v.x;
-          acc[1] += wgt * v.y;
-          acc[2] += wgt * v.z;
-          acc[3] += wgt * v.w;
-        }
-      }
-    }
-    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-    __nv_bfloat16 *orow = p.out + ((size_t)t * H + h) * D + lane * CPL;
-    if constexpr (CPL == 2) {
-      *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    } else {
-      uint2 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2 *>(orow) = v;
-    }
-    if (lane == 0 && p.lse != nullptr)
-      p.lse[(size_t)h * T + t] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+    merge_partial_rows<D>(p.lse_part + (size_t)h * T + t, (size_t)H * T,
+                          p.o_part + ((size_t)t * H + h) * D, (size_t)T * H * D, S, lane,
+                          p.out + ((size_t)t * H + h) * D,
+                          p.lse != nullptr ? p.lse + (size_t)h * T + t : nullptr);
   }
 }
 
