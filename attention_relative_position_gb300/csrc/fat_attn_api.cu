@@ -244,6 +244,42 @@ int sm_count() {
   return cached[dev];
 }
 
+int max_pair_ctas(const void *fn, size_t smem, int nthreads) {
+  struct Entry {
+    const void *fn;
+    int dev;
+    size_t smem;
+    int ctas;
+  };
+  static std::mutex mu;
+  static Entry tab[32];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i)
+    if (tab[i].fn == fn && tab[i].dev == dev && tab[i].smem == smem) return tab[i].ctas;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(nthreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // this query's own error: the caller launches without clusters
+    n = 0;
+  }
+  if (used == 32) used = 0;
+  tab[used++] = Entry{fn, dev, smem, 2 * n};
+  return 2 * n;
+}
+
 void set_last_error(const char *what, int code, const char *text) {
   snprintf(g_last_error, sizeof g_last_error, "%s: error %d (%s)", what, code, text ? text : "");
 }

@@ -105,7 +105,7 @@ size_t bwd_smem_bytes_t(int lut_len) {
   // lut, diag (fp32), bucket ids (bytes), one table column (256 fp32), the staged thresholds
   // (64 int), the item ring
   return 1024 + (size_t)BwdCfg<D, NS>::OFF_LUT + (size_t)lut_len * 9 + 16 + 1024 +
-         kMaxThresholds * 4 + kItemSlots * sizeof(ItemSlot);
+         kMaxThresholds * 4 + kItemSlots * sizeof(ItemSlot) + 16 * sizeof(int4);
 }
 // Three Q/dO stages when they fit next to the bias table, else two.
 int bwd_stages(int head_dim, int lut_len) {
@@ -395,6 +395,7 @@ __global__ void __launch_bounds__(640, 1)
   float *tcol_s = reinterpret_cast<float *>(sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15));
   int *thr_s = reinterpret_cast<int *>(tcol_s + 256);
   ItemSlot *slots = reinterpret_cast<ItemSlot *>(thr_s + kMaxThresholds);
+  int4 *last_dq = reinterpret_cast<int4 *>(slots + kItemSlots);  // [16], one per P/dS warp
 
   // The producer warp sets up the barriers and starts the first item's first step (K, V, the
   // first Q/dO tile and the loads of its lse) before the rest of the block builds its tables, so
@@ -762,8 +763,9 @@ __global__ void __launch_bounds__(640, 1)
     const bool has_slopes = p.bias.slopes != nullptr;
     bool dq_staged = false;  // this warp has a bulk reduction in flight from its staging slice
 
-    // dQ of global step g (query tile starting at qs of item w) into the fp32 accumulator
-    auto drain_dq = [&](const WorkItem &w, int g, int qs) -> bool {
+    // dQ of global step g into the fp32 accumulator: the tile's first token row0, its head h and
+    // the rows left in its document from row0
+    auto drain_dq = [&](int g, int row0, int h, int rows) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, wd))) return false;
       tc_fence_after();
       uint32_t vq[16];
@@ -789,16 +791,16 @@ __global__ void __launch_bounds__(640, 1)
         __syncwarp();
         // rows past the document end carry zeros (their dS is masked), rows past T are clipped
         if (lane == 0) {
-          tma_reduce_add_3d(&tm_dq, slice, 16 * wg, w.h, w.seq_start + qs + 32 * (warp & 3));
+          tma_reduce_add_3d(&tm_dq, slice, 16 * wg, h, row0 + 32 * (warp & 3));
           bulk_commit_group();
         }
         dq_staged = true;
       } else {  // lane = channel, columns = query rows 16*wg ..
-        float *dst = p.dq_acc + ((size_t)(w.seq_start + qs + 16 * wg) * H + w.h) * D + r;
+        float *dst = p.dq_acc + ((size_t)(row0 + 16 * wg) * H + h) * D + r;
         const size_t step = (size_t)H * D;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (qs + 16 * wg + j < w.L) red_add(dst + j * step, __uint_as_float(vq[j]));
+          if (16 * wg + j < rows) red_add(dst + j * step, __uint_as_float(vq[j]));
       }
       return true;
     };
@@ -950,13 +952,29 @@ __global__ void __launch_bounds__(640, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(ds_ready);
-        // ---- the previous tile's dQ (its product was issued after this tile's S^T and dP^T)
-        if (it >= 1 && !drain_dq(w, g - 1, qtile_start(w, it - 1))) {
+        // ---- the previous step's dQ (its product was issued after that step's dS); an item's
+        // last one is read after the next item's first dS, so that the wait for it overlaps the
+        // dK/dV epilogue and the switch between items
+        bool drained;
+        if (it >= 1) {
+          const int qp = qtile_start(w, it - 1);
+          drained = drain_dq(g - 1, w.seq_start + qp, w.h, w.L - qp);
+        } else if (g >= 1) {
+          const int4 l = last_dq[warp];
+          drained = drain_dq(g - 1, l.x, l.y, l.z);
+        } else {
+          drained = true;
+        }
+        if (!drained) {
           ok = false;
           break;
         }
       }
-      if (ok && w.nq >= 1) ok = drain_dq(w, gs + w.nq - 1, qtile_start(w, w.nq - 1));
+      if (ok && w.nq >= 1) {  // where the item's last dQ goes, for the step that drains it
+        const int qp = qtile_start(w, w.nq - 1);
+        if (lane == 0) last_dq[warp] = make_int4(w.seq_start + qp, w.h, w.L - qp, 0);
+        __syncwarp();
+      }
       // ---- dK, dV of the item: this warpgroup's quarter of the channels
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, ii & 1, wd));
       if (!ok) break;
@@ -1036,11 +1054,18 @@ __global__ void __launch_bounds__(640, 1)
         mbar_arrive(comp_sync);
         if (!__all_sync(0xffffffffu, mbar_wait(comp_sync, 1, wd))) { ok = false; break; }
       }
-      if (!more) break;
+      if (!more) {
+        gs += w.nq;
+        break;
+      }
       gs += w.nq;
       w = slots[ii % kItemSlots].next;
       ++ii;
     } while (true);
+    if (ok && gs >= 1) {  // the last item's last dQ
+      const int4 l = last_dq[warp];
+      ok = drain_dq(gs - 1, l.x, l.y, l.z);
+    }
     (void)ok;
     grid_dep_launch();  // the finishing grid may be scheduled
     if (C::DQ_TMA && lane == 0) bulk_wait_all();  // reductions complete before smem is released
@@ -1702,27 +1727,54 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
   }
   const long long tail_ctas = (items - pp.tail_first) * pp.tail_splits;
   if (tail_ctas > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
-  const dim3 grid = persistent ? dim3((unsigned)std::min<long long>(items, sms > 0 ? sms : 1))
-                               : dim3((unsigned)pp.nkb, H, p.seq.num_seqs);
+  // The persistent grid runs as clusters of two CTAs, which puts CTAs 2c and 2c + 1 on the two
+  // SMs of one TPC. Neighbouring CTAs walk neighbouring items (the same document and key tile,
+  // adjacent heads), so the two SMs of a pair run the same code path in step. Placed apart (as a
+  // launch that overlaps the preprocessing grid places them, SM by SM as it drains), the pairs
+  // run unrelated paths and stall on instruction fetch: on the causal varlen workload 3.2 warps
+  // per issue instead of 0.9, and 20% longer CTAs. The grid is then an even number of CTAs that
+  // fit at once as pairs.
+  long long pgrid = std::min<long long>(items, sms > 0 ? sms : 1);
+  bool pairs = false;
+  if (persistent && items >= 2) {
+    const void *fn = ns == 3 ? (const void *)fat_bwd_kernel<64, 3>
+                             : (const void *)fat_bwd_kernel<64, 2>;
+    if (prepare_kernel(fn, smem, BwdCfg<64, 2>::NTHREADS, 0) == (int)cudaSuccess) {
+      const int cap = max_pair_ctas(fn, smem, BwdCfg<64, 2>::NTHREADS) & ~1;
+      if (cap >= 2) {
+        pgrid = std::min<long long>((items + 1) & ~1LL, cap);
+        pairs = true;
+      }
+    }
+  }
+  const dim3 grid = persistent ? dim3((unsigned)pgrid) : dim3((unsigned)pp.nkb, H, p.seq.num_seqs);
   cudaError_t e;
   bool attr_failed = false;
-  auto go = [&](auto kernel, dim3 g, bool overlap) {
+  auto go = [&](auto kernel, dim3 g, bool overlap, bool cluster2 = false) {
     e = (cudaError_t)prepare_kernel((const void *)kernel, smem, BwdCfg<64, 2>::NTHREADS, 0);
     if (e != cudaSuccess) {
       attr_failed = true;
       return;
     }
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = g;
     cfg.blockDim = dim3(BwdCfg<64, 2>::NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
     if (overlap) {  // programmatic dependent launch on the preprocessing grid
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+      ++cfg.numAttrs;
+    }
+    if (cluster2) {
+      attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+      attr[cfg.numAttrs].val.clusterDim.x = 2;
+      attr[cfg.numAttrs].val.clusterDim.y = 1;
+      attr[cfg.numAttrs].val.clusterDim.z = 1;
+      ++cfg.numAttrs;
     }
     e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, mdq, pp);
   };
@@ -1730,8 +1782,8 @@ int launch_bwd(const BwdParams &p, int head_dim, const void *q, const void *k, c
   const dim3 tail_grid((unsigned)tail_ctas);
   if (head_dim == 64) {
     if (persistent) {
-      if (ns == 3) go(fat_bwd_kernel<64, 3>, grid, overlap_previous);
-      else go(fat_bwd_kernel<64, 2>, grid, overlap_previous);
+      if (ns == 3) go(fat_bwd_kernel<64, 3>, grid, overlap_previous, pairs);
+      else go(fat_bwd_kernel<64, 2>, grid, overlap_previous, pairs);
     } else if (ns == 3) {
       go(fat_bwd_tiles_kernel<64, 3, false>, grid, overlap_previous);
       if (e == cudaSuccess && tail_ctas) go(fat_bwd_tiles_kernel<64, 3, true>, tail_grid, false);

@@ -290,6 +290,11 @@ int prepare_kernel(const void *fn, size_t smem, int nthreads, int regs_needed);
 // Number of SMs of the current device (cached per device; 0 if the query fails).
 int sm_count();
 
+// How many CTAs of kernel `fn` (nthreads threads, smem bytes of dynamic shared memory, set up by
+// prepare_kernel) can be resident at once when launched as clusters of two: twice the number of
+// co-resident two-CTA clusters, cached per (kernel, device, size); 0 if the query fails.
+int max_pair_ctas(const void *fn, size_t smem, int nthreads);
+
 // Record a description of the last failing CUDA call of this thread (read by the C ABI).
 void set_last_error(const char *what, int code, const char *text);
 
