@@ -227,6 +227,7 @@ struct BwdParams {
   float *dbias;       // [nb, H] or nullptr
   int *err;
   int nkb;            // key tiles of the longest document (filled by the launcher)
+  int lpt;            // persistent kernel: walk the items longest-first (filled by the launcher)
   long long timeout_ns;
   int debug_flags;
   // Balanced last wave of the one-CTA-per-key-tile grid (documents of equal length, no causal
