@@ -99,10 +99,6 @@ struct ItemSlot {
   int pad[7];
 };
 constexpr int kItemSlots = 8;
-// Work order by decreasing length (documents of different lengths): at most kLptGroups
-// (key tile, document) groups are sorted, and each CTA keeps at most kLptRounds item ranks.
-constexpr int kLptGroups = 8192;
-constexpr int kLptRounds = 128;
 
 template <int D, int NS>
 size_t bwd_smem_bytes_t(int lut_len) {
@@ -300,109 +296,28 @@ __device__ __forceinline__ float bwd_ds_chunk(const uint32_t (&pf)[W], const uin
 }
 
 
-// The item ranks this CTA walks when the documents differ in length (all threads of the block
-// call it; it synchronises the block). The rank order (key tile slowest) is longest-first only
-// when every document has the same length; otherwise a CTA's share depends on which documents
-// its rounds happen to hit. Here the (key tile, document) groups are sorted by decreasing
-// query-tile count, the cost of each of their items, with a stable counting sort (so that the H
-// heads of a group stay adjacent: the two CTAs of a pair keep walking neighbouring heads), and
-// the sorted items are dealt in the same alternating rounds (round v of CTA c takes position
-// v G + c, or v G + G - 1 - c when v is odd): the longest-processing-time-first rule. Groups
-// past a document's end, or with no query that sees their keys, are left out; corrupt or
-// out-of-bound cu_seqlens entries are reported as the rank walk reports them. Returns the
-// number of ranks written to list, or -1 when the CTAs would need more than kLptRounds rounds
-// (every CTA reaches the same answer). scratch: shared memory unused until the first pass,
-// room for kLptGroups bytes + (68 + 68 * warps + kLptGroups) ints.
+// Bucket of key-tile group g = kb * nseq + doc for lpt_order: 64 - the query tiles each of its
+// items walks (1..64; longer first), 64 when the group has no item. Corrupt or out-of-bound
+// cu_seqlens entries are reported as the rank walk reports them.
 template <int BQ>
-__device__ int bwd_lpt_order(const BwdParams &p, uint8_t *scratch, int *list) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-  const int nseq = p.seq.num_seqs, H = p.seq.num_heads;
-  const int ng = p.nkb * nseq;  // group g = kb * nseq + doc: the order of the item ranks
-  uint8_t *key = scratch;       // bucket of each group: 64 - query tiles (1..64), 64 = none
-  int *hist = reinterpret_cast<int *>(scratch + ((ng + 15) & ~15));  // [68]
-  int *wcnt = hist + 68;                                              // [warps][68]
-  int *sorted = wcnt + nwarps * 68;                                   // [valid groups]
-  for (int i = tid; i < 68; i += nthreads) hist[i] = 0;
-  __syncthreads();
-  for (int g = tid; g < ng; g += nthreads) {
+struct BwdLptBucket {
+  const BwdParams &p;
+  __device__ int operator()(int g) const {
+    const int nseq = p.seq.num_seqs;
     const int kb = g / nseq, doc = g - kb * nseq;
     const DocSpan sp = doc_span(p.seq, doc);
-    int b = 64;
     if (!sp.ok) {
       if (kb == 0) atomicOr(p.err, FAT_DEVERR_SEQLENS);
-    } else {
-      if (kb == 0 && (sp.lq > p.seq.max_seqlen || sp.lk > p.seq.max_seqlen_k))
-        atomicOr(p.err, FAT_DEVERR_SEQLENS);
-      if (kb * 128 < sp.lk) {
-        const int i0 = p.causal ? max(0, kb * 128 - sp.shift) / BQ : 0;
-        const int nq = (sp.lq + BQ - 1) / BQ - i0;
-        if (nq > 0) b = 64 - min(nq, 64);
-      }
+      return 64;
     }
-    key[g] = static_cast<uint8_t>(b);
-    atomicAdd(hist + b, 1);
+    if (kb == 0 && (sp.lq > p.seq.max_seqlen || sp.lk > p.seq.max_seqlen_k))
+      atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    if (kb * 128 >= sp.lk) return 64;
+    const int i0 = p.causal ? max(0, kb * 128 - sp.shift) / BQ : 0;
+    const int nq = (sp.lq + BQ - 1) / BQ - i0;
+    return nq > 0 ? 64 - min(nq, 64) : 64;
   }
-  __syncthreads();
-  if (warp == 0) {  // bucket starts (exclusive scan of the 65 counts)
-    int run = 0;
-    for (int b0 = 0; b0 < 65; b0 += 32) {
-      const int b = b0 + lane;
-      const int c = b < 65 ? hist[b] : 0;
-      int x = c;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
-      }
-      if (b < 65) hist[b] = run + x - c;
-      run += __shfl_sync(0xffffffffu, x, 31);
-    }
-  }
-  __syncthreads();
-  const int n_valid = hist[64];
-  // stable scatter, one group per thread and chunk: rank within the warp by matching buckets,
-  // warp offsets per bucket from the chunk's counts
-  for (int base = 0; base < ng; base += nthreads) {
-    for (int i = tid; i < nwarps * 68; i += nthreads) wcnt[i] = 0;
-    __syncthreads();
-    const int g = base + tid;
-    const int b = g < ng ? key[g] : 255;
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    const int rank_w = __popc(peers & ((1u << lane) - 1u));
-    if (b < 64 && rank_w == 0) wcnt[warp * 68 + b] = __popc(peers);
-    __syncthreads();
-    if (tid < 64) {
-      int run = hist[tid];
-      for (int w = 0; w < nwarps; ++w) {
-        const int c = wcnt[w * 68 + tid];
-        wcnt[w * 68 + tid] = run;
-        run += c;
-      }
-      hist[tid] = run;
-    }
-    __syncthreads();
-    if (b < 64) sorted[wcnt[warp * 68 + b] + rank_w] = g;
-    __syncthreads();
-  }
-  const long long total = (long long)n_valid * H;
-  const long long G = gridDim.x, c = blockIdx.x;
-  const long long rounds = (total + G - 1) / G;
-  if (rounds > kLptRounds) return -1;
-  // rounds before the last are full; the last holds this CTA's position if it is < total
-  const long long last = (rounds - 1) * G + (((rounds - 1) & 1) ? G - 1 - c : c);
-  const int n = rounds == 0 ? 0 : (int)(rounds - 1) + (last < total ? 1 : 0);
-  const long long n_dh = (long long)H * nseq;
-  for (int v = tid; v < n; v += nthreads) {
-    const long long pos = (long long)v * G + ((v & 1) ? G - 1 - c : c);
-    const int g = sorted[pos / H];
-    const int h = (int)(pos % H);
-    const int kb = g / nseq, doc = g - kb * nseq;
-    list[v] = (int)(kb * n_dh + (long long)doc * H + h);
-  }
-  __syncthreads();
-  return n;
-}
+};
 
 template <int D, int NSTAGES>
 __global__ void __launch_bounds__(640, 1)
@@ -423,16 +338,19 @@ __global__ void __launch_bounds__(640, 1)
   // k G + c on even rounds and k G + G - 1 - c on odd ones (G CTAs), which evens out the work
   // per CTA; every role walks the same sequence. Items past a document's end are skipped; a
   // corrupt cu_seqlens entry is reported and its items skipped. Documents of different lengths
-  // (p.lpt): the ranks come sorted longest-first from bwd_lpt_order instead.
+  // (p.lpt): the ranks come sorted longest-first from lpt_order instead.
   const long long n_virtual = (long long)p.nkb * H * p.seq.num_seqs;
   const long long n_dh = (long long)H * p.seq.num_seqs;
-  // documents of different lengths: this CTA's ranks in longest-first order (bwd_lpt_order)
+  // documents of different lengths: this CTA's ranks in longest-first order (lpt_order)
   int *lpt_list = reinterpret_cast<int *>(
       sm + C::OFF_LUT + ((p.bias.lut_len * 9 + 15) & ~15) + 1024 + kMaxThresholds * 4 +
       kItemSlots * sizeof(ItemSlot) + 16 * sizeof(int4));
-  static_assert(D != 64 || 2 * C::DSTILE >= kLptGroups + 4 * (68 + 68 * 20 + kLptGroups),
+  static_assert(D != 64 || 2 * C::DSTILE >= lpt_scratch_bytes(C::NTHREADS),
                 "the ordering scratch fits the dS tiles");
-  const int lpt_n = (D == 64 && p.lpt) ? bwd_lpt_order<C::BQ>(p, sm + C::OFF_DS, lpt_list) : -1;
+  const int lpt_n = (D == 64 && p.lpt)
+                        ? lpt_order(p.nkb * p.seq.num_seqs, p.seq.num_seqs, H, kLptRounds,
+                                    BwdLptBucket<C::BQ>{p}, sm + C::OFF_DS, lpt_list)
+                        : -1;
   auto next_item = [&](long long &v, WorkItem &w) -> bool {
     for (;; ++v) {
       long long rank;

@@ -24,6 +24,7 @@
 // units to itself, and the other's logits and waits overlap it.
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 
 #include "fat_attn_internal.cuh"
 
@@ -771,6 +772,518 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::NTHREADS, FwdCfg<D, NT>::MIN_BL
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Persistent one-tile forward (d = 64, documents of at most kFwdOneTileMaxRows rows, whole key
+// ranges). Short documents give each CTA of the one-tile grid only a few key-tile steps, so its
+// fixed costs (barriers, TMEM allocation, bias table, the first loads, the epilogue and the
+// block's own launch) weigh as much as its steps. Here two CTAs per SM walk all items (document,
+// head, 128-row block) in turn with the roles of the one-tile CTA: the producer loads the next
+// item's Q and K/V tiles while the softmax warpgroup writes the current item's rows, the MMA
+// issuer computes the next item's first S as soon as the current one's last S has been read,
+// and the bias table is rebuilt only when the head changes. Item ranks r = a (n H) + doc H + h
+// with block qb = blocks(doc) - 1 - a (longest rows first when causal); documents of different
+// lengths walk them longest-first (lpt_order), else in alternating rounds over the ranks.
+
+// One item of the persistent forward.
+struct FwdItem {
+  int h, seq_start, L, seq_start_k, Lk, shift, q0;
+  int nkv;       // key tiles its rows see (0: rows without keys)
+  int kt0, kdir;  // stream position j holds key tile kt0 + kdir j
+};
+
+// Bucket of block group g = a * nseq + doc for lpt_order: 64 - the key tiles its rows see
+// (1..64; more first), 63 for rows without keys, 64 when the document has no block a.
+struct FwdLptBucket {
+  const FwdParams &p;
+  __device__ int operator()(int g) const {
+    const int nseq = p.seq.num_seqs;
+    const int a = g / nseq, doc = g - a * nseq;
+    const DocSpan sp = doc_span(p.seq, doc);
+    if (!sp.ok) return 64;
+    const int nblk = (sp.lq + 127) >> 7;
+    if (a >= nblk) return 64;
+    const int q0 = (nblk - 1 - a) * 128;
+    const int nkv_all = (sp.lk + 127) >> 7;
+    int nkv = nkv_all;
+    if (p.causal) {
+      const int last = min(sp.lq, q0 + 128) - 1 + sp.shift;
+      nkv = last < 0 ? 0 : min((last >> 7) + 1, nkv_all);
+    }
+    return nkv > 0 ? 64 - min(nkv, 64) : 63;
+  }
+};
+
+// Every head's slope and table column fit the staging area (H + nb H floats).
+constexpr int kFwdHeadStage = 2304;
+__host__ __device__ inline bool fwd_pers_stages_heads(const BiasParams &b, int H) {
+  return b.has_bias && H + (b.table ? b.nb * H : 0) <= kFwdHeadStage;
+}
+size_t fwd_pers_smem_bytes(const BiasParams &b, int H) {
+  return fwd_smem_bytes(64, b.lut_len, 1) + (((size_t)b.lut_len + 15) & ~(size_t)15) +
+         kLptRounds * 4 + (fwd_pers_stages_heads(b, H) ? (size_t)kFwdHeadStage * 4 : 0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D, 1>::NTHREADS, FwdCfg<D, 1>::MIN_BLOCKS)
+    fat_fwd_pers_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D, 1>;
+  static_assert(C::SEP_P, "one-tile CTAs keep P in its own TMEM columns");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.seq.total_tokens, H = p.seq.num_heads, nseq = p.seq.num_seqs;
+  const int nqb = (p.seq.max_seqlen + 127) >> 7;
+  const long long n_dh = (long long)H * nseq;
+  const long long n_virtual = (long long)nqb * n_dh;
+
+  uint8_t *sQ = sm + C::OFF_Q, *sK = sm + C::OFF_K, *sV = sm + C::OFF_V;
+  float *lut = reinterpret_cast<float *>(sm + C::OFF_LUT);
+  int *thr_s = reinterpret_cast<int *>(sm + C::OFF_LUT + ((p.bias.lut_len * 4 + 15) & ~15));
+  float *col_s = reinterpret_cast<float *>(thr_s + kMaxThresholds);
+  uint8_t *lbk = reinterpret_cast<uint8_t *>(col_s + 256);  // bucket of each delta
+  int *lpt_list = reinterpret_cast<int *>(lbk + ((p.bias.lut_len + 15) & ~15));
+  // every head's slope and table column, staged once when they fit (fwd_pers_stages_heads), so
+  // that a change of head between items reads shared memory only
+  float *heads_s = reinterpret_cast<float *>(lpt_list + kLptRounds);
+  const bool staged_heads = fwd_pers_stages_heads(p.bias, H);
+
+  // corrupt or out-of-bound cu_seqlens entries, reported once (their items are skipped)
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < nseq; i += blockDim.x) {
+      const DocSpan sp = doc_span(p.seq, i);
+      if (!sp.ok || sp.lq > p.seq.max_seqlen || sp.lk > p.seq.max_seqlen_k)
+        atomicOr(p.err, FAT_DEVERR_SEQLENS);
+    }
+  }
+  // this CTA's ranks, longest first (the K/V ring is the scratch: nothing is loaded yet)
+  static_assert(2 * C::NS * C::TILE >= lpt_scratch_bytes(C::NTHREADS), "ordering scratch");
+  const int lpt_n = p.lpt ? lpt_order(nqb * nseq, nseq, H, kLptRounds, FwdLptBucket{p}, sK,
+                                      lpt_list)
+                          : -1;
+  // the item of round v (advanced past items without rows); false when the walk is done
+  auto next_item = [&](long long &v, FwdItem &it) -> bool {
+    for (;; ++v) {
+      long long rank;
+      if (lpt_n >= 0) {
+        if (v >= lpt_n) return false;
+        rank = lpt_list[v];
+      } else {
+        rank = v * gridDim.x +
+               ((v & 1) ? (long long)gridDim.x - 1 - blockIdx.x : (long long)blockIdx.x);
+        if (rank >= n_virtual) return false;
+      }
+      const int a = (int)(rank / n_dh);
+      const long long rest = rank - (long long)a * n_dh;
+      const int doc = (int)(rest / H);
+      const DocSpan sp = doc_span(p.seq, doc);
+      if (!sp.ok) continue;
+      const int nblk = (sp.lq + 127) >> 7;
+      if (a >= nblk) continue;
+      it.h = (int)(rest - (long long)doc * H);
+      it.seq_start = sp.sq;
+      it.L = sp.lq;
+      it.seq_start_k = sp.sk;
+      it.Lk = sp.lk;
+      it.shift = sp.shift;
+      it.q0 = (nblk - 1 - a) * 128;
+      const int nkv_all = (sp.lk + 127) >> 7;
+      int nkv = nkv_all;
+      if (p.causal) {
+        const int last = min(sp.lq, it.q0 + 128) - 1 + sp.shift;
+        nkv = last < 0 ? 0 : min((last >> 7) + 1, nkv_all);
+      }
+      it.nkv = nkv;
+      // causal rows take their key tiles from the diagonal backwards (the largest ALiBi bias
+      // first, so the running max rarely grows afterwards)
+      it.kt0 = p.causal ? nkv - 1 : 0;
+      it.kdir = p.causal ? -1 : 1;
+      return true;
+    }
+  };
+  long long v_first = 0;
+  FwdItem first;
+  if (!next_item(v_first, first)) return;  // nothing to do: before any barrier or allocation
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+  uint64_t *q_full = bars;
+  uint64_t *q_empty = q_full + 1;   // the item's S products have read Q
+  uint64_t *k_full = q_empty + 1;   // [NS]
+  uint64_t *v_full = k_full + C::NS;
+  uint64_t *k_empty = v_full + C::NS;
+  uint64_t *v_empty = k_empty + C::NS;
+  uint64_t *s_full = v_empty + C::NS;
+  uint64_t *p_ready = s_full + 1;
+  uint64_t *o_ready = p_ready + 1;
+  uint64_t *s_free = o_ready + 1;   // S has been read into registers
+  uint64_t *o_free = s_free + 1;    // the item's O has been read out of TMEM
+  uint64_t *mma_done = o_free + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  static_assert((2 + 4 * C::NS + 6) * 8 + 8 <= 256, "barrier block");
+
+  if (warp == C::WARP_PROD && lane == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(o_ready, 1);
+    mbar_init(s_free, 128);
+    mbar_init(o_free, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  // bias: thresholds and the first head's table column staged, the bucket of every delta kept
+  // (head-independent), the first head's table built
+  const bool has_table = p.bias.table != nullptr, has_slopes = p.bias.slopes != nullptr;
+  FarBias *fbs = reinterpret_cast<FarBias *>(sm + C::OFF_WD + 32);
+  bias_stage(p.bias, first.h, H, thr_s, col_s, tid, C::NTHREADS);
+  if (staged_heads) {  // slopes [H], then the columns [H][nb] (table rows are [nb][H])
+    if (has_slopes)
+      for (int i = tid; i < H; i += C::NTHREADS) heads_s[i] = __ldg(p.bias.slopes + i);
+    if (has_table)
+      for (int i = tid; i < p.bias.nb * H; i += C::NTHREADS)
+        heads_s[H + (i % H) * p.bias.nb + i / H] = __ldg(p.bias.table + i);
+  }
+  __syncthreads();
+  {
+    const float slope = has_slopes ? __ldg(p.bias.slopes + first.h) : 0.f;
+    for (int i = tid; i < p.bias.lut_len; i += C::NTHREADS) {
+      const int delta = p.bias.lut_lo + i;
+      const int bk = has_table ? t5_bucket_staged(delta, p.bias, thr_s) : 0;
+      lbk[i] = static_cast<uint8_t>(bk);
+      lut[i] = bias_log2_staged(bk, delta, slope, p.bias, col_s);
+    }
+    if (tid == 0) {
+      *reinterpret_cast<Watchdog *>(sm + C::OFF_WD) =
+          Watchdog{abort_flag, p.err, FAT_DEVERR_TIMEOUT_FWD, p.timeout_ns};
+      *fbs = far_bias_staged(p.bias, thr_s, col_s, slope);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog &wd = *reinterpret_cast<const Watchdog *>(sm + C::OFF_WD);
+
+  if (warp >= C::WARP_PROD) regs_dec<C::REG_OTHER>();
+
+  if (warp == C::WARP_PROD) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_k[C::NS], last_v[C::NS];
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) last_k[s] = last_v[s] = -1;
+      int ni = 0;       // items with keys so far (the phases of q_full / q_empty)
+      int last_q = -1;  // phase of the last Q copy issued
+      long long J = 0;  // K/V stream position
+      bool ok = !(p.debug_flags & 1);  // test hook: no copies, the consumers' waits run out
+      long long v = v_first;
+      FwdItem it = first;
+      if (ok) do {
+        if (it.nkv == 0) continue;
+        if (ni > 0 && !mbar_wait(q_empty, (ni - 1) & 1, wd)) { ok = false; break; }
+        mbar_arrive_expect_tx(q_full, C::TILE);
+        tma_load_3d(&tm_q, q_full, sQ, 0, it.h, it.seq_start + it.q0);
+        last_q = ni;
+        const int hk = it.h / p.seq.group;
+        for (int j = 0; ok && j < it.nkv; ++j) {
+          const long long g = J + j;
+          const int s = (int)(g % C::NS), u = (int)(g / C::NS);
+          const int krow = it.seq_start_k + 128 * (it.kt0 + it.kdir * j);
+          if (u > 0 && !mbar_wait(k_empty + s, (u - 1) & 1, wd)) { ok = false; break; }
+          mbar_arrive_expect_tx(k_full + s, C::TILE);
+          tma_load_3d(&tm_k, k_full + s, sK + s * C::TILE, 0, hk, krow);
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == s) last_k[x] = u;
+          if (u > 0 && !mbar_wait(v_empty + s, (u - 1) & 1, wd)) { ok = false; break; }
+          mbar_arrive_expect_tx(v_full + s, C::TILE);
+          tma_load_3d(&tm_v, v_full + s, sV + s * C::TILE, 0, hk, krow);
+#pragma unroll
+          for (int x = 0; x < C::NS; ++x)
+            if (x == s) last_v[x] = u;
+        }
+        if (!ok) break;
+        J += it.nkv;
+        ++ni;
+      } while (++v, next_item(v, it));
+      // teardown: every copy this thread issued has landed before the CTA exits
+      if (last_q >= 0) mbar_wait_teardown(q_full, last_q & 1, kTeardownNs);
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) {
+        if (last_k[s] >= 0) mbar_wait_teardown(k_full + s, last_k[s] & 1, kTeardownNs);
+        if (last_v[s] >= 0) mbar_wait_teardown(v_full + s, last_v[s] & 1, kTeardownNs);
+      }
+      (void)ok;
+    }
+  } else if (warp == C::WARP_MMA) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t dS = tmem + C::COL_S0, dO = tmem + C::COL_O0, aP = tmem + C::COL_P0;
+      const uint64_t dQd = sw128_desc(smem_u32(sQ), 16, 1024);
+      const uint64_t dKd = sw128_desc(smem_u32(sK), 16, 1024);
+      const uint64_t dVd = sw128_desc(smem_u32(sV), C::BLK, 1024);
+      auto issue_S = [&](int st) {
+        const uint64_t kd = dKd + ((st * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::BLK + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(dS, dQd + off, kd + off, C::IDESC_S, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int st, bool acc) {
+        const uint64_t vd = dVd + ((st * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(dO, aP + kk * 8, vd + ((kk * 2048) >> 4), C::IDESC_PV,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      int ni = 0;
+      long long J = 0, GS = 0;  // K/V stream position, steps so far
+      bool ok = true;
+      long long v = v_first;
+      FwdItem it = first;
+      do {
+        if (it.nkv == 0) continue;
+        const int s0 = (int)(J % C::NS), u0 = (int)(J / C::NS);
+        // S is free: the softmax has read the previous step's S (waited for below, in order)
+        if (!mbar_wait(q_full, ni & 1, wd) || !mbar_wait(k_full + s0, u0 & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_S(s0);
+        mma_commit(s_full);
+        mma_commit(k_empty + s0);
+        if (it.nkv == 1) mma_commit(q_empty);
+        for (int jl = 0; jl < it.nkv; ++jl) {
+          const long long g = GS + jl, j = J + jl;
+          const int s = (int)(j % C::NS), u = (int)(j / C::NS);
+          // the next S once the softmax has read this one
+          if (!mbar_wait(s_free, g & 1, wd)) { ok = false; break; }
+          if (jl + 1 < it.nkv) {
+            const int sn = (int)((j + 1) % C::NS), un = (int)((j + 1) / C::NS);
+            if (!mbar_wait(k_full + sn, un & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+            issue_S(sn);
+            mma_commit(s_full);
+            mma_commit(k_empty + sn);
+            if (jl + 2 == it.nkv) mma_commit(q_empty);  // the item's last S reads Q
+          }
+          if (!mbar_wait(v_full + s, u & 1, wd) || !mbar_wait(p_ready, g & 1, wd)) {
+            ok = false;
+            break;
+          }
+          // the first P V overwrites O: the previous item's rows have been read out
+          if (jl == 0 && ni > 0 && !mbar_wait(o_free, (ni - 1) & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          issue_PV(s, jl > 0);
+          mma_commit(o_ready);
+          mma_commit(v_empty + s);
+        }
+        if (!ok) break;
+        GS += it.nkv;
+        J += it.nkv;
+        ++ni;
+      } while (++v, next_item(v, it));
+      (void)ok;
+      mma_commit(mma_done);
+      mbar_wait_teardown(mma_done, 0, kTeardownNs);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ softmax warpgroup
+    regs_inc<C::REG_SM>();
+    const int r = tid & 127;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::COL_S0;
+    const uint32_t tO = tmem + lane_off + C::COL_O0;
+    const uint32_t tP = tmem + lane_off + C::COL_P0;
+    int cur_h = first.h;
+    long long GS = 0;  // steps so far (the phases of s_full, s_free, p_ready, o_ready)
+    int ni = 0;        // items with keys so far (the phases of o_free)
+    bool ok = true;
+    long long v = v_first;
+    FwdItem it = first;
+    do {
+      if (it.h != cur_h && p.bias.has_bias) {
+        // the next head's table column and bias table (only these 128 threads read them)
+        named_bar_sync(1, 128);
+        float slope;
+        const float *col;
+        if (staged_heads) {
+          slope = has_slopes ? heads_s[it.h] : 0.f;
+          col = heads_s + H + it.h * p.bias.nb;
+        } else {
+          slope = has_slopes ? __ldg(p.bias.slopes + it.h) : 0.f;
+          if (has_table)
+            for (int i = r; i < p.bias.nb; i += 128)
+              col_s[i] = __ldg(p.bias.table + (size_t)i * H + it.h);
+          named_bar_sync(1, 128);
+          col = col_s;
+        }
+        for (int i = r; i < p.bias.lut_len; i += 128) {
+          const int delta = p.bias.lut_lo + i;
+          lut[i] = bias_log2_staged(lbk[i], delta, slope, p.bias, col);
+        }
+        if (r == 0) *fbs = far_bias_staged(p.bias, thr_s, col, slope);
+        named_bar_sync(1, 128);
+      }
+      cur_h = it.h;
+      const int qrow = it.q0 + r;
+      if (it.nkv == 0) {  // no key for any row of the block: empty rows, TMEM untouched
+        fwd_write_empty_rows<D, false>(p, it.seq_start, it.q0, min(it.L - it.q0, 128), it.h, 0,
+                                       it.q0, r, 128);
+        continue;
+      }
+      const FarBias fb = *fbs;
+      float m = -INFINITY, l = 0.f;
+      for (int jl = 0; jl < it.nkv; ++jl) {
+        const long long g = GS + jl;
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd));
+        if (!ok) break;
+        tc_fence_after();
+        const int ks = 128 * (it.kt0 + it.kdir * jl);
+        const int d0 = ks - it.q0 - it.shift;  // delta of (row 0, key 0) of the tile
+        const bool need_mask = (ks + 128 > it.Lk) || (p.causal && d0 + 127 > 0);
+        const int lim = min(it.Lk - ks, p.causal ? (qrow + it.shift - ks + 1) : 128);
+        int mode;
+        float rowc = 0.f, kk = 0.f;
+        if (!p.bias.has_bias) {
+          mode = 0;
+        } else if (d0 - 127 >= p.bias.sat_pos) {
+          kk = fb.k_pos;
+          rowc = fmaf(fb.k_pos, (float)(d0 - r), fb.c_pos);
+          mode = has_slopes ? 1 : 0;
+        } else if (d0 + 127 <= -p.bias.sat_neg) {
+          kk = fb.k_neg;
+          rowc = fmaf(fb.k_neg, (float)(d0 - r), fb.c_neg);
+          mode = has_slopes ? 1 : 0;
+        } else {
+          mode = 2;
+        }
+        const float *lut_row = lut + (d0 - r - p.bias.lut_lo);
+        uint32_t x[4][32];
+        float mx;  // row max of x
+#define FAT_LOGITS(MODE, MASK) \
+  fwd_logits<MODE, MASK, false>(tS, x, p.scale_log2, rowc, kk, lut_row, lim, 0)
+        if (mode == 0)
+          mx = need_mask ? FAT_LOGITS(0, true) : FAT_LOGITS(0, false);
+        else if (mode == 1)
+          mx = need_mask ? FAT_LOGITS(1, true) : FAT_LOGITS(1, false);
+        else
+          mx = need_mask ? FAT_LOGITS(2, true) : FAT_LOGITS(2, false);
+#undef FAT_LOGITS
+        tc_fence_before();
+        mbar_arrive(s_free);  // S is in registers: the next S may be computed
+        if (jl == 0) {
+          m = mx;
+        } else {
+          // P and O are still read by the previous step's P V
+          ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (g - 1) & 1, wd));
+          if (!ok) break;
+          tc_fence_after();
+          const bool fresh = m == -INFINITY;  // no key of this row so far
+          const bool need = fresh ? (mx != -INFINITY) : (mx > m + 32.0f);
+          if (__any_sync(0xffffffffu, need)) {
+            // O holds sum_{i<j} P_i V_i relative to the old max: rescaled once
+            const float f = need ? (fresh ? 0.f : ex2(m - mx)) : 1.0f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+              tmem_st32(tO + c * 32, o);
+            }
+            if (need) {
+              l *= f;
+              m = mx;
+            }
+          }
+        }
+        uint64_t sum2[4];  // four short dependency chains
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sum2[k] = f2_pack(0.f, 0.f);
+        {
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          fwd_exp_pass<true>(x, f2_pack(m_use, m_use), tP, sum2);
+        }
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(f2_add(sum2[0], sum2[2]), s0, s1);
+          f2_unpack(f2_add(sum2[1], sum2[3]), s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+      }
+      if (!ok) break;
+      // the item's rows: O / l and lse once its last P V is done; then O is free for the next
+      const long long g_last = GS + it.nkv - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(o_ready, g_last & 1, wd));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const bool valid = qrow < it.L;
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        const float lse_row = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+        __nv_bfloat16 *orow = p.out + ((size_t)(it.seq_start + qrow) * H + it.h) * D;
+        uint32_t o[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32_issue(tO + c * 32, o[c]);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32_fence(o[c]);
+        tc_fence_before();
+        mbar_arrive(o_free);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[c][2 * i]) * inv_l,
+                                __uint_as_float(o[c][2 * i + 1]) * inv_l);
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid && p.lse != nullptr) p.lse[(size_t)it.h * T + it.seq_start + qrow] = lse_row;
+      }
+      GS += it.nkv;
+      ++ni;
+    } while (++v, next_item(v, it));
+    (void)ni;
+    grid_dep_launch();  // a dependent grid (the backward preprocessing) may be scheduled
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // One output row merged from S <= 64 normalised partial rows o_s with their (natural) lse l_s
 // by one warp: lse = log sum_s exp(l_s), out = sum_s exp(l_s - lse) o_s; a row with no key in
 // any range gets out 0, lse -inf. Lane s loads l_s and l_{s+32} (all S loads in flight at once),
@@ -900,6 +1413,62 @@ int launch_fwd_t(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &m
   return (int)e;
 }
 
+// Persistent one-tile forward: as many CTAs as fit at once (two per SM unless the bias table
+// makes them too large), at most one per item. Shared memory beyond the one-tile CTA's: the
+// bucket of each delta, the CTA's item list and, when they fit, every head's bias constants.
+int launch_fwd_pers(const FwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                    const CUtensorMap &mv, cudaStream_t stream) {
+  using C = FwdCfg<64, 1>;
+  const size_t smem = fwd_pers_smem_bytes(p.bias, p.seq.num_heads);
+  if (smem > (size_t)kSmemLimit) return (int)cudaErrorInvalidValue;
+  const void *fn = (const void *)fat_fwd_pers_kernel<64>;
+  cudaError_t e = (cudaError_t)prepare_kernel(fn, smem, C::NTHREADS, C::REGS_NEEDED);
+  if (e != cudaSuccess) return (int)e;  // reason recorded by prepare_kernel
+  // CTAs per SM: the launch bound's two unless shared memory holds fewer (1 KB per block is
+  // reserved by the system)
+  static std::mutex mu;
+  static int smem_sm[64] = {0};
+  int dev = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lk(mu);
+    if (smem_sm[dev] == 0) {
+      // the largest shared-memory share of the SM, so that the CTAs counted here fit at once
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+          cudaDeviceGetAttribute(&smem_sm[dev], cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                 dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        smem_sm[dev] = 0;
+      }
+    }
+    per_sm = smem_sm[dev];
+  }
+  const int bps = std::max(1, std::min<int>(C::MIN_BLOCKS, (int)(per_sm / (smem + 1024))));
+  const int sms = sm_count();
+  const long long nqb = (p.seq.max_seqlen + 127) / 128;
+  const long long items = nqb * p.seq.num_heads * p.seq.num_seqs;
+  if (items == 0) return 0;
+  const long long grid = std::min<long long>(items, (long long)(sms > 0 ? sms : 1) * bps);
+  FwdParams pp = p;
+  // documents of different lengths: longest-first (with equal documents the rank order is)
+  const bool unequal =
+      (long long)p.seq.total_tokens != (long long)p.seq.num_seqs * p.seq.max_seqlen ||
+      (long long)p.seq.total_k != (long long)p.seq.num_seqs * p.seq.max_seqlen_k;
+  pp.lpt = (unequal && nqb * p.seq.num_seqs <= kLptGroups) ? 1 : 0;
+  fat_fwd_pers_kernel<64><<<(unsigned)grid, C::NTHREADS, smem, stream>>>(mq, mk, mv, pp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, fat_fwd_pers_kernel<64>);
+    char msg[160];
+    snprintf(msg, sizeof msg, "%s [regs %d, max threads %d, local %zu B, dyn smem %zu B]",
+             cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, (size_t)fa.localSizeBytes,
+             smem);
+    set_last_error("kernel launch", (int)e, msg);
+  }
+  return (int)e;
+}
+
 int fwd_tiles_per_cta(int head_dim, int max_seqlen) {
   return head_dim == 64 && max_seqlen <= kFwdOneTileMaxRows ? 1 : 2;
 }
@@ -914,6 +1483,16 @@ int launch_fwd(const FwdParams &p, int head_dim, const void *q, const void *k, c
     return (int)cudaErrorInvalidValue;
   if (head_dim == 128) return launch_fwd_t<128, 2>(p, mq, mk, mv, stream);
   // a split last wave is planned for two-tile CTAs
+  if (p.tail_splits == 0 && fwd_tiles_per_cta(head_dim, p.seq.max_seqlen) == 1 &&
+      p.kv_splits == 1 && !(p.debug_flags & 4)) {
+    // Persistent CTAs once each resident CTA gets three items or more (at most T / 128 + n
+    // blocks per head): with fewer, the grid of one-tile CTAs, two per SM, overlaps the fixed
+    // costs as well and runs its steps with fewer registers spilled.
+    const long long blocks = ((long long)p.seq.total_tokens / 128 + p.seq.num_seqs) *
+                             p.seq.num_heads;
+    if ((p.debug_flags & 8) || blocks >= 3LL * 2 * std::max(1, sm_count()))
+      return launch_fwd_pers(p, mq, mk, mv, stream);
+  }
   if (p.tail_splits == 0 && fwd_tiles_per_cta(head_dim, p.seq.max_seqlen) == 1) {
     FwdParams pf = p;
     // documents of different lengths: the flat grid, when it has fewer blocks

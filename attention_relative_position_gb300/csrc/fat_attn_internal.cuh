@@ -71,6 +71,105 @@ __device__ __forceinline__ DocSpan doc_span(const SeqParams &s, int doc) {
   d.shift = d.lk - d.lq;
   return d;
 }
+// ---- longest-first work order for the persistent kernels ----------------------------------------
+// Work order by decreasing cost (documents of different lengths): at most kLptGroups groups are
+// sorted, and each CTA keeps at most kLptRounds item ranks.
+constexpr int kLptGroups = 8192;
+constexpr int kLptRounds = 128;
+// shared-memory scratch lpt_order needs for a block of nthreads threads
+__host__ __device__ constexpr int lpt_scratch_bytes(int nthreads) {
+  return kLptGroups + 4 * (68 + 68 * (nthreads / 32) + kLptGroups);
+}
+
+// The item ranks this CTA walks (all threads of the block call it; it synchronises the block).
+// Items are ranked r = a * (nseq * H) + doc * H + h for a group g = a * nseq + doc (a is the key
+// tile of the backward, the reversed query block of the forward) and head h; bucket(g) gives
+// 0..63 (lower costs more) or 64 (a group without items). A plain round-robin over the rank
+// order balances the CTAs only when the documents have one length; otherwise a CTA's share
+// depends on which documents its rounds happen to hit. Here the groups are sorted by bucket with
+// a stable counting sort (so that the H heads of a group stay adjacent: the two CTAs of a pair
+// keep walking neighbouring heads) and their items dealt in alternating rounds (round v of CTA
+// c takes position v G + c, or v G + G - 1 - c when v is odd, G CTAs): the longest-processing-
+// time-first rule. Returns the number of ranks written to list, or -1 when the CTAs would need
+// more than max_rounds rounds (every CTA reaches the same answer). scratch: shared memory the
+// block does not use yet, lpt_scratch_bytes(blockDim.x) bytes; ng <= kLptGroups.
+template <typename BucketFn>
+__device__ int lpt_order(int ng, int nseq, int H, int max_rounds, BucketFn bucket,
+                         uint8_t *scratch, int *list) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  uint8_t *key = scratch;  // bucket of each group
+  int *hist = reinterpret_cast<int *>(scratch + ((ng + 15) & ~15));  // [68]
+  int *wcnt = hist + 68;                                              // [warps][68]
+  int *sorted = wcnt + nwarps * 68;                                   // [groups with items]
+  for (int i = tid; i < 68; i += nthreads) hist[i] = 0;
+  __syncthreads();
+  for (int g = tid; g < ng; g += nthreads) {
+    const int b = bucket(g);
+    key[g] = static_cast<uint8_t>(b);
+    atomicAdd(hist + b, 1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // bucket starts (exclusive scan of the 65 counts)
+    int run = 0;
+    for (int b0 = 0; b0 < 65; b0 += 32) {
+      const int b = b0 + lane;
+      const int c = b < 65 ? hist[b] : 0;
+      int x = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (b < 65) hist[b] = run + x - c;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  __syncthreads();
+  const int n_valid = hist[64];
+  // stable scatter, one group per thread and chunk: rank within the warp by matching buckets,
+  // warp offsets per bucket from the chunk's counts
+  for (int base = 0; base < ng; base += nthreads) {
+    for (int i = tid; i < nwarps * 68; i += nthreads) wcnt[i] = 0;
+    __syncthreads();
+    const int g = base + tid;
+    const int b = g < ng ? key[g] : 255;
+    const unsigned peers = __match_any_sync(0xffffffffu, b);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (b < 64 && rank_w == 0) wcnt[warp * 68 + b] = __popc(peers);
+    __syncthreads();
+    if (tid < 64) {
+      int run = hist[tid];
+      for (int w = 0; w < nwarps; ++w) {
+        const int c = wcnt[w * 68 + tid];
+        wcnt[w * 68 + tid] = run;
+        run += c;
+      }
+      hist[tid] = run;
+    }
+    __syncthreads();
+    if (b < 64) sorted[wcnt[warp * 68 + b] + rank_w] = g;
+    __syncthreads();
+  }
+  const long long total = (long long)n_valid * H;
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long rounds = (total + G - 1) / G;
+  if (rounds > max_rounds) return -1;
+  // rounds before the last are full; the last holds this CTA's position if it is < total
+  const long long last = (rounds - 1) * G + (((rounds - 1) & 1) ? G - 1 - c : c);
+  const int n = rounds == 0 ? 0 : (int)(rounds - 1) + (last < total ? 1 : 0);
+  const long long n_dh = (long long)H * nseq;
+  for (int v = tid; v < n; v += nthreads) {
+    const long long pos = (long long)v * G + ((v & 1) ? G - 1 - c : c);
+    const int g = sorted[pos / H];
+    const int h = (int)(pos % H);
+    const int a = g / nseq, doc = g - a * nseq;
+    list[v] = (int)(a * n_dh + (long long)doc * H + h);
+  }
+  __syncthreads();
+  return n;
+}
+
 // natural-log lse of a row -> the log2 statistic the backward subtracts; a row that saw no key
 // (lse = -inf) gets +inf, so that every P of the row is 2^-inf = 0
 __device__ __forceinline__ float lse_to_log2_stat(float lse) {
@@ -210,6 +309,8 @@ struct FwdParams {
   // i + 1) (at least its ceil(L_i / 128) blocks; an extra id exits at once), so no CTA is spent
   // on rows a short document does not have. 0: the (block, head, document) grid.
   int flat;
+  // Persistent one-tile forward: walk the items longest-first (filled by the launcher).
+  int lpt;
 };
 
 struct BwdParams {

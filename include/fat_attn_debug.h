@@ -25,7 +25,11 @@ int fat_attn_debug_buckets(long long delta_lo, int n, int num_buckets, int max_d
 /*
  * Process-wide knobs for the watchdog test. timeout_ns: time limit of every pipeline wait
  * (<= 0 restores the default of 4 s). flags bit 0: the forward producer warp issues no copies,
- * so the consumers' waits run out, the kernel records FAT_DEVERR_TIMEOUT_FWD and exits cleanly.
+ * so the consumers' waits run out, the kernel records FAT_DEVERR_TIMEOUT_FWD and exits cleanly;
+ * bit 1: likewise for the backward's first copies (FAT_DEVERR_TIMEOUT_BWD). The forward over
+ * short documents at head_dim 64 runs as persistent CTAs when there are enough 128-row blocks,
+ * else as a grid of one-tile CTAs (both compute the same results): bit 2 takes the grid, bit 3
+ * the persistent CTAs, whatever the size (the tests compare them).
  */
 void fat_attn_debug_set_watchdog(long long timeout_ns, int flags);
 
