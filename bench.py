@@ -723,7 +723,13 @@ def run_ours(args, rank, world, local_rank):
     # else as one CTA per key tile
     persistent = w.head_dim == 64 and (w.max_seqlen + 127) // 128 <= 64
     bwd_name = "fat_bwd_kernel" if persistent else "fat_bwd_tiles_kernel"
-    kernels = {"fwd": ("fat_fwd_kernel", f, med["fwd"], "fat_attn_fwd.cu"),
+    # the forward runs as persistent one-tile CTAs for d = 64, documents of <= 2048 rows and at
+    # least three 128-row blocks per resident CTA (two per SM), else as a grid
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks = (w.total_tokens // 128 + len(w.seqlens)) * w.num_heads
+    fwd_pers = w.head_dim == 64 and w.max_seqlen <= 2048 and blocks >= 3 * 2 * sms
+    fwd_name = "fat_fwd_pers_kernel" if fwd_pers else "fat_fwd_kernel"
+    kernels = {"fwd": (fwd_name, f, med["fwd"], "fat_attn_fwd.cu"),
                "bwd_main": (bwd_name, 2.5 * f, med["bwd_main"], "fat_attn_bwd.cu")}
     dom = max(kernels, key=lambda k: kernels[k][2])
     kname, kflops, kms, ksrc = kernels[dom]
