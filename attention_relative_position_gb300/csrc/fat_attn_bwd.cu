@@ -1019,6 +1019,13 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, ii & 1, wd));
       if (!ok) break;
       tc_fence_after();
+      // Own key/value heads, d = 64: the item's dK and dV rows go through shared memory, so that
+      // the global stores write whole 128-byte rows (a thread holds 16 channels of one row, and
+      // rows of one head lie H d 2 bytes apart: stored from registers, every store instruction
+      // touched 32 lines, about 2 us per item). The staging area is the dS buffer the item's
+      // last step did not use: its products (and the previous step's dQ) have completed.
+      const bool stage = D == 64 && p.dk_acc == nullptr;
+      const uint32_t stg = smem_u32(sDS) + ((gs + w.nq) & 1) * C::DSTILE;  // dK [128][64], dV
       {
         const int cb = wg * (D / 4);
         const size_t kvrow = ((size_t)(w.seq_start_k + krow) * p.seq.num_heads_kv + w.hk) * D + cb;
@@ -1033,13 +1040,35 @@ __global__ void __launch_bounds__(640, 1)
             tc_fence_before();
             mbar_arrive(dkdv_free);
           }
-          if (row_valid) store_dkdv_row(p, kvrow + 16 * c, a, b);
+          if (stage) {
+            // row r (128 bytes) at 128 r, its 16-byte chunk j at (j ^ (r & 7)) 16: this
+            // warpgroup's chunks 2 wg, 2 wg + 1 land in different bank groups across a warp
+            uint32_t pa[8], pb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
+                                  __uint_as_float(a[2 * i + 1]) * p.scale);
+              pb[i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+            }
+            const uint32_t row = stg + r * 128;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t off = static_cast<uint32_t>(((2 * wg + h2) ^ (r & 7)) << 4);
+              st_shared_v4(row + off, pa[4 * h2], pa[4 * h2 + 1], pa[4 * h2 + 2], pa[4 * h2 + 3]);
+              st_shared_v4(row + 128 * 128 + off, pb[4 * h2], pb[4 * h2 + 1], pb[4 * h2 + 2],
+                           pb[4 * h2 + 3]);
+            }
+          } else if (row_valid) {
+            store_dkdv_row(p, kvrow + 16 * c, a, b);
+          }
         }
       }
-      // ---- table gradient of the item, then the next item's bias table (between two syncs
-      // of the P/dS warpgroups)
+
+      // ---- table gradient of the item, then the next item's bias table, and the staged dK, dV
+      // rows written back (between two syncs of the P/dS warpgroups: bounded waits, so that a
+      // warp leaving on a timeout cannot hold the others)
       const bool more = slots[ii % kItemSlots].more != 0;
-      if (do_dbias || new_head) {
+      if (do_dbias || new_head || stage) {
         if (do_dbias) {  // far sides: one bucket each, added at the saturation deltas
           float a = acc_pos, b = acc_neg;
 #pragma unroll
@@ -1055,6 +1084,22 @@ __global__ void __launch_bounds__(640, 1)
         if (new_head && tid < p.bias.nb) tcol_s[tid] = tcol_next;
         mbar_arrive(comp_sync);
         if (!__all_sync(0xffffffffu, mbar_wait(comp_sync, 0, wd))) { ok = false; break; }
+        if (stage) {  // 2 tensors x 128 rows x 8 chunks, eight threads per row
+          const int nvalid = min(128, w.Lk - w.ks);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int idx = tid + C::NCOMP * k;
+            const int t = idx >> 10, rr = (idx >> 3) & 127, ch = idx & 7;
+            const uint4 val =
+                ld_shared_v4(stg + t * (128 * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            if (rr < nvalid) {
+              __nv_bfloat16 *dst =
+                  (t == 0 ? p.dk : p.dv) +
+                  ((size_t)(w.seq_start_k + w.ks + rr) * p.seq.num_heads_kv + w.hk) * D + 8 * ch;
+              *reinterpret_cast<uint4 *>(dst) = val;
+            }
+          }
+        }
         if (do_dbias) {
           // per-delta sums to per-bucket sums: each warp takes 32 consecutive deltas, runs of
           // equal buckets are summed with a segmented scan and each run adds once
