@@ -1228,6 +1228,10 @@ __global__ void __launch_bounds__(640, 1)
     return (i0 + (k >= nq_all ? k - nq_all : k)) * C::BQ;
   };
   const bool do_dbias = p.dbias != nullptr && p.bias.table != nullptr;
+  // dK, dV of own key/value heads go back as whole rows through the Q/dO ring (a thread holds
+  // D / 4 channels of one row, and rows of one head lie H d 2 bytes apart)
+  const bool staged_out = !TAIL && p.dk_acc == nullptr;
+  static_assert(2 * C::NS * C::QTILE >= 2 * 128 * D * 2, "staging fits the Q/dO ring");
 
   uint8_t *sK = sm + C::OFF_K, *sV = sm + C::OFF_V, *sQ = sm + C::OFF_Q, *sDO = sm + C::OFF_DO;
   uint8_t *sDS = sm + C::OFF_DS;
@@ -1733,6 +1737,28 @@ __global__ void __launch_bounds__(640, 1)
         tmem_ld16_issue(tmem + lane_off + C::COL_DV + cb + 16 * c, b);
         tmem_ld16_fence(a);
         tmem_ld16_fence(b);
+        if (staged_out) {
+          // bf16 rows into the Q/dO ring (its last readers, the dK and dV products, are done):
+          // row r at r D 2, its 16-byte chunk j in 128-byte segment j / 8 at ((j % 8) ^ (r % 8))
+          uint32_t pa[8], pb[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            pa[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * p.scale,
+                                __uint_as_float(a[2 * i + 1]) * p.scale);
+            pb[i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+          }
+          const uint32_t row = smem_u32(sQ) + r * (D * 2);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = (cb + 16 * c) / 8 + h2;
+            const uint32_t off =
+                static_cast<uint32_t>((j >> 3) * 128 + (((j & 7) ^ (r & 7)) << 4));
+            st_shared_v4(row + off, pa[4 * h2], pa[4 * h2 + 1], pa[4 * h2 + 2], pa[4 * h2 + 3]);
+            st_shared_v4(row + 128 * D * 2 + off, pb[4 * h2], pb[4 * h2 + 1], pb[4 * h2 + 2],
+                         pb[4 * h2 + 3]);
+          }
+          continue;
+        }
         if (!row_valid) continue;
         if (TAIL && p.dk_acc == nullptr)
           add_dkdv_tail<D>(p, blockIdx.x / p.tail_splits, r, cb + 16 * c, a, b);
@@ -1744,6 +1770,22 @@ __global__ void __launch_bounds__(640, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (staged_out && !*abort_flag) {
+    // the staged dK, dV rows written back whole: consecutive threads take consecutive 16-byte
+    // chunks of a row (2 tensors x 128 rows x D / 8 chunks)
+    const int nvalid = min(128, Lk - ks);
+    constexpr int CPR = D / 8;  // chunks per row
+    for (int idx = tid; idx < 2 * 128 * CPR; idx += C::NTHREADS) {
+      const int t = idx / (128 * CPR), rem = idx - t * (128 * CPR);
+      const int rr = rem / CPR, j = rem - rr * CPR;
+      if (rr >= nvalid) continue;
+      const uint4 val = ld_shared_v4(smem_u32(sQ) + t * (128 * D * 2) + rr * (D * 2) +
+                                     (j >> 3) * 128 + (((j & 7) ^ (rr & 7)) << 4));
+      *reinterpret_cast<uint4 *>((t == 0 ? p.dk : p.dv) +
+                                 ((size_t)(seq_start_k + ks + rr) * p.seq.num_heads_kv + hk) * D +
+                                 8 * j) = val;
+    }
+  }
   if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
