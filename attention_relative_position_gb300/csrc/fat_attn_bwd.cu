@@ -413,8 +413,9 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *kv_full = bars;
   uint64_t *qd_full = kv_full + 1;       // [NS]
   uint64_t *qd_empty = qd_full + C::NS;  // [NS]
-  uint64_t *s_full = qd_empty + C::NS;
-  uint64_t *dp_full = s_full + 1;
+  // (one slot unused: the P/dS warpgroups wait for dP^T only, whose commit follows S^T's
+  // products, so its completion covers both)
+  uint64_t *dp_full = qd_empty + C::NS + 1;
   uint64_t *p_ready = dp_full + 1;
   uint64_t *ds_ready = p_ready + 1;
   uint64_t *ds_empty = ds_ready + 1;     // [2]
@@ -450,7 +451,6 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(qd_full + s, 32);
         mbar_init(qd_empty + s, 2);  // the dV and dK issuers release a stage
       }
-      mbar_init(s_full, 1);
       mbar_init(dp_full, 1);
       mbar_init(p_ready, C::NCOMP);
       mbar_init(ds_ready, C::NCOMP);
@@ -666,7 +666,6 @@ __global__ void __launch_bounds__(640, 1)
         };
         auto issue_sdp = [&](int st) {
           issue_qk(dKk, dQk + ((st * C::QTILE) >> 4), C::COL_S);
-          mma_commit_e(s_full);
           issue_qk(dVk, dDOk + ((st * C::QTILE) >> 4), C::COL_DP);
           mma_commit_e(dp_full);
         };
@@ -860,7 +859,6 @@ __global__ void __launch_bounds__(640, 1)
         const int g = gs + it, st = g % C::NS;
         const int qs = qtile_start(w, it);
         ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (g / C::NS) & 1, wd)) &&
-             __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd)) &&
              __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, wd)) &&
              (g < 2 ||
               __all_sync(0xffffffffu, mbar_wait(ds_empty + (g & 1), ((g >> 1) - 1) & 1, wd)));
@@ -1245,8 +1243,9 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *kv_full = bars;
   uint64_t *qd_full = kv_full + 1;       // [NS]
   uint64_t *qd_empty = qd_full + C::NS;  // [NS]
-  uint64_t *s_full = qd_empty + C::NS;
-  uint64_t *dp_full = s_full + 1;
+  // (one slot unused: the P/dS warpgroups wait for dP^T only, whose commit follows S^T's
+  // products, so its completion covers both)
+  uint64_t *dp_full = qd_empty + C::NS + 1;
   uint64_t *p_ready = dp_full + 1;
   uint64_t *ds_ready = p_ready + 1;
   uint64_t *ds_empty = ds_ready + 1;     // [2]
@@ -1274,7 +1273,6 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(qd_full + s, 32);
         mbar_init(qd_empty + s, 2);  // both MMA issuers release a stage
       }
-      mbar_init(s_full, 1);
       mbar_init(dp_full, 1);
       mbar_init(p_ready, C::NCOMP);
       mbar_init(ds_ready, C::NCOMP);
@@ -1452,7 +1450,6 @@ __global__ void __launch_bounds__(640, 1)
         if (ok) {
           tc_fence_after();
           issue_qk(dKk, dQk, C::COL_S);
-          mma_commit_e(s_full);
           issue_qk(dVk, dDOk, C::COL_DP);
           mma_commit_e(dp_full);
         }
@@ -1468,7 +1465,6 @@ __global__ void __launch_bounds__(640, 1)
             }
             tc_fence_after();
             issue_qk(dKk, dQk + ((stn * C::QTILE) >> 4), C::COL_S);
-            mma_commit_e(s_full);
             issue_qk(dVk, dDOk + ((stn * C::QTILE) >> 4), C::COL_DP);
             mma_commit_e(dp_full);
           }
@@ -1594,7 +1590,6 @@ __global__ void __launch_bounds__(640, 1)
       const int st = it % C::NS;
       const int qs = qtile_start(it);
       ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
-           __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wd)) &&
            __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
            (it < 2 ||
             __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
