@@ -1641,9 +1641,14 @@ __global__ void __launch_bounds__(640, 1)
           constexpr bool MASK = decltype(mask_c)::value;
           constexpr bool NEAR = decltype(near_c)::value;
           constexpr bool SUM = decltype(sum_c)::value;  // far-side table-gradient sum wanted
+          // bf16 P^T of every chunk, written to TMEM (the dV product's A operand) after the pass:
+          // the previous tile's dV product, queued behind this tile's S^T and dP^T, has then had
+          // time to finish reading the columns
+          uint32_t pks[QW / 16][8];
 #pragma unroll
           for (int sub = 0; sub < QW / 16; ++sub) {
-            uint32_t raw[16], dp[16], pk[8];
+            uint32_t raw[16], dp[16];
+            uint32_t (&pk)[8] = pks[sub];
             tmem_ld16_issue(tS + 16 * sub, raw);
             tmem_ld16_issue(tDP + 16 * sub, dp);
             tmem_ld16_fence(raw);
@@ -1654,21 +1659,23 @@ __global__ void __launch_bounds__(640, 1)
             }
             bwd_p_chunk<16, BIAS, MASK>(raw, pk, (BIAS >= 3 ? col4 : lse4) + 4 * sub, lut_row,
                                         c0 + 16 * sub, rowc, kq, sl, lo_j, hi_j);
-            if (sub == 0 && it >= 1) {  // the previous tile's dV product has read P^T
-              if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
-              tc_fence_after();
-            }
-            tmem_st8(tP + 8 * sub, pk);  // bf16 P^T: A operand of the dV product
+            uint32_t dsk[8];
             const float4 *d4 = dvs4 + 4 * sub;
             if (sub == 0)
-              part += bwd_ds_chunk<16, NEAR, 0, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
+              part += bwd_ds_chunk<16, NEAR, 0, SUM>(raw, dp, d4, dsk, lane, acc_a, acc_b);
             else
-              part += bwd_ds_chunk<16, NEAR, 16, SUM>(raw, dp, d4, pk, lane, acc_a, acc_b);
+              part += bwd_ds_chunk<16, NEAR, 16, SUM>(raw, dp, d4, dsk, lane, acc_a, acc_b);
 #pragma unroll
             for (int gg = 0; gg < 2; ++gg)  // groups of 8 queries = 16 bytes each
-              st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), pk[4 * gg], pk[4 * gg + 1],
-                           pk[4 * gg + 2], pk[4 * gg + 3]);
+              st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), dsk[4 * gg], dsk[4 * gg + 1],
+                           dsk[4 * gg + 2], dsk[4 * gg + 3]);
           }
+          if (it >= 1) {  // the previous tile's dV product has read P^T
+            if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int sub = 0; sub < QW / 16; ++sub) tmem_st8(tP + 8 * sub, pks[sub]);
           return true;
         };
         using B0 = std::integral_constant<int, 0>;
