@@ -858,10 +858,15 @@ __global__ void __launch_bounds__(640, 1)
       for (int it = 0; it < w.nq; ++it) {
         const int g = gs + it, st = g % C::NS;
         const int qs = qtile_start(w, it);
-        ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (g / C::NS) & 1, wd)) &&
-             __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, wd)) &&
-             (g < 2 ||
-              __all_sync(0xffffffffu, mbar_wait(ds_empty + (g & 1), ((g >> 1) - 1) & 1, wd)));
+        {  // the three phases tested at once (usually all complete), else waited for in turn
+          const uint32_t pq = (g / C::NS) & 1, pd = g & 1, pe = ((g >> 1) - 1) & 1;
+          const bool all = g >= 2 ? mbar_try_wait3(qd_full + st, pq, dp_full, pd, ds_empty + (g & 1), pe)
+                                  : mbar_try_wait2(qd_full + st, pq, dp_full, pd);
+          ok = __all_sync(0xffffffffu, all) ||
+               (__all_sync(0xffffffffu, mbar_wait(qd_full + st, pq, wd)) &&
+                __all_sync(0xffffffffu, mbar_wait(dp_full, pd, wd)) &&
+                (g < 2 || __all_sync(0xffffffffu, mbar_wait(ds_empty + (g & 1), pe, wd))));
+        }
         if (!ok) break;
         tc_fence_after();
         if (it == 0) {
@@ -1589,10 +1594,15 @@ __global__ void __launch_bounds__(640, 1)
     for (int it = 0; it < nq; ++it) {
       const int st = it % C::NS;
       const int qs = qtile_start(it);
-      ok = __all_sync(0xffffffffu, mbar_wait(qd_full + st, (it / C::NS) & 1, wd)) &&
-           __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, wd)) &&
-           (it < 2 ||
-            __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), ((it >> 1) - 1) & 1, wd)));
+      {  // the three phases tested at once (usually all complete), else waited for in turn
+        const uint32_t pq = (it / C::NS) & 1, pd = it & 1, pe = ((it >> 1) - 1) & 1;
+        const bool all = it >= 2 ? mbar_try_wait3(qd_full + st, pq, dp_full, pd, ds_empty + (it & 1), pe)
+                                 : mbar_try_wait2(qd_full + st, pq, dp_full, pd);
+        ok = __all_sync(0xffffffffu, all) ||
+             (__all_sync(0xffffffffu, mbar_wait(qd_full + st, pq, wd)) &&
+              __all_sync(0xffffffffu, mbar_wait(dp_full, pd, wd)) &&
+              (it < 2 || __all_sync(0xffffffffu, mbar_wait(ds_empty + (it & 1), pe, wd))));
+      }
       if (!ok) break;
       tc_fence_after();
       const int d0 = ks - qs - shift;  // delta of (key row 0, query column 0)

@@ -100,6 +100,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Several phases at once: the tests are issued back to back, so that their latencies overlap
+// when the phases have completed (the common case); otherwise each is waited for in turn.
+__device__ __forceinline__ bool mbar_try_wait2(uint64_t *b0, uint32_t p0, uint64_t *b1,
+                                               uint32_t p1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 b, [%3], %4;\n\t"
+      "and.pred a, a, b;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait3(uint64_t *b0, uint32_t p0, uint64_t *b1,
+                                               uint32_t p1, uint64_t *b2, uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred a, b, c;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 b, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 c, [%5], %6;\n\t"
+      "and.pred a, a, b;\n\t"
+      "and.pred a, a, c;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
 // mbar_wait for a whole converged warp, with one answer for all its lanes.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, wd));
