@@ -1550,9 +1550,10 @@ __global__ void __launch_bounds__(640, 1)
         p.bias.slopes != nullptr ? __ldg(p.bias.slopes + h) : 0.f);
     const bool has_slopes = p.bias.slopes != nullptr;
 
-    // dQ tile `it` (quarter of its 64 columns) into the fp32 accumulator
-    auto drain_dq = [&](int it) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wd))) return false;
+    // dQ tile `it` (quarter of its 64 columns) into the fp32 accumulator (`known`: its product
+    // was already seen complete, with the P^T wait of the following step)
+    auto drain_dq = [&](int it, bool known) -> bool {
+      if (!known && !__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wd))) return false;
       tc_fence_after();
       uint32_t v[16];
       tmem_ld16(tDQ, v);
@@ -1593,6 +1594,7 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int st = it % C::NS;
+      bool dq_known = false;  // the previous step's dQ product seen complete (with P^T's wait)
       const int qs = qtile_start(it);
       {  // the three phases tested at once (usually all complete), else waited for in turn
         const uint32_t pq = (it / C::NS) & 1, pd = it & 1, pe = ((it >> 1) - 1) & 1;
@@ -1680,8 +1682,10 @@ __global__ void __launch_bounds__(640, 1)
               st_shared_v4(dsb + (ds_x ^ ((2 * sub + gg) << 4)), dsk[4 * gg], dsk[4 * gg + 1],
                            dsk[4 * gg + 2], dsk[4 * gg + 3]);
           }
-          if (it >= 1) {  // the previous tile's dV product has read P^T
-            if (!__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd))) return false;
+          if (it >= 1) {  // the previous tile's dV product has read P^T; its dQ, tested with it
+            dq_known = __all_sync(0xffffffffu, mbar_try_wait2(p_free, (it - 1) & 1, dq_full, (it - 1) & 1));
+            if (!dq_known && !__all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, wd)))
+              return false;
             tc_fence_after();
           }
 #pragma unroll
@@ -1728,12 +1732,12 @@ __global__ void __launch_bounds__(640, 1)
       fence_proxy_async_smem();
       mbar_arrive(ds_ready);
       // ---- the previous tile's dQ (its product was issued after this tile's S^T and dP^T)
-      if (it >= 1 && !drain_dq(it - 1)) {
+      if (it >= 1 && !drain_dq(it - 1, dq_known)) {
         ok = false;
         break;
       }
     }
-    if (ok && nq >= 1) ok = drain_dq(nq - 1);
+    if (ok && nq >= 1) ok = drain_dq(nq - 1, false);
     if (C::DQ_TMA && lane == 0) bulk_wait_all();  // reductions complete before shared memory is released
     grid_dep_launch();  // the finishing grid may be scheduled
     // ---- dK, dV: this warpgroup's quarter of the channels
