@@ -687,8 +687,7 @@ __global__ void __launch_bounds__(640, 1)
             // once these complete
             if (it + 1 < w.nq) {
               const int gn = g + 1;
-              if (!warp_wait(s_consumed, g & 1, wd) ||
-                  !warp_wait(qd_full + gn % C::NS, (gn / C::NS) & 1, wd)) {
+              if (!warp_wait2(s_consumed, g & 1, qd_full + gn % C::NS, (gn / C::NS) & 1, wd)) {
                 ok = false;
                 break;
               }
@@ -731,8 +730,8 @@ __global__ void __launch_bounds__(640, 1)
         do {
           for (int it = 0; ok && it < w.nq; ++it) {
             const int g = gs + it;
-            if (!warp_wait(ds_ready, g & 1, wd) ||
-                (g >= 1 && !warp_wait(dq_empty, (g - 1) & 1, wd))) {
+            if (g >= 1 ? !warp_wait2(ds_ready, g & 1, dq_empty, (g - 1) & 1, wd)
+                       : !warp_wait(ds_ready, g & 1, wd)) {
               ok = false;
               break;
             }

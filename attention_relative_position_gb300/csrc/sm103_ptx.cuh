@@ -137,6 +137,12 @@ __device__ __forceinline__ bool mbar_try_wait3(uint64_t *b0, uint32_t p0, uint64
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, wd));
 }
+// Two phases for a whole warp: tested at once, else waited for in turn.
+__device__ __forceinline__ bool warp_wait2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
+                                           const Watchdog &wd) {
+  if (__all_sync(0xffffffffu, mbar_try_wait2(b0, p0, b1, p1))) return true;
+  return warp_wait(b0, p0, wd) && warp_wait(b1, p1, wd);
+}
 
 // Wait used during teardown: ignores the abort flag, gives up silently after limit_ns.
 __device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parity,
