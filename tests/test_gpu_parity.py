@@ -39,6 +39,13 @@ SMALL = [
       False, False, 0.5, seed=22),
     W("t5dec_many_docs_causal_d64", (200,) * 16 + (1,) * 4 + (383,), 3, 64, 1.0,
       (32, 128, False), False, True, 0.5, seed=23),
+    # documents of different lengths past the persistent backward's longest-first limits, so
+    # that it falls back to the round-robin order: more (key tile, document) groups than the
+    # sort takes, and (20000 items on one CTA per SM) more rounds per CTA than its list holds
+    W("t5enc_many_tiny_docs_d64", tuple([1, 2, 17, 5, 30, 9, 3, 16] * 1100), 1, 64, 1.0,
+      (32, 128, True), False, False, 0.3, seed=41),
+    W("t5dec_many_short_docs_heads_d64", tuple([20, 3, 33, 9] * 625), 8, 64, 1.0,
+      (32, 128, False), False, True, 0.3, seed=42),
     # documents of at most 8 tokens: the forward takes the few-row kernel (rows = the
     # document's queries), the backward the tiled kernels
     W("tiny_docs_t5_alibi_causal_d64", (1, 3, 8, 2, 5, 0, 7, 8, 4), 4, 64, 1.0,
