@@ -89,7 +89,10 @@ typedef struct {
  * max_distance > nbh/2) and the ALiBi term (when alibi_slopes is not NULL). Both NULL gives
  * plain attention. lse may be NULL if the caller does not need it (the backward needs it).
  * FAT_EUNSUPPORTED: the bucket layout needs a larger in-kernel lookup table than shared memory
- * holds (saturation distance above about 3800 for head_dim 64 / 2800 for head_dim 128).
+ * holds. The table has sat_pos + sat_neg + 507 entries (sat_neg = the saturation distance of
+ * fat_attn_bucket_thresholds, sat_pos = the same when bidirectional, else 0); the forward takes
+ * up to 24687 entries at head_dim 64 and 8303 at head_dim 128 (32 buckets, bidirectional:
+ * max_distance up to 34404 / 9436).
  */
 int fat_attn_fwd(const fat_shape_t *shape, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,
@@ -136,6 +139,9 @@ size_t fat_attn_bwd_workspace_size(const fat_shape_t *shape);
  * It enqueues the three stages below; the second and third are launched as programmatic
  * dependents of the grid before them (each is scheduled while that grid drains and waits for
  * its outputs inside the kernel), which the stage-by-stage calls do not do.
+ * FAT_EUNSUPPORTED: the lookup table (entries as for the forward), with its per-delta gradient
+ * sums, does not fit next to the backward's tiles: up to 3083 entries at head_dim 64 and 6951
+ * at head_dim 128 (32 buckets, bidirectional: max_distance up to 2661 / 7590).
  */
 int fat_attn_bwd(const fat_shape_t *shape, const void *q, const void *k, const void *v,
                  const float *bias_table, int num_buckets, int max_distance, int bidirectional,

@@ -154,6 +154,34 @@ def test_bwd_argument_errors(lib):
     assert bwd(d=80) == -2
 
 
+def _bwd_table(lib, d, md):
+    sh = _shape(d=d)
+    need = lib.fat_attn_bwd_workspace_size(ctypes.byref(sh))
+    return lib.fat_attn_bwd(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, 32, md, 1, None, FAKE, 0,
+                            1.0, FAKE, FAKE, FAKE, FAKE, need, FAKE, FAKE, FAKE, FAKE)
+
+
+def test_lookup_table_limits_rejected(lib):
+    # the first bucket layouts (32 buckets, bidirectional) past the table sizes the header
+    # states are rejected before anything touches the device
+    assert _fwd(lib, _shape(d=64), table=FAKE, nb=32, md=34405, bidir=1) == -5
+    assert _fwd(lib, _shape(d=128), table=FAKE, nb=32, md=9437, bidir=1) == -5
+    assert _bwd_table(lib, 64, 2662) == -5
+    assert _bwd_table(lib, 128, 7591) == -5
+    for md, entries in ((34404, 24687), (9436, 8303), (2661, 3083), (7590, 6951)):
+        sat = fa.fat_attn_bucket_thresholds(32, md, True)[1]
+        assert 2 * sat + 507 == entries
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU path")
+def test_lookup_table_limits_accepted(lib):
+    # the largest layouts pass the host checks; the first CUDA call then fails (no GPU)
+    assert _fwd(lib, _shape(d=64), table=FAKE, nb=32, md=34404, bidir=1) == -4
+    assert _fwd(lib, _shape(d=128), table=FAKE, nb=32, md=9436, bidir=1) == -4
+    assert _bwd_table(lib, 64, 2661) == -4
+    assert _bwd_table(lib, 128, 7590) == -4
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     # host validation passes, the first CUDA call fails: an error code, no crash

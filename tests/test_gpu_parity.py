@@ -46,6 +46,13 @@ SMALL = [
       (32, 128, True), False, False, 0.3, seed=41),
     W("t5dec_many_short_docs_heads_d64", tuple([20, 3, 33, 9] * 625), 8, 64, 1.0,
       (32, 128, False), False, True, 0.3, seed=42),
+    # bucket layouts with large lookup tables: at head_dim 128 the backward drops to two Q/dO
+    # stages (4265 entries), at head_dim 64 the table nearly fills the backward's shared memory
+    # (3031 of at most 3083 entries)
+    W("t5_bidir_big_table_d128", (700, 300), 2, 128, 1.0, (32, 4096, True), False, False, 0.3,
+      seed=43),
+    W("t5_bidir_big_table_d64", (900, 200), 2, 64, 1.0, (32, 2600, True), False, False, 0.3,
+      seed=44),
     # documents of at most 8 tokens: the forward takes the few-row kernel (rows = the
     # document's queries), the backward the tiled kernels
     W("tiny_docs_t5_alibi_causal_d64", (1, 3, 8, 2, 5, 0, 7, 8, 4), 4, 64, 1.0,
