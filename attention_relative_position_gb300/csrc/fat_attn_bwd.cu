@@ -1125,7 +1125,7 @@ __global__ void __launch_bounds__(640, 1)
               red_add(p.dbias + (size_t)b * H + w.h, x);
           }
         }
-        if (new_head) {  // same arithmetic as the set-up's table (bias_log2_bucket_dev)
+        if (new_head) {  // same arithmetic as the set-up's table (bias_log2_staged)
           for (int i = tid; i < p.bias.lut_len; i += C::NCOMP) {
             const int delta = p.bias.lut_lo + i;
             float x = 0.f;

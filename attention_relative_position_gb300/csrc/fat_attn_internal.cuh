@@ -191,24 +191,11 @@ __device__ __forceinline__ int t5_bucket_dev(int delta, const BiasParams &b) {
   return off + b.me + t;
 }
 
-// Bias of relative position `delta` (whose T5 bucket is `bucket`) for head h, in log2 units
-// (natural bias * log2(e)).
-__device__ __forceinline__ float bias_log2_bucket_dev(int bucket, int delta, int h, int H,
-                                                      const BiasParams &b) {
-  float v = 0.f;
-  if (b.table) v += __ldg(b.table + (size_t)bucket * H + h);
-  if (b.slopes) v -= __ldg(b.slopes + h) * (float)(delta < 0 ? -delta : delta);
-  return v * kLog2e;
-}
-__device__ __forceinline__ float bias_log2_dev(int delta, int h, int H, const BiasParams &b) {
-  return bias_log2_bucket_dev(b.table ? t5_bucket_dev(delta, b) : 0, delta, h, H, b);
-}
-
 // Building a block's bias table over delta without a global load per entry: the thresholds and
 // head h's table column are first staged in shared memory (bias_stage, one load per value, all
 // in flight together), then each entry's bucket is a binary search over the staged thresholds
-// (the same integer function as t5_bucket_dev: the count of thresholds <= n) and its bias the
-// same arithmetic as bias_log2_bucket_dev.
+// (the same integer function as t5_bucket_dev: the count of thresholds <= n) and its bias, in
+// log2 units, (table[bucket, h] - slope_h |delta|) log2(e) (bias_log2_staged).
 __device__ __forceinline__ void bias_stage(const BiasParams &b, int h, int H, int *thr_s,
                                            float *col_s, int tid, int nthreads) {
   for (int i = tid; i < b.n_thr; i += nthreads) thr_s[i] = b.thr[i];
@@ -247,21 +234,9 @@ __device__ __forceinline__ float bias_log2_staged(int bucket, int delta, float s
 struct FarBias {
   float c_pos, k_pos, c_neg, k_neg;
 };
-__device__ __forceinline__ FarBias far_bias_dev(int h, int H, const BiasParams &b) {
-  FarBias f{0.f, 0.f, 0.f, 0.f};
-  if (b.table) {
-    f.c_pos = __ldg(b.table + (size_t)t5_bucket_dev(b.sat_pos, b) * H + h) * kLog2e;
-    f.c_neg = __ldg(b.table + (size_t)t5_bucket_dev(-b.sat_neg, b) * H + h) * kLog2e;
-  }
-  if (b.slopes) {
-    const float s = __ldg(b.slopes + h) * kLog2e;
-    f.k_pos = -s;
-    f.k_neg = s;
-  }
-  return f;
-}
 
-// far_bias_dev from the staged thresholds and table column (no global load but the slope's)
+// Each side's constant (the table entry of the saturated bucket) and slope term, from the staged
+// thresholds and table column (no global load but the slope's)
 __device__ __forceinline__ FarBias far_bias_staged(const BiasParams &b, const int *thr_s,
                                                    const float *col_s, float slope) {
   FarBias f{0.f, 0.f, 0.f, 0.f};
