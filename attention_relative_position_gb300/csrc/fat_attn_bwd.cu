@@ -25,8 +25,9 @@
 //                TMEM, dK and dV for the whole walk.
 // Bias gradient: tiles beyond the T5 saturation distance add dS into one register per side;
 // the other tiles reduce each 32-row block along its diagonals with warp shuffles and add the
-// sums into a shared-memory array indexed by delta; at the end the CTA folds deltas into
-// buckets (segmented warp scan) and adds each run once into the global table gradient.
+// sums into a shared-memory array indexed by delta; at the end of each item the CTA folds
+// deltas into buckets (segmented warp scan) and adds each run once into the global table
+// gradient.
 // Query tiles are 128 wide for d = 64 and 64 wide for d = 128 so that S, dP, dQ, P, dK and dV
 // fit the 512 TMEM columns together.
 #include <algorithm>
